@@ -1,0 +1,247 @@
+/*
+ * lora_sgmv.h -- C ABI of the GB300 multi-LoRA delta path (Punica-style
+ * segmented gather matrix-vector / matrix multiplication, "SGMV").
+ *
+ * The path computes, for a batch of M token rows where row i carries an
+ * adapter slot ids[i] in a contiguous adapter pool,
+ *
+ *     y[i, :] += s_a * (x[i, :] . A[a]^T) . B[a]^T        a = ids[i]
+ *
+ * (unmerged LoRA delta with its alpha/r scaling: "vLLM-Ascend LoRA"
+ * article, section 1.1; the per-token routing through a weight pool:
+ * "09. Triton Fused LoRA", Steps 1-3; the segmented form
+ * Y = X W + (x1 A1 B1, ..., xn An Bn): "III.Punica: Multi-Tenant LoRA
+ * Serving", section SGMV).  The base product X W is not part of this
+ * library; y holds it on entry.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Every pointer argument named as "device" is a CUDA device pointer; the
+ *    library never allocates, frees or synchronises.  All work is enqueued
+ *    on `stream` (a cudaStream_t passed as void*; NULL = legacy default
+ *    stream) and runs asynchronously.  The caller owns every buffer and
+ *    must keep it alive until the stream has finished the call.
+ *  - Element types: LORA_F32 or LORA_BF16.  x, the pools and y share one
+ *    type; the intermediate h is always fp32; accumulation is always fp32.
+ *    fp32 inputs are computed with fp32 FMA only (no reduced-precision
+ *    tensor math).
+ *  - Layouts (element strides; the innermost dimension is contiguous):
+ *      x       [M][ldx]                      row i = token i
+ *      A pool  [n_adapters][r_max][d_in]     rows of A[a] at a_stride_r,
+ *                                            adapters at a_stride_adapter
+ *      B pool  [n_adapters][d_out][r_max]    per output slice
+ *      y       [M][ldy]                      updated in place (+=)
+ *      h       [M][ldh]  fp32                indexed by token row
+ *    ("09. Triton Fused LoRA", Step 1: lora_a_pool is (num_loras, r,
+ *    in_features); its test builds lora_b_pool as (num_loras, out, r).)
+ *  - Alignment: every base pointer 16-byte aligned; every row stride a
+ *    multiple of 16 bytes; d_in, every slice's d_out and y column offset
+ *    multiples of 8 (bf16) or 4 (fp32) elements.
+ *  - Rows whose id is -1 carry no adapter and are left bit-identical.  Ids
+ *    outside [-1, n_adapters) are treated the same way and counted on the
+ *    device (LORA_COUNT_INVALID).  Nothing traps.
+ *  - Mixed ranks: with a rank table ranks[a] (device, may be NULL = every
+ *    adapter has rank r_max), adapter a uses rows [0, ranks[a]) of A[a] and
+ *    columns [0, ranks[a]) of B[a]; the padding up to r_max is never read
+ *    into a result ("vLLM-Ascend LoRA" article, section 3.4).  A rank
+ *    outside [0, r_max] skips that adapter's rows and sets
+ *    LORA_DEVERR_RANK in the batch counters.
+ *  - Scale: s_a = adapter_scale[a] when adapter_scale (device, fp32,
+ *    n_adapters entries) is non-NULL, else `scale`.  It is applied exactly
+ *    once, to the fp32 intermediate ("vLLM-Ascend LoRA" article, sections
+ *    2.1 and 3.3: alpha/r is kept apart from the weights and multiplied in
+ *    once, as (tmp * scale) . B^T).
+ *  - y is rounded once: fp32(y) + delta, converted to y's type (round to
+ *    nearest even).
+ *
+ * Errors: every call returns lora_status_t.  Host-side argument checks
+ * return LORA_ERR_INVALID / LORA_ERR_UNSUPPORTED / LORA_ERR_WORKSPACE
+ * before anything is enqueued; a failed kernel launch returns
+ * LORA_ERR_CUDA.  lora_last_error_string() describes the last failure on
+ * the calling thread.  Conditions only the device can see are reported
+ * through the batch's device counters (see LORA_COUNT_*), never by a trap.
+ */
+#ifndef LORA_SGMV_H
+#define LORA_SGMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int lora_status_t;
+
+#define LORA_OK 0
+#define LORA_ERR_INVALID (-1)     /* a null pointer, negative size, bad stride */
+#define LORA_ERR_UNSUPPORTED (-2) /* dtype, alignment or size outside the support */
+#define LORA_ERR_WORKSPACE (-3)   /* workspace smaller than lora_workspace_size() */
+#define LORA_ERR_CUDA (-4)        /* a CUDA call or kernel launch failed */
+
+#define LORA_F32 0
+#define LORA_BF16 1
+
+/* Path selection for lora_delta / lora_shrink / lora_expand. */
+#define LORA_PATH_AUTO 0      /* segments with >= tc_min_rows rows use tensor cores (bf16) */
+#define LORA_PATH_CUDA_CORE 1 /* every segment on CUDA-core dot products */
+#define LORA_PATH_TENSOR 2    /* every segment on tcgen05 tensor cores (bf16 only) */
+
+/* Largest supported sizes. */
+#define LORA_MAX_TOKENS (1 << 24)
+#define LORA_MAX_RANK 128
+#define LORA_MAX_SLICES 4
+
+/* Device counters written by lora_prepare_batch (int32 each, in order). */
+#define LORA_COUNT_SEGS 0       /* number of segments S */
+#define LORA_COUNT_ACTIVE 1     /* rows with a valid adapter */
+#define LORA_COUNT_INVALID 2    /* rows whose id is outside [-1, n_adapters) */
+#define LORA_COUNT_SMALL_SEGS 3 /* segments with fewer than tc_min_rows rows */
+#define LORA_COUNT_TC_SEGS 4    /* segments with at least tc_min_rows rows */
+#define LORA_COUNT_TC_ROWS 5    /* rows inside those segments */
+#define LORA_COUNT_DEVERR 6     /* bit set of LORA_DEVERR_* raised by later calls */
+#define LORA_COUNT_GROUPS 7     /* distinct adapters in the batch */
+#define LORA_NUM_COUNTS 8
+
+#define LORA_DEVERR_RANK 1 /* an adapter's rank was outside [0, r_max] */
+#define LORA_DEVERR_WAIT 2 /* a bounded device wait gave up (result incomplete) */
+
+/*
+ * Segment metadata of one batch, built on the device by lora_prepare_batch
+ * (token regrouping of "III.Punica: Multi-Tenant LoRA Serving", section
+ * 代码: weight_indices, seg_lens, seg_indptr, sorted_token_ids).
+ *
+ * Device arrays (all int32, inside the caller's workspace):
+ *   sorted_token_ids[M]     token rows grouped by adapter; the first
+ *                           counts[LORA_COUNT_ACTIVE] entries are valid
+ *   seg_indptr[max_segs+1]  start of segment s in sorted_token_ids
+ *   seg_lens[max_segs]      rows in segment s (> 0)
+ *   weight_indices[max_segs] adapter slot of segment s
+ *   small_segs[max_segs]    ids of segments with < tc_min_rows rows
+ *   tc_segs[max_segs]       ids of segments with >= tc_min_rows rows
+ *   tc_indptr[max_segs+1]   prefix sum of rows over tc_segs
+ *   counts[LORA_NUM_COUNTS] see LORA_COUNT_*
+ * Host fields describe the batch the metadata was built for.
+ */
+typedef struct lora_batch {
+    int32_t *sorted_token_ids;
+    int32_t *seg_indptr;
+    int32_t *seg_lens;
+    int32_t *weight_indices;
+    int32_t *small_segs;
+    int32_t *tc_segs;
+    int32_t *tc_indptr;
+    int32_t *counts;
+    int32_t M;           /* token rows */
+    int32_t n_adapters;  /* pool size the ids index into */
+    int32_t chunk_size;  /* 0 = one segment per adapter group */
+    int32_t max_segs;    /* capacity of the segment arrays */
+    int32_t tc_min_rows; /* tensor-core row threshold used for the split */
+    uint32_t magic;      /* set by lora_prepare_batch */
+} lora_batch_t;
+
+/* One output slice of the expand step: B pool and the y columns it writes
+ * (a fused projection such as QKV keeps one B pool per slice). */
+typedef struct lora_b_slice {
+    const void *B_pool;     /* device, [n_adapters][d_out][>= r_max] */
+    int64_t stride_adapter; /* elements between adapters, >= d_out * stride_n */
+    int64_t stride_n;       /* elements between rows, >= r_max */
+    int32_t d_out;          /* rows of this slice */
+    int32_t y_col;          /* first y column written by this slice */
+} lora_b_slice_t;
+
+/*
+ * Workspace bytes lora_prepare_batch needs for a batch of M rows over a
+ * pool of n_adapters with the given chunk size (0 = no chunking).  Returns
+ * 0 when an argument is out of range.
+ */
+size_t lora_workspace_size(int32_t M, int32_t n_adapters, int32_t chunk_size);
+
+/*
+ * Build segment metadata on the device, with no host synchronisation.
+ *
+ * ids          device int32[M]: adapter slot per token row, -1 = none.
+ * M            rows, 0 <= M <= LORA_MAX_TOKENS.
+ * n_adapters   pool size, >= 1.
+ * chunk_size   0: one segment per adapter group; > 0: every group is cut
+ *              into segments of chunk_size rows, the last one shorter
+ *              ("III.Punica: Multi-Tenant LoRA Serving", section 代码:
+ *              the regrouped token stream is cut into fixed-size chunks,
+ *              each a logical segment with its own adapter).
+ * tc_min_rows  segments with at least this many rows go to the tensor-core
+ *              kernel under LORA_PATH_AUTO ("vLLM-Ascend LoRA" article,
+ *              section 4.1: blocks below a row threshold use vector dot
+ *              products); <= 0 selects the library default.
+ * workspace    device buffer of >= lora_workspace_size(M, n_adapters,
+ *              chunk_size) bytes, 256-byte aligned; owned by the caller and
+ *              referenced by *batch until the batch is no longer used.
+ * batch        host struct filled with pointers into workspace.
+ *
+ * Grouping rule: adapter groups appear in the order in which their adapter
+ * first occurs among the rows; rows inside a group keep ascending row
+ * order (the Punica page's example: ids 2 2 2 5 5 1 1 give
+ * seg_indptr = [0, 3, 5, 7]).  Rows with id -1 or an out-of-range id are
+ * in no segment.
+ */
+lora_status_t lora_prepare_batch(const int32_t *ids, int32_t M, int32_t n_adapters,
+                                 int32_t chunk_size, int32_t tc_min_rows,
+                                 void *workspace, size_t workspace_bytes,
+                                 lora_batch_t *batch, void *stream);
+
+/*
+ * Shrink: h[i, j] = sum_k x[i, k] * A[a, j, k] for j < r_a, and 0 for
+ * r_a <= j < r_max, for every row i in a segment (unscaled; "vLLM-Ascend
+ * LoRA" article, section 3.2: first project d_in down to r).  Rows in no
+ * segment keep their h contents.  h: device fp32 [M][ldh], ldh >= r_max.
+ */
+lora_status_t lora_shrink(const lora_batch_t *batch, int32_t dtype,
+                          const void *x, int64_t ldx, int32_t d_in,
+                          const void *A_pool, int64_t a_stride_adapter,
+                          int64_t a_stride_r, int32_t r_max,
+                          const int32_t *ranks, float *h, int64_t ldh,
+                          int32_t path, void *stream);
+
+/*
+ * Expand: y[i, y_col_t + n] += s_a * sum_{j < r_a} h[i, j] * B_t[a, n, j]
+ * for every row i in a segment and every slice t ("vLLM-Ascend LoRA"
+ * article, section 3.3: delta = (tmp * scale) . B^T added into out).
+ * slices: host array of n_slices (1..LORA_MAX_SLICES) descriptors.
+ */
+lora_status_t lora_expand(const lora_batch_t *batch, int32_t dtype,
+                          const float *h, int64_t ldh, int32_t r_max,
+                          const lora_b_slice_t *slices, int32_t n_slices,
+                          const int32_t *ranks, float scale,
+                          const float *adapter_scale, void *y, int64_t ldy,
+                          int32_t path, void *stream);
+
+/*
+ * Fused delta: shrink, scale and expand in one pass; the M x r
+ * intermediate stays in registers, shared memory or tensor memory and is
+ * never written to global memory ("vLLM-Ascend LoRA" article, section 4.3).
+ * Arguments as for lora_shrink and lora_expand.
+ */
+lora_status_t lora_delta(const lora_batch_t *batch, int32_t dtype,
+                         const void *x, int64_t ldx, int32_t d_in,
+                         const void *A_pool, int64_t a_stride_adapter,
+                         int64_t a_stride_r, int32_t r_max,
+                         const lora_b_slice_t *slices, int32_t n_slices,
+                         const int32_t *ranks, float scale,
+                         const float *adapter_scale, void *y, int64_t ldy,
+                         int32_t path, void *stream);
+
+/* Description of the last failure on the calling thread ("" if none). */
+const char *lora_last_error_string(void);
+
+/* ABI version of this library (major * 100 + minor). */
+int32_t lora_abi_version(void);
+
+/* Number of kernel launches this library has enqueued in this process (a
+ * diagnostic; launches captured into a CUDA graph are counted once, at
+ * capture). */
+int64_t lora_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LORA_SGMV_H */

@@ -1,0 +1,301 @@
+"""Thin Python binding of the C ABI in ``include/lora_sgmv.h``.
+
+Argument marshalling only: every step of the path runs in the CUDA library.
+PyTorch supplies device memory and the current stream.  The binding raises
+if the library has not been built (``segmented_gather_gemv_gb300.build``)
+or if a call returns an error status; there is no fallback.
+
+Calls (same names as the C ABI):
+  lora_workspace_size(M, n_adapters, chunk_size) -> int
+  lora_prepare_batch(ids, n_adapters, chunk_size=0, tc_min_rows=0) -> Batch
+  lora_shrink(batch, x, A_pool, h=None, ranks=None, path=PATH_AUTO) -> h
+  lora_expand(batch, h, B_pools, y, scale=1.0, adapter_scale=None,
+              ranks=None, y_cols=None, path=PATH_AUTO) -> y
+  lora_delta(batch, x, A_pool, B_pools, y, scale=1.0, adapter_scale=None,
+             ranks=None, y_cols=None, path=PATH_AUTO) -> y
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Sequence
+
+import torch
+
+from . import build as _build
+
+LORA_OK = 0
+LORA_ERR_INVALID = -1
+LORA_ERR_UNSUPPORTED = -2
+LORA_ERR_WORKSPACE = -3
+LORA_ERR_CUDA = -4
+F32, BF16 = 0, 1
+PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR = 0, 1, 2
+MAX_SLICES = 4
+COUNT_NAMES = ("num_segs", "num_active", "num_invalid", "num_small_segs",
+               "num_tc_segs", "tc_rows", "device_error", "num_groups")
+DEVERR_RANK, DEVERR_WAIT = 1, 2
+
+_STATUS = {LORA_ERR_INVALID: "invalid argument", LORA_ERR_UNSUPPORTED: "unsupported",
+           LORA_ERR_WORKSPACE: "workspace too small", LORA_ERR_CUDA: "CUDA error"}
+
+
+class LoraError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__("%s (%d): %s" % (_STATUS.get(status, "error"), status, msg))
+        self.status = status
+
+
+class _Batch(ctypes.Structure):
+    _fields_ = [("sorted_token_ids", ctypes.c_void_p), ("seg_indptr", ctypes.c_void_p),
+                ("seg_lens", ctypes.c_void_p), ("weight_indices", ctypes.c_void_p),
+                ("small_segs", ctypes.c_void_p), ("tc_segs", ctypes.c_void_p),
+                ("tc_indptr", ctypes.c_void_p), ("counts", ctypes.c_void_p),
+                ("M", ctypes.c_int32), ("n_adapters", ctypes.c_int32),
+                ("chunk_size", ctypes.c_int32), ("max_segs", ctypes.c_int32),
+                ("tc_min_rows", ctypes.c_int32), ("magic", ctypes.c_uint32)]
+
+
+class _BSlice(ctypes.Structure):
+    _fields_ = [("B_pool", ctypes.c_void_p), ("stride_adapter", ctypes.c_int64),
+                ("stride_n", ctypes.c_int64), ("d_out", ctypes.c_int32),
+                ("y_col", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    "CUDA library %s is missing: build it with "
+                    "`python -m segmented_gather_gemv_gb300.build`" % path)
+            L = ctypes.CDLL(path)
+            vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+            L.lora_workspace_size.restype = ctypes.c_size_t
+            L.lora_workspace_size.argtypes = [i32, i32, i32]
+            L.lora_prepare_batch.restype = ctypes.c_int
+            L.lora_prepare_batch.argtypes = [vp, i32, i32, i32, i32, vp, ctypes.c_size_t,
+                                             ctypes.POINTER(_Batch), vp]
+            L.lora_shrink.restype = ctypes.c_int
+            L.lora_shrink.argtypes = [ctypes.POINTER(_Batch), i32, vp, i64, i32, vp, i64, i64,
+                                      i32, vp, vp, i64, i32, vp]
+            L.lora_expand.restype = ctypes.c_int
+            L.lora_expand.argtypes = [ctypes.POINTER(_Batch), i32, vp, i64, i32,
+                                      ctypes.POINTER(_BSlice), i32, vp, ctypes.c_float, vp, vp,
+                                      i64, i32, vp]
+            L.lora_delta.restype = ctypes.c_int
+            L.lora_delta.argtypes = [ctypes.POINTER(_Batch), i32, vp, i64, i32, vp, i64, i64, i32,
+                                     ctypes.POINTER(_BSlice), i32, vp, ctypes.c_float, vp, vp,
+                                     i64, i32, vp]
+            L.lora_last_error_string.restype = ctypes.c_char_p
+            L.lora_last_error_string.argtypes = []
+            L.lora_abi_version.restype = ctypes.c_int32
+            L.lora_launch_count.restype = ctypes.c_int64
+            _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != LORA_OK:
+        msg = lib().lora_last_error_string().decode(errors="replace")
+        raise LoraError(status, msg)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError("unsupported dtype %s (float32 or bfloat16)" % t.dtype)
+
+
+def _dev_ptr(t: Optional[torch.Tensor], what: str, dtype=None) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % what)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s" % (what, dtype))
+    return t.data_ptr()
+
+
+def _inner_contig(t: torch.Tensor, what: str):
+    if t.dim() < 1 or t.stride(-1) != 1:
+        raise ValueError("%s must have a contiguous last dimension" % what)
+
+
+class Batch:
+    """Device segment metadata of one batch (wraps ``lora_batch_t``).
+
+    Holds a reference to its workspace, which must stay alive while the
+    batch is used."""
+
+    def __init__(self, raw: _Batch, workspace: torch.Tensor, ids: torch.Tensor):
+        self.raw = raw
+        self.workspace = workspace
+        self.ids = ids
+
+    @property
+    def M(self) -> int:
+        return self.raw.M
+
+    @property
+    def max_segs(self) -> int:
+        return self.raw.max_segs
+
+    def _view(self, field: str, n: int) -> torch.Tensor:
+        base = self.workspace.data_ptr()
+        off = getattr(self.raw, field) - base
+        assert off % 4 == 0 and off >= 0
+        flat = self.workspace.view(torch.int32)
+        return flat[off // 4: off // 4 + n]
+
+    def counts(self) -> dict:
+        """Device counters (synchronises with the current stream)."""
+        c = self._view("counts", len(COUNT_NAMES)).cpu().tolist()
+        return dict(zip(COUNT_NAMES, c))
+
+    def arrays(self) -> dict:
+        """Copies of the device arrays, trimmed to their valid lengths."""
+        c = self.counts()
+        S, act = c["num_segs"], c["num_active"]
+        return {
+            "sorted_token_ids": self._view("sorted_token_ids", act).cpu(),
+            "seg_indptr": self._view("seg_indptr", S + 1).cpu(),
+            "seg_lens": self._view("seg_lens", S).cpu(),
+            "weight_indices": self._view("weight_indices", S).cpu(),
+            "small_segs": self._view("small_segs", c["num_small_segs"]).cpu(),
+            "tc_segs": self._view("tc_segs", c["num_tc_segs"]).cpu(),
+            "tc_indptr": self._view("tc_indptr", c["num_tc_segs"] + 1).cpu(),
+            **c,
+        }
+
+
+def lora_launch_count() -> int:
+    """Kernel launches the library has enqueued in this process."""
+    return int(lib().lora_launch_count())
+
+
+def lora_workspace_size(M: int, n_adapters: int, chunk_size: int = 0) -> int:
+    return int(lib().lora_workspace_size(int(M), int(n_adapters), int(chunk_size)))
+
+
+def lora_prepare_batch(ids: torch.Tensor, n_adapters: int, chunk_size: int = 0,
+                       tc_min_rows: int = 0, workspace: Optional[torch.Tensor] = None,
+                       stream=None) -> Batch:
+    """Build segment metadata on the device for per-token adapter ids."""
+    if ids.dim() != 1:
+        raise ValueError("ids must be 1-D")
+    M = ids.shape[0]
+    ids_ptr = _dev_ptr(ids, "ids", torch.int32) if M else (ids.data_ptr() or None)
+    if M and not ids.is_contiguous():
+        raise ValueError("ids must be contiguous")
+    need = lora_workspace_size(M, n_adapters, chunk_size)
+    if need == 0:
+        raise LoraError(LORA_ERR_INVALID, "bad batch size arguments")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=ids.device if M else "cuda")
+    raw = _Batch()
+    _check(lib().lora_prepare_batch(ids_ptr, M, int(n_adapters), int(chunk_size), int(tc_min_rows),
+                                    workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                    ctypes.byref(raw), _stream(stream)))
+    return Batch(raw, workspace, ids)
+
+
+def _slices(B_pools, y: torch.Tensor, y_cols, r_max: int, dtype):
+    if isinstance(B_pools, torch.Tensor):
+        B_pools = [B_pools]
+    B_pools = list(B_pools)
+    if not 1 <= len(B_pools) <= MAX_SLICES:
+        raise ValueError("1..%d B pools" % MAX_SLICES)
+    arr = (_BSlice * len(B_pools))()
+    col = 0
+    for t, B in enumerate(B_pools):
+        if B.dim() != 3 or B.dtype != dtype:
+            raise ValueError("B pool %d must be (n, d_out, r_max) of the input dtype" % t)
+        _inner_contig(B, "B pool")
+        arr[t].B_pool = _dev_ptr(B, "B pool")
+        arr[t].stride_adapter = B.stride(0)
+        arr[t].stride_n = B.stride(1)
+        arr[t].d_out = B.shape[1]
+        arr[t].y_col = int(y_cols[t]) if y_cols is not None else col
+        col += B.shape[1]
+    return arr, len(B_pools)
+
+
+def _ranks_scale(ranks, adapter_scale):
+    rp = _dev_ptr(ranks, "ranks", torch.int32)
+    sp = _dev_ptr(adapter_scale, "adapter_scale", torch.float32)
+    return rp, sp
+
+
+def lora_shrink(batch: Batch, x: torch.Tensor, A_pool: torch.Tensor,
+                h: Optional[torch.Tensor] = None, ranks: Optional[torch.Tensor] = None,
+                path: int = PATH_AUTO, stream=None) -> torch.Tensor:
+    """h[i, :r] = x[i] . A[id_i]^T (fp32, unscaled) for rows in a segment."""
+    _inner_contig(x, "x")
+    _inner_contig(A_pool, "A_pool")
+    n, r_max, d_in = A_pool.shape
+    if h is None:
+        h = torch.zeros((batch.M, r_max), dtype=torch.float32, device=x.device)
+    _inner_contig(h, "h")
+    rp, _ = _ranks_scale(ranks, None)
+    _check(lib().lora_shrink(ctypes.byref(batch.raw), _dtype_code(x), _dev_ptr(x, "x"), x.stride(0),
+                             d_in, _dev_ptr(A_pool, "A_pool", x.dtype), A_pool.stride(0),
+                             A_pool.stride(1), r_max, rp, _dev_ptr(h, "h", torch.float32),
+                             h.stride(0), int(path), _stream(stream)))
+    return h
+
+
+def lora_expand(batch: Batch, h: torch.Tensor, B_pools, y: torch.Tensor, scale: float = 1.0,
+                adapter_scale: Optional[torch.Tensor] = None,
+                ranks: Optional[torch.Tensor] = None, y_cols: Optional[Sequence[int]] = None,
+                path: int = PATH_AUTO, stream=None) -> torch.Tensor:
+    """y[i, slice] += s_id * h[i] . B_id^T for rows in a segment (in place)."""
+    _inner_contig(h, "h")
+    _inner_contig(y, "y")
+    r_max = (B_pools if isinstance(B_pools, torch.Tensor) else B_pools[0]).shape[2]
+    arr, ns = _slices(B_pools, y, y_cols, r_max, y.dtype)
+    rp, sp = _ranks_scale(ranks, adapter_scale)
+    _check(lib().lora_expand(ctypes.byref(batch.raw), _dtype_code(y), _dev_ptr(h, "h", torch.float32),
+                             h.stride(0), r_max, arr, ns, rp, float(scale), sp, _dev_ptr(y, "y"),
+                             y.stride(0), int(path), _stream(stream)))
+    return y
+
+
+def lora_delta(batch: Batch, x: torch.Tensor, A_pool: torch.Tensor, B_pools, y: torch.Tensor,
+               scale: float = 1.0, adapter_scale: Optional[torch.Tensor] = None,
+               ranks: Optional[torch.Tensor] = None, y_cols: Optional[Sequence[int]] = None,
+               path: int = PATH_AUTO, stream=None) -> torch.Tensor:
+    """y[i] += s_id * (x[i] . A_id^T) . B_id^T, fused (in place)."""
+    _inner_contig(x, "x")
+    _inner_contig(A_pool, "A_pool")
+    _inner_contig(y, "y")
+    n, r_max, d_in = A_pool.shape
+    arr, ns = _slices(B_pools, y, y_cols, r_max, x.dtype)
+    rp, sp = _ranks_scale(ranks, adapter_scale)
+    _check(lib().lora_delta(ctypes.byref(batch.raw), _dtype_code(x), _dev_ptr(x, "x"), x.stride(0), d_in,
+                            _dev_ptr(A_pool, "A_pool", x.dtype), A_pool.stride(0), A_pool.stride(1),
+                            r_max, arr, ns, rp, float(scale), sp, _dev_ptr(y, "y", x.dtype),
+                            y.stride(0), int(path), _stream(stream)))
+    return y

@@ -1,0 +1,290 @@
+// api.cu -- the extern "C" boundary of the library: argument checks,
+// workspace carving and kernel dispatch.  Declarations and the contract of
+// every entry point are in include/lora_sgmv.h.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <atomic>
+
+#include "common.cuh"
+
+namespace lora {
+cudaError_t launch_prepare(const int32_t *ids, int32_t M, int32_t n, int32_t chunk, int32_t tc_min,
+                           char *ws, const WsLayout &L, lora_batch_t *b, cudaStream_t stream);
+cudaError_t launch_cc(const DeltaArgs &p, int dtype, int mode, int cluster, int sms, cudaStream_t stream);
+int cc_cluster_size(int d_in, int d_out);
+cudaError_t launch_tc(const DeltaArgs &p, int mode, int sms, cudaStream_t stream);
+bool tc_available();
+}  // namespace lora
+
+namespace lora {
+std::atomic<int64_t> &launch_counter() {
+    static std::atomic<int64_t> count{0};
+    return count;
+}
+}  // namespace lora
+
+using namespace lora;
+
+namespace {
+
+thread_local char g_err[512];
+
+lora_status_t fail(lora_status_t code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_size(int dtype) { return dtype == LORA_BF16 ? 2 : 4; }
+
+// Number of SMs of the current device (cached per device).
+int sm_count() {
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cache[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+        cache[dev] = v;
+    }
+    return cache[dev];
+}
+
+lora_status_t check_batch(const lora_batch_t *b) {
+    if (!b) return fail(LORA_ERR_INVALID, "batch is NULL");
+    if (b->magic != kBatchMagic || !b->counts || !b->sorted_token_ids)
+        return fail(LORA_ERR_INVALID, "batch was not filled by lora_prepare_batch");
+    return LORA_OK;
+}
+
+lora_status_t check_dtype_path(int32_t dtype, int32_t path) {
+    if (dtype != LORA_F32 && dtype != LORA_BF16) return fail(LORA_ERR_UNSUPPORTED, "dtype %d not supported", dtype);
+    if (path != LORA_PATH_AUTO && path != LORA_PATH_CUDA_CORE && path != LORA_PATH_TENSOR)
+        return fail(LORA_ERR_INVALID, "unknown path %d", path);
+    if (path == LORA_PATH_TENSOR && dtype != LORA_BF16)
+        return fail(LORA_ERR_UNSUPPORTED, "the tensor-core path computes bf16 inputs only");
+    return LORA_OK;
+}
+
+lora_status_t check_rank(int32_t r_max) {
+    if (r_max < 1 || r_max > LORA_MAX_RANK) return fail(LORA_ERR_UNSUPPORTED, "r_max %d outside [1, %d]", r_max, LORA_MAX_RANK);
+    return LORA_OK;
+}
+
+lora_status_t check_x_a(const lora_batch_t *b, int32_t dtype, const void *x, int64_t ldx, int32_t d_in,
+                        const void *A, int64_t sa, int64_t sr, int32_t r_max) {
+    const int es = elem_size(dtype), V = 16 / es;
+    if (d_in < 1 || d_in % V) return fail(LORA_ERR_UNSUPPORTED, "d_in %d must be a positive multiple of %d", d_in, V);
+    if (b->M > 0 && (!x || !A)) return fail(LORA_ERR_INVALID, "x or A_pool is NULL");
+    if (!aligned16(x) || !aligned16(A)) return fail(LORA_ERR_UNSUPPORTED, "x and A_pool must be 16-byte aligned");
+    if (ldx < d_in || (ldx * es) % 16) return fail(LORA_ERR_UNSUPPORTED, "ldx %lld invalid", (long long)ldx);
+    if (sr < d_in || (sr * es) % 16) return fail(LORA_ERR_UNSUPPORTED, "a_stride_r %lld invalid", (long long)sr);
+    if (sa < (int64_t)r_max * sr || (sa * es) % 16)
+        return fail(LORA_ERR_UNSUPPORTED, "a_stride_adapter %lld invalid", (long long)sa);
+    return LORA_OK;
+}
+
+lora_status_t check_slices(const lora_batch_t *b, int32_t dtype, const lora_b_slice_t *slices, int32_t n_slices,
+                           int32_t r_max, const void *y, int64_t ldy, DeltaArgs &p) {
+    const int es = elem_size(dtype), V = 16 / es;
+    if (!slices || n_slices < 1 || n_slices > LORA_MAX_SLICES)
+        return fail(LORA_ERR_INVALID, "n_slices %d outside [1, %d] or slices NULL", n_slices, LORA_MAX_SLICES);
+    if (b->M > 0 && !y) return fail(LORA_ERR_INVALID, "y is NULL");
+    if (!aligned16(y) || ldy < 1 || (ldy * es) % 16) return fail(LORA_ERR_UNSUPPORTED, "y alignment or ldy invalid");
+    int col = 0;
+    for (int t = 0; t < n_slices; ++t) {
+        const lora_b_slice_t &s = slices[t];
+        if (b->M > 0 && !s.B_pool) return fail(LORA_ERR_INVALID, "slice %d: B_pool is NULL", t);
+        if (!aligned16(s.B_pool)) return fail(LORA_ERR_UNSUPPORTED, "slice %d: B_pool not 16-byte aligned", t);
+        if (s.d_out < 1 || s.d_out % V) return fail(LORA_ERR_UNSUPPORTED, "slice %d: d_out %d not a multiple of %d", t, s.d_out, V);
+        if (s.stride_n < r_max || (s.stride_n * es) % 16) return fail(LORA_ERR_UNSUPPORTED, "slice %d: stride_n invalid", t);
+        if (s.stride_adapter < (int64_t)s.d_out * s.stride_n || (s.stride_adapter * es) % 16)
+            return fail(LORA_ERR_UNSUPPORTED, "slice %d: stride_adapter invalid", t);
+        if (s.y_col < 0 || s.y_col % V || (int64_t)s.y_col + s.d_out > ldy)
+            return fail(LORA_ERR_UNSUPPORTED, "slice %d: y_col %d invalid", t, s.y_col);
+        for (int u = 0; u < t; ++u) {
+            const lora_b_slice_t &o = slices[u];
+            if (s.y_col < o.y_col + o.d_out && o.y_col < s.y_col + s.d_out)
+                return fail(LORA_ERR_INVALID, "slices %d and %d write overlapping y columns", u, t);
+        }
+        p.slices[t].B = s.B_pool;
+        p.slices[t].stride_adapter = s.stride_adapter;
+        p.slices[t].stride_n = s.stride_n;
+        p.slices[t].d_out = s.d_out;
+        p.slices[t].y_col = s.y_col;
+        p.slices[t].col_begin = col;
+        col += s.d_out;
+    }
+    p.n_slices = n_slices;
+    p.d_out_total = col;
+    p.y = const_cast<void *>(y);
+    p.ldy = ldy;
+    return LORA_OK;
+}
+
+void fill_batch(const lora_batch_t *b, DeltaArgs &p) {
+    p.sorted = b->sorted_token_ids;
+    p.indptr = b->seg_indptr;
+    p.lens = b->seg_lens;
+    p.widx = b->weight_indices;
+    p.counts = b->counts;
+}
+
+// Launches the kernels of one call according to the path.
+lora_status_t dispatch(const lora_batch_t *b, int32_t dtype, int mode, int32_t path, int d_in, DeltaArgs &p,
+                       cudaStream_t stream) {
+    fill_batch(b, p);
+    if (b->M == 0) return LORA_OK;
+    const int sms = sm_count();
+    const int cluster = cc_cluster_size(mode == kExpand ? 1 : d_in, p.d_out_total ? p.d_out_total : 1);
+    cudaError_t e = cudaSuccess;
+    const bool tensor_ok = dtype == LORA_BF16 && tc_available();
+    if (path == LORA_PATH_TENSOR) {
+        if (!tensor_ok) return fail(LORA_ERR_UNSUPPORTED, "the tensor-core path is not available for this call");
+        p.seg_list = nullptr;
+        p.count_index = LORA_COUNT_SEGS;
+        p.max_list = b->max_segs;
+        e = launch_tc(p, mode, sms, stream);
+        if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
+    } else if (path == LORA_PATH_AUTO && tensor_ok) {
+        p.seg_list = b->small_segs;
+        p.count_index = LORA_COUNT_SMALL_SEGS;
+        p.max_list = b->max_segs;
+        e = launch_cc(p, dtype, mode, cluster, sms, stream);
+        if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
+        if (e == cudaSuccess && b->M >= b->tc_min_rows) {
+            p.seg_list = b->tc_segs;
+            p.count_index = LORA_COUNT_TC_SEGS;
+            e = launch_tc(p, mode, sms, stream);
+            if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
+        }
+    } else {
+        p.seg_list = nullptr;
+        p.count_index = LORA_COUNT_SEGS;
+        p.max_list = b->max_segs;
+        e = launch_cc(p, dtype, mode, cluster, sms, stream);
+        if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
+    }
+    if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+    return LORA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t lora_workspace_size(int32_t M, int32_t n_adapters, int32_t chunk_size) {
+    if (M < 0 || M > LORA_MAX_TOKENS || n_adapters < 1 || chunk_size < 0) return 0;
+    return ws_layout(M, n_adapters, chunk_size).total;
+}
+
+lora_status_t lora_prepare_batch(const int32_t *ids, int32_t M, int32_t n_adapters, int32_t chunk_size,
+                                 int32_t tc_min_rows, void *workspace, size_t workspace_bytes,
+                                 lora_batch_t *batch, void *stream) {
+    g_err[0] = 0;
+    if (!batch) return fail(LORA_ERR_INVALID, "batch is NULL");
+    if (M < 0 || M > LORA_MAX_TOKENS) return fail(LORA_ERR_INVALID, "M %d outside [0, %d]", M, LORA_MAX_TOKENS);
+    if (n_adapters < 1) return fail(LORA_ERR_INVALID, "n_adapters %d < 1", n_adapters);
+    if (chunk_size < 0) return fail(LORA_ERR_INVALID, "chunk_size %d < 0", chunk_size);
+    if (M > 0 && !ids) return fail(LORA_ERR_INVALID, "ids is NULL");
+    if (!workspace) return fail(LORA_ERR_INVALID, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(LORA_ERR_UNSUPPORTED, "workspace not 256-byte aligned");
+    const WsLayout L = ws_layout(M, n_adapters, chunk_size);
+    if (workspace_bytes < L.total)
+        return fail(LORA_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, L.total);
+    const int32_t tc_min = tc_min_rows > 0 ? tc_min_rows : kDefaultTcMinRows;
+    lora_batch_t b{};
+    cudaError_t e = launch_prepare(ids, M, n_adapters, chunk_size, tc_min, static_cast<char *>(workspace), L, &b,
+                                   static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "prepare launch failed: %s", cudaGetErrorString(e));
+    launch_counter().fetch_add(1, std::memory_order_relaxed);
+    b.M = M;
+    b.n_adapters = n_adapters;
+    b.chunk_size = chunk_size;
+    b.max_segs = L.max_segs;
+    b.tc_min_rows = tc_min;
+    b.magic = kBatchMagic;
+    *batch = b;
+    return LORA_OK;
+}
+
+lora_status_t lora_shrink(const lora_batch_t *batch, int32_t dtype, const void *x, int64_t ldx, int32_t d_in,
+                          const void *A_pool, int64_t a_stride_adapter, int64_t a_stride_r, int32_t r_max,
+                          const int32_t *ranks, float *h, int64_t ldh, int32_t path, void *stream) {
+    g_err[0] = 0;
+    lora_status_t st;
+    if ((st = check_batch(batch)) || (st = check_dtype_path(dtype, path)) || (st = check_rank(r_max))) return st;
+    if ((st = check_x_a(batch, dtype, x, ldx, d_in, A_pool, a_stride_adapter, a_stride_r, r_max))) return st;
+    if (batch->M > 0 && !h) return fail(LORA_ERR_INVALID, "h is NULL");
+    if (ldh < r_max) return fail(LORA_ERR_INVALID, "ldh %lld < r_max", (long long)ldh);
+    DeltaArgs p{};
+    p.x = x;
+    p.ldx = ldx;
+    p.d_in = d_in;
+    p.A = A_pool;
+    p.a_stride_adapter = a_stride_adapter;
+    p.a_stride_r = a_stride_r;
+    p.r_max = r_max;
+    p.ranks = ranks;
+    p.scale = 1.f;
+    p.h = h;
+    p.ldh = ldh;
+    p.n_slices = 0;
+    p.d_out_total = 0;
+    return dispatch(batch, dtype, kShrink, path, d_in, p, static_cast<cudaStream_t>(stream));
+}
+
+lora_status_t lora_expand(const lora_batch_t *batch, int32_t dtype, const float *h, int64_t ldh, int32_t r_max,
+                          const lora_b_slice_t *slices, int32_t n_slices, const int32_t *ranks, float scale,
+                          const float *adapter_scale, void *y, int64_t ldy, int32_t path, void *stream) {
+    g_err[0] = 0;
+    lora_status_t st;
+    if ((st = check_batch(batch)) || (st = check_dtype_path(dtype, path)) || (st = check_rank(r_max))) return st;
+    if (batch->M > 0 && !h) return fail(LORA_ERR_INVALID, "h is NULL");
+    if (ldh < r_max) return fail(LORA_ERR_INVALID, "ldh %lld < r_max", (long long)ldh);
+    DeltaArgs p{};
+    if ((st = check_slices(batch, dtype, slices, n_slices, r_max, y, ldy, p))) return st;
+    p.r_max = r_max;
+    p.ranks = ranks;
+    p.scale = scale;
+    p.adapter_scale = adapter_scale;
+    p.h = const_cast<float *>(h);
+    p.ldh = ldh;
+    return dispatch(batch, dtype, kExpand, path, 0, p, static_cast<cudaStream_t>(stream));
+}
+
+lora_status_t lora_delta(const lora_batch_t *batch, int32_t dtype, const void *x, int64_t ldx, int32_t d_in,
+                         const void *A_pool, int64_t a_stride_adapter, int64_t a_stride_r, int32_t r_max,
+                         const lora_b_slice_t *slices, int32_t n_slices, const int32_t *ranks, float scale,
+                         const float *adapter_scale, void *y, int64_t ldy, int32_t path, void *stream) {
+    g_err[0] = 0;
+    lora_status_t st;
+    if ((st = check_batch(batch)) || (st = check_dtype_path(dtype, path)) || (st = check_rank(r_max))) return st;
+    if ((st = check_x_a(batch, dtype, x, ldx, d_in, A_pool, a_stride_adapter, a_stride_r, r_max))) return st;
+    DeltaArgs p{};
+    if ((st = check_slices(batch, dtype, slices, n_slices, r_max, y, ldy, p))) return st;
+    p.x = x;
+    p.ldx = ldx;
+    p.d_in = d_in;
+    p.A = A_pool;
+    p.a_stride_adapter = a_stride_adapter;
+    p.a_stride_r = a_stride_r;
+    p.r_max = r_max;
+    p.ranks = ranks;
+    p.scale = scale;
+    p.adapter_scale = adapter_scale;
+    return dispatch(batch, dtype, kFused, path, d_in, p, static_cast<cudaStream_t>(stream));
+}
+
+const char *lora_last_error_string(void) { return g_err; }
+
+int32_t lora_abi_version(void) { return 100; }
+
+int64_t lora_launch_count(void) { return launch_counter().load(std::memory_order_relaxed); }
+
+}  // extern "C"

@@ -1,0 +1,217 @@
+// common.cuh -- shared definitions of the sm_103a multi-LoRA delta kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "../../include/lora_sgmv.h"
+
+namespace lora {
+
+// ---------------------------------------------------------------------------
+// Workspace layout of a prepared batch.  Every array starts on a 256-byte
+// boundary so that the device arrays are aligned for vector access.
+// ---------------------------------------------------------------------------
+struct WsLayout {
+    size_t sorted, indptr, lens, widx, small, tc, tcptr, counts;
+    size_t first_pos, adapter_cnt, adapter_group;   // per adapter [n]
+    size_t group_adapter, group_row, group_seg;      // per group [g_max]
+    size_t warp_hist;                                // [32][g_max]
+    size_t total;
+    int32_t max_segs, g_max;
+};
+
+static inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+static inline int64_t max_segments(int64_t M, int64_t n, int64_t chunk) {
+    int64_t g = M < n ? M : n;              // distinct groups
+    if (chunk <= 0) return g;
+    int64_t s = M / chunk + g;              // sum ceil(L_g / C) <= M / C + G
+    return s < M ? s : M;                   // and never more than the rows
+}
+
+static inline WsLayout ws_layout(int32_t M, int32_t n, int32_t chunk) {
+    WsLayout L{};
+    int64_t ms = max_segments(M, n, chunk);
+    int64_t gm = M < n ? M : n;
+    if (ms < 1) ms = 1;
+    if (gm < 1) gm = 1;
+    L.max_segs = (int32_t)ms;
+    L.g_max = (int32_t)gm;
+    size_t o = 0;
+    auto take = [&](size_t ints) { size_t at = o; o = align256(o + ints * 4); return at; };
+    L.sorted = take(M > 0 ? (size_t)M : 1);
+    L.indptr = take((size_t)ms + 1);
+    L.lens = take((size_t)ms);
+    L.widx = take((size_t)ms);
+    L.small = take((size_t)ms);
+    L.tc = take((size_t)ms);
+    L.tcptr = take((size_t)ms + 1);
+    L.counts = take(LORA_NUM_COUNTS);
+    L.first_pos = take((size_t)n);
+    L.adapter_cnt = take((size_t)n);
+    L.adapter_group = take((size_t)n);
+    L.group_adapter = take((size_t)gm);
+    L.group_row = take((size_t)gm + 1);
+    L.group_seg = take((size_t)gm + 1);
+    L.warp_hist = take((size_t)gm * 32);
+    L.total = o;
+    return L;
+}
+
+// Runs a set-up step once per device (kernel attributes are per device).
+struct DeviceOnce {
+    static constexpr int kMaxDevices = 64;
+    volatile bool done[kMaxDevices] = {};
+    template <typename F>
+    cudaError_t run(F &&f) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+        if (done[dev]) return cudaSuccess;
+        e = f();
+        if (e == cudaSuccess) done[dev] = true;
+        return e;
+    }
+};
+
+// Process-wide count of kernel launches made by the library.
+std::atomic<int64_t> &launch_counter();
+
+constexpr uint32_t kBatchMagic = 0x4C6F5241u;  // "LoRA"
+constexpr int kDefaultTcMinRows = 64;
+
+// ---------------------------------------------------------------------------
+// Device helpers.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte global -> shared copy through the async-copy unit.  `src_bytes`
+// (0..16) bytes are read; the rest of the 16 are zero-filled.
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(smem_dst)),
+                 "l"(gsrc), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// Thread-block cluster helpers.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;\n" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;\n" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t nclusters_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;\n" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n"
+                 "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// Address of the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// Element helpers: a 16-byte vector holds 8 bf16 or 4 fp32 values.
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static constexpr int kVec = 4;
+    __device__ __forceinline__ static void to_f32(const uint4 &v, float *o) {
+        o[0] = __uint_as_float(v.x); o[1] = __uint_as_float(v.y);
+        o[2] = __uint_as_float(v.z); o[3] = __uint_as_float(v.w);
+    }
+    __device__ __forceinline__ static float load1(const float *p) { return *p; }
+    __device__ __forceinline__ static void store1(float *p, float v) { *p = v; }
+};
+template <> struct Elem<__nv_bfloat16> {
+    static constexpr int kVec = 8;
+    __device__ __forceinline__ static void to_f32(const uint4 &v, float *o) {
+        // bf16 -> fp32 is exact: the bf16 bits are the high half of the fp32.
+        o[0] = __uint_as_float(v.x << 16); o[1] = __uint_as_float(v.x & 0xFFFF0000u);
+        o[2] = __uint_as_float(v.y << 16); o[3] = __uint_as_float(v.y & 0xFFFF0000u);
+        o[4] = __uint_as_float(v.z << 16); o[5] = __uint_as_float(v.z & 0xFFFF0000u);
+        o[6] = __uint_as_float(v.w << 16); o[7] = __uint_as_float(v.w & 0xFFFF0000u);
+    }
+    __device__ __forceinline__ static float load1(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+    __device__ __forceinline__ static void store1(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
+};
+
+__device__ __forceinline__ void raise_deverr(int32_t *counts, int bit) {
+    if (counts) atomicOr(reinterpret_cast<unsigned int *>(counts + LORA_COUNT_DEVERR), (unsigned)bit);
+}
+
+// ---------------------------------------------------------------------------
+// Host-side launch descriptors (internal).
+// ---------------------------------------------------------------------------
+struct SliceDesc {
+    const void *B;
+    int64_t stride_adapter, stride_n;
+    int32_t d_out, y_col, col_begin;  // col_begin: first column in the concatenated N range
+};
+
+struct DeltaArgs {
+    // batch
+    const int32_t *sorted, *indptr, *lens, *widx, *seg_list;
+    int32_t *counts;
+    int32_t count_index;   // which counter holds the number of entries in seg_list
+    int32_t max_list;      // host-side capacity of seg_list
+    // operands
+    const void *x;
+    int64_t ldx;
+    int32_t d_in;
+    const void *A;
+    int64_t a_stride_adapter, a_stride_r;
+    int32_t r_max;
+    const int32_t *ranks;
+    float scale;
+    const float *adapter_scale;
+    float *h;            // shrink output / expand input (fp32)
+    int64_t ldh;
+    void *y;
+    int64_t ldy;
+    int32_t n_slices;
+    int32_t d_out_total;
+    SliceDesc slices[LORA_MAX_SLICES];
+};
+
+enum Mode { kFused = 0, kShrink = 1, kExpand = 2 };
+
+}  // namespace lora

@@ -1,0 +1,310 @@
+// prepare.cu -- device-side segment metadata for a batch of per-token
+// adapter ids ("III.Punica: Multi-Tenant LoRA Serving", section 代码:
+// prepare_lora_batch regroups tokens by adapter and can cut the regrouped
+// stream into fixed-size chunks; section SGMV: the segment boundary array).
+//
+// One CTA builds the whole batch in seven phases separated by block
+// barriers; nothing is read back by the host.
+//   1. per adapter: first row it appears in (atomicMin) and its row count;
+//      ids outside [-1, n) are counted as invalid.
+//   2. group number of each adapter = number of adapters that appear
+//      earlier (block scan of "row i is its adapter's first row").
+//   3. per group: row base and segment base (block scans of the row count
+//      and of ceil(count / chunk)).
+//   4. per segment: start, length and adapter (binary search of the
+//      segment's group).
+//   5. path split: segments below / at or above the tensor-core row
+//      threshold, with a row prefix over the latter.
+//   6. stable row positions: every warp owns a contiguous range of rows,
+//      counts its rows per group (warp match), the per-group counts are
+//      scanned across warps, then each warp re-walks its range and places
+//      its rows -- rows inside a group keep ascending order.
+//   7. counters.
+#include <climits>
+
+#include "common.cuh"
+
+namespace lora {
+
+struct PrepArgs {
+    const int32_t *ids;
+    int32_t M, n, chunk, tc_min;
+    int32_t *sorted, *indptr, *lens, *widx, *small, *tc, *tcptr, *counts;
+    int32_t *first_pos, *acnt, *agroup;  // global copies, used when not in smem
+    int32_t *gadapter, *grow, *gseg;
+    int32_t *whist;                      // global copy, used when not in smem
+    int32_t adapters_in_smem, hist_in_smem;
+};
+
+// Block-wide exclusive scan of one value per thread.  `ws` is shared scratch
+// of 33 ints.  All threads must call it.
+__device__ __forceinline__ int block_excl_scan(int v, int *total, int *ws) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = (blockDim.x + 31) >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int t = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += t;
+    }
+    if (lane == 31) ws[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < nwarps ? ws[lane] : 0;
+        int s = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int t = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += t;
+        }
+        ws[lane] = s - w;
+        if (lane == 31) ws[32] = s;
+    }
+    __syncthreads();
+    int res = ws[warp] + x - v;
+    *total = ws[32];
+    __syncthreads();
+    return res;
+}
+
+__global__ void prepare_kernel(const PrepArgs p) {
+    extern __shared__ int32_t sm[];
+    __shared__ int scan_ws[33];
+    __shared__ int s_invalid;
+
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
+    const int M = p.M, n = p.n;
+
+    int32_t *first_pos = p.adapters_in_smem ? sm : p.first_pos;
+    int32_t *acnt = p.adapters_in_smem ? sm + n : p.acnt;
+    int32_t *agroup = p.adapters_in_smem ? sm + 2 * n : p.agroup;
+    int32_t *whist = p.hist_in_smem ? sm + (p.adapters_in_smem ? 3 * n : 0) : p.whist;
+
+    // Phase 1: first appearance and row count per adapter.
+    for (int a = tid; a < n; a += nthr) {
+        first_pos[a] = INT_MAX;
+        acnt[a] = 0;
+    }
+    if (tid == 0) s_invalid = 0;
+    __syncthreads();
+    int bad = 0;
+    for (int i = tid; i < M; i += nthr) {
+        const int a = p.ids[i];
+        if (a == -1) continue;
+        if (a < 0 || a >= n) {
+            ++bad;
+            continue;
+        }
+        atomicMin(&first_pos[a], i);
+        atomicAdd(&acnt[a], 1);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
+    if (lane == 0 && bad) atomicAdd(&s_invalid, bad);
+    __syncthreads();
+
+    // Phase 2: group number by order of first appearance.
+    int G = 0;
+    for (int base = 0; base < M; base += nthr) {
+        const int i = base + tid;
+        const int a = i < M ? p.ids[i] : -1;
+        const int flag = (i < M && a >= 0 && a < n && first_pos[a] == i) ? 1 : 0;
+        int tot;
+        const int ex = block_excl_scan(flag, &tot, scan_ws);
+        if (flag) {
+            agroup[a] = G + ex;
+            p.gadapter[G + ex] = a;
+        }
+        G += tot;
+    }
+    __syncthreads();
+
+    // Phase 3: row base and segment base of every group.
+    int rows_run = 0, segs_run = 0;
+    for (int base = 0; base < G; base += nthr) {
+        const int g = base + tid;
+        int len = 0, ns = 0;
+        if (g < G) {
+            len = acnt[p.gadapter[g]];
+            ns = p.chunk > 0 ? (len + p.chunk - 1) / p.chunk : 1;
+        }
+        int tl, tn;
+        const int el = block_excl_scan(len, &tl, scan_ws);
+        const int en = block_excl_scan(ns, &tn, scan_ws);
+        if (g < G) {
+            p.grow[g] = rows_run + el;
+            p.gseg[g] = segs_run + en;
+        }
+        rows_run += tl;
+        segs_run += tn;
+    }
+    if (tid == 0) {
+        p.grow[G] = rows_run;
+        p.gseg[G] = segs_run;
+    }
+    __syncthreads();
+    const int S = segs_run, ACT = rows_run;
+
+    // Phase 4: segments.
+    for (int s = tid; s < S; s += nthr) {
+        int lo = 0, hi = G - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.gseg[mid] <= s) lo = mid;
+            else hi = mid - 1;
+        }
+        const int g = lo, c = s - p.gseg[g];
+        const int start = p.grow[g], len = p.grow[g + 1] - start;
+        int seg_start = start, seg_len = len;
+        if (p.chunk > 0) {
+            seg_start = start + c * p.chunk;
+            seg_len = min(p.chunk, len - c * p.chunk);
+        }
+        p.indptr[s] = seg_start;
+        p.lens[s] = seg_len;
+        p.widx[s] = p.gadapter[g];
+    }
+    if (tid == 0) p.indptr[S] = ACT;
+    __syncthreads();
+
+    // Phase 5: split by the tensor-core row threshold.
+    int n_small = 0, n_tc = 0, tc_rows = 0;
+    for (int base = 0; base < S; base += nthr) {
+        const int s = base + tid;
+        const int len = s < S ? p.lens[s] : 0;
+        const int is_tc = (s < S && len >= p.tc_min) ? 1 : 0;
+        const int is_small = (s < S && !is_tc) ? 1 : 0;
+        int t1, t2, t3;
+        const int es = block_excl_scan(is_small, &t1, scan_ws);
+        const int et = block_excl_scan(is_tc, &t2, scan_ws);
+        const int er = block_excl_scan(is_tc ? len : 0, &t3, scan_ws);
+        if (is_small) p.small[n_small + es] = s;
+        if (is_tc) {
+            p.tc[n_tc + et] = s;
+            p.tcptr[n_tc + et] = tc_rows + er;
+        }
+        n_small += t1;
+        n_tc += t2;
+        tc_rows += t3;
+    }
+    if (tid == 0) p.tcptr[n_tc] = tc_rows;
+
+    // Phase 6: stable row positions.
+    for (int k = tid; k < nwarps * G; k += nthr) whist[k] = 0;
+    __syncthreads();
+    const int per_warp = (M + nwarps - 1) / nwarps;
+    const int w0 = warp * per_warp;
+    const int w1 = min(M, w0 + per_warp);
+    int32_t *wh = whist + warp * G;
+    for (int b = w0; b < w1; b += 32) {
+        const int i = b + lane;
+        int g = -1;
+        if (i < w1) {
+            const int a = p.ids[i];
+            if (a >= 0 && a < n) g = agroup[a];
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, g);
+        if (g >= 0 && lane == __ffs(peers) - 1) wh[g] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int g = tid; g < G; g += nthr) {
+        int run = p.grow[g];
+        for (int w = 0; w < nwarps; ++w) {
+            const int t = whist[w * G + g];
+            whist[w * G + g] = run;
+            run += t;
+        }
+    }
+    __syncthreads();
+    for (int b = w0; b < w1; b += 32) {
+        const int i = b + lane;
+        int g = -1;
+        if (i < w1) {
+            const int a = p.ids[i];
+            if (a >= 0 && a < n) g = agroup[a];
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, g);
+        const int base_pos = g >= 0 ? wh[g] : 0;
+        __syncwarp();
+        if (g >= 0) {
+            p.sorted[base_pos + __popc(peers & ((1u << lane) - 1u))] = i;
+            if (lane == __ffs(peers) - 1) wh[g] = base_pos + __popc(peers);
+        }
+        __syncwarp();
+    }
+
+    // Phase 7: counters.
+    if (tid == 0) {
+        p.counts[LORA_COUNT_SEGS] = S;
+        p.counts[LORA_COUNT_ACTIVE] = ACT;
+        p.counts[LORA_COUNT_INVALID] = s_invalid;
+        p.counts[LORA_COUNT_SMALL_SEGS] = n_small;
+        p.counts[LORA_COUNT_TC_SEGS] = n_tc;
+        p.counts[LORA_COUNT_TC_ROWS] = tc_rows;
+        p.counts[LORA_COUNT_DEVERR] = 0;
+        p.counts[LORA_COUNT_GROUPS] = G;
+    }
+}
+
+// Shared-memory budget of the prepare kernel.
+constexpr size_t kPrepSmemMax = 160 * 1024;
+
+cudaError_t launch_prepare(const int32_t *ids, int32_t M, int32_t n, int32_t chunk,
+                           int32_t tc_min, char *ws, const WsLayout &L,
+                           lora_batch_t *b, cudaStream_t stream) {
+    PrepArgs p{};
+    p.ids = ids;
+    p.M = M;
+    p.n = n;
+    p.chunk = chunk;
+    p.tc_min = tc_min;
+    auto at = [&](size_t off) { return reinterpret_cast<int32_t *>(ws + off); };
+    p.sorted = at(L.sorted);
+    p.indptr = at(L.indptr);
+    p.lens = at(L.lens);
+    p.widx = at(L.widx);
+    p.small = at(L.small);
+    p.tc = at(L.tc);
+    p.tcptr = at(L.tcptr);
+    p.counts = at(L.counts);
+    p.first_pos = at(L.first_pos);
+    p.acnt = at(L.adapter_cnt);
+    p.agroup = at(L.adapter_group);
+    p.gadapter = at(L.group_adapter);
+    p.grow = at(L.group_row);
+    p.gseg = at(L.group_seg);
+    p.whist = at(L.warp_hist);
+
+    const int threads = M > 4096 ? 1024 : (M > 512 ? 512 : 256);
+    const size_t adapter_bytes = size_t(3) * n * 4;
+    const size_t hist_bytes = size_t(threads / 32) * L.g_max * 4;
+    size_t smem = 0;
+    p.adapters_in_smem = adapter_bytes <= kPrepSmemMax / 2;
+    if (p.adapters_in_smem) smem += adapter_bytes;
+    p.hist_in_smem = smem + hist_bytes <= kPrepSmemMax;
+    if (p.hist_in_smem) smem += hist_bytes;
+
+    static DeviceOnce configured;
+    cudaError_t e = configured.run([] {
+        return cudaFuncSetAttribute(prepare_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kPrepSmemMax);
+    });
+    if (e != cudaSuccess) return e;
+    prepare_kernel<<<1, threads, smem, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    b->sorted_token_ids = p.sorted;
+    b->seg_indptr = p.indptr;
+    b->seg_lens = p.lens;
+    b->weight_indices = p.widx;
+    b->small_segs = p.small;
+    b->tc_segs = p.tc;
+    b->tc_indptr = p.tcptr;
+    b->counts = p.counts;
+    return cudaSuccess;
+}
+
+}  // namespace lora

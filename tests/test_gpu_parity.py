@@ -1,0 +1,244 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the
+same seeded inputs.  Segment metadata must match bit for bit; values must
+match within max|y - y_ref| / max|y_ref - y_base| <= 1e-5 (fp32 inputs) or
+1e-2 (bf16 inputs, fp32 accumulation); rows outside every segment must be
+left bit-identical."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from segmented_gather_gemv_gb300 import workloads as wl
+from tests._lora_case import TOL, active_rows, oracle_delta, rel_err, to_dev
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module")
+def B():
+    from segmented_gather_gemv_gb300 import binding
+    binding.lib()
+    return binding
+
+
+# ----------------------------------------------------------------- grouping
+
+def _check_prepare(B, ids_np, n, chunk, tc_min=0):
+    ids = torch.from_numpy(np.asarray(ids_np, np.int32)).cuda()
+    batch = B.lora_prepare_batch(ids, n, chunk, tc_min_rows=tc_min)
+    got = batch.arrays()
+    ref = oracle.prepare_batch(ids_np, n, chunk)
+    assert got["num_segs"] == ref["num_segs"]
+    assert got["num_active"] == ref["num_active"]
+    assert got["num_invalid"] == ref["num_invalid"]
+    for k in ("sorted_token_ids", "seg_indptr", "seg_lens", "weight_indices"):
+        assert np.array_equal(got[k].numpy(), ref[k]), k
+    # path split: every segment in exactly one list, by its length
+    thr = tc_min if tc_min > 0 else batch.raw.tc_min_rows
+    lens = ref["seg_lens"]
+    assert np.array_equal(got["small_segs"].numpy(), np.nonzero(lens < thr)[0])
+    assert np.array_equal(got["tc_segs"].numpy(), np.nonzero(lens >= thr)[0])
+    big = lens[lens >= thr]
+    assert np.array_equal(got["tc_indptr"].numpy(), np.concatenate([[0], np.cumsum(big)]).astype(np.int32))
+    assert got["device_error"] == 0
+    return batch
+
+
+def test_prepare_punica_page_example(B):
+    g = json.load(open(os.path.join(GOLDEN, "punica_segment_example.json")))
+    batch = _check_prepare(B, g["ids"], g["n_adapters"], 0)
+    assert batch.arrays()["seg_indptr"].tolist() == g["seg_indptr"]
+
+
+@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("chunk", [0, 1, 3, 64, 5000])
+@pytest.mark.parametrize("M,n", [(1, 1), (7, 6), (256, 64), (2047, 100), (9000, 3000), (20000, 8)])
+def test_prepare_bit_exact(B, seed, chunk, M, n):
+    rng = np.random.default_rng(seed * 1000 + M)
+    ids = rng.integers(-1, n, size=M).astype(np.int32)
+    if seed == 1:
+        ids = np.repeat(rng.integers(0, n, size=(M + 99) // 100), 100)[:M].astype(np.int32)
+    if seed == 2:
+        ids[rng.choice(M, size=max(1, M // 10), replace=False)] = n + 5  # out of range
+    _check_prepare(B, ids, n, chunk, tc_min=[0, 16, 64, 1][seed])
+
+
+def test_prepare_degenerate(B):
+    _check_prepare(B, np.zeros(0, np.int32), 4, 0)
+    _check_prepare(B, np.full(50, -1, np.int32), 4, 0)
+    _check_prepare(B, np.full(50, 3, np.int32), 4, 7)
+    _check_prepare(B, np.array([99, -7, 2], np.int32), 4, 0)
+
+
+def test_prepare_large_pool_and_batch(B):
+    rng = np.random.default_rng(7)
+    _check_prepare(B, rng.integers(0, 200000, size=30000).astype(np.int32), 200000, 0)
+    _check_prepare(B, rng.integers(0, 50, size=70000).astype(np.int32), 50, 96)
+
+
+def test_prepare_workspace_too_small(B):
+    ids = torch.zeros(16, dtype=torch.int32, device="cuda")
+    ws = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(B.LoraError) as e:
+        B.lora_prepare_batch(ids, 4, 0, workspace=ws)
+    assert e.value.status == B.LORA_ERR_WORKSPACE
+
+
+# ----------------------------------------------------------------- values
+
+def _run_delta(B, w, path=0, tc_min=0, guard_cols=0):
+    d = to_dev(w)
+    ids = d["ids"]
+    batch = B.lora_prepare_batch(ids, w.n_adapters, w.chunk_size, tc_min_rows=tc_min)
+    y = d["y"]
+    if guard_cols:
+        # y inside a wider buffer whose extra columns hold a sentinel
+        big = torch.full((w.M, w.d_out + guard_cols), 12345.0, dtype=y.dtype, device="cuda")
+        big[:, :w.d_out] = y
+        y = big[:, :w.d_out]
+    B.lora_delta(batch, d["x"], d["A"], d["B"], y, scale=w.scale, adapter_scale=d["adapter_scale"],
+                 ranks=d["ranks"], path=path)
+    torch.cuda.synchronize()
+    if guard_cols:
+        assert torch.all(big[:, w.d_out:] == 12345.0), "write outside y's columns"
+    return y.float().cpu().numpy().astype(np.float64), batch
+
+
+def _assert_delta(w, y_gpu, counts=None):
+    y_ref = oracle_delta(w)
+    act = active_rows(w)
+    err = rel_err(y_gpu, y_ref, w.y.astype(np.float64), act)
+    assert err <= TOL[w.dtype], "rel err %.3e > %.0e" % (err, TOL[w.dtype])
+    assert np.array_equal(y_gpu[~act], w.y[~act].astype(np.float64)), "inactive rows changed"
+    assert np.isfinite(y_gpu).all()
+    return err
+
+
+@pytest.mark.parametrize("path", [0, 1])
+def test_page1_toy(B, path):
+    w = wl.page1_toy()
+    y, _ = _run_delta(B, w, path)
+    _assert_delta(w, y)
+    assert np.abs(y - oracle_delta(w)).max() < 1e-3  # the page's own criterion
+
+
+def test_segment_example_values(B):
+    w = wl.segment_example()
+    y, batch = _run_delta(B, w)
+    _assert_delta(w, y)
+
+
+SMALL_CASES = [
+    # several row tiles per segment, ragged d, mixed ranks, slices, skips
+    dict(M=300, d_in=1000, d_outs=[776], n_pool=5, r_max=16, run_len=40),
+    dict(M=257, d_in=520, d_outs=[264, 64, 136], n_pool=9, r_max=32, ranks=[8, 16, 24, 32],
+         skip_frac=0.2, bad_frac=0.05, per_adapter_scale=True),
+    dict(M=64, d_in=4096, d_outs=[4096], n_pool=16, r_max=16),
+    dict(M=33, d_in=64, d_outs=[128], n_pool=40, r_max=64, ranks=[8, 16, 32, 64], skip_frac=0.25),
+    dict(M=90, d_in=2048, d_outs=[512], n_pool=3, r_max=128, run_len=30),
+    dict(M=200, d_in=304, d_outs=[96], n_pool=12, r_max=8, ranks=[1, 3, 5, 8], run_len=25),
+    dict(M=1, d_in=256, d_outs=[256], n_pool=2, r_max=16),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("ci", range(len(SMALL_CASES)))
+@pytest.mark.parametrize("chunk", [0, 7])
+def test_delta_small(B, dtype, ci, chunk):
+    w = wl.random_batch(seed=100 + ci, dtype=dtype, chunk_size=chunk, **SMALL_CASES[ci])
+    y, batch = _run_delta(B, w, path=1, guard_cols=8 if dtype == "bf16" else 4)
+    _assert_delta(w, y)
+    c = batch.counts()
+    assert c["num_invalid"] == int(((w.ids >= w.n_adapters) | (w.ids < -1)).sum())
+    assert c["device_error"] == 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("ci", [0, 1, 3])
+def test_shrink_and_expand(B, dtype, ci):
+    w = wl.random_batch(seed=200 + ci, dtype=dtype, **SMALL_CASES[ci])
+    d = to_dev(w)
+    batch = B.lora_prepare_batch(d["ids"], w.n_adapters, 0)
+    guard = torch.full((w.M, w.r_max + 4), -777.0, device="cuda")
+    h = guard[:, :w.r_max]
+    B.lora_shrink(batch, d["x"], d["A"], h=h, ranks=d["ranks"], path=1)
+    torch.cuda.synchronize()
+    act = active_rows(w)
+    assert torch.all(guard[:, w.r_max:] == -777.0)
+    assert torch.all(h[torch.from_numpy(~act).cuda()] == -777.0), "h rows outside segments written"
+    h_ref = oracle.shrink(w.x, w.ids, w.A, ranks=w.ranks)
+    hg = h.cpu().numpy().astype(np.float64)
+    err = np.abs(hg[act] - h_ref[act]).max() / np.abs(h_ref[act]).max()
+    assert err <= TOL[dtype]
+    # expand from a seeded h of its own (not the GPU's)
+    rng = np.random.default_rng(5)
+    h_in = rng.standard_normal((w.M, w.r_max)).astype(np.float32)
+    y = d["y"].clone()
+    B.lora_expand(batch, torch.from_numpy(h_in).cuda(), d["B"], y, scale=w.scale,
+                  adapter_scale=d["adapter_scale"], ranks=d["ranks"], path=1)
+    y_ref = oracle.expand(h_in, w.ids, w.B, w.y, scale=w.scale, adapter_scale=w.adapter_scale,
+                          ranks=w.ranks)
+    yg = y.float().cpu().numpy().astype(np.float64)
+    assert rel_err(yg, y_ref, w.y.astype(np.float64), act) <= TOL[dtype]
+    assert np.array_equal(yg[~act], w.y[~act].astype(np.float64))
+
+
+def test_mixed_rank_nan_padding_never_read(B):
+    w = wl.random_batch(seed=300, M=128, d_in=512, d_outs=[384], n_pool=10, r_max=64,
+                        ranks=[8, 16, 32, 64], dtype="bf16", pad_value=float("nan"),
+                        per_adapter_scale=True)
+    y, _ = _run_delta(B, w, path=1)
+    _assert_delta(w, y)
+
+
+def test_rank_out_of_range_sets_device_error(B):
+    w = wl.random_batch(seed=301, M=40, d_in=128, d_outs=[64], n_pool=4, r_max=16, dtype="bf16")
+    w.ranks = np.array([16, 99, 16, 16], np.int32)  # adapter 1 claims rank 99 > r_max
+    y, batch = _run_delta(B, w, path=1)
+    assert batch.counts()["device_error"] & B.DEVERR_RANK
+    bad = w.ids == 1
+    assert np.array_equal(y[bad], w.y[bad].astype(np.float64))
+
+
+def test_empty_and_all_skipped(B):
+    for ids in (np.zeros(0, np.int32), np.full(9, -1, np.int32)):
+        w = wl.random_batch(seed=302, M=len(ids), d_in=64, d_outs=[64], n_pool=3, r_max=8, dtype="bf16")
+        w.ids = ids
+        y, _ = _run_delta(B, w)
+        assert np.array_equal(y, w.y.astype(np.float64))
+
+
+def test_unaligned_pointer_rejected(B):
+    w = wl.random_batch(seed=303, M=8, d_in=64, d_outs=[64], n_pool=2, r_max=8, dtype="bf16")
+    d = to_dev(w)
+    batch = B.lora_prepare_batch(d["ids"], 2, 0)
+    xb = torch.zeros(8 * 64 + 1, dtype=torch.bfloat16, device="cuda")[1:].view(8, 64)
+    with pytest.raises(B.LoraError) as e:
+        B.lora_delta(batch, xb, d["A"], d["B"], d["y"])
+    assert e.value.status == B.LORA_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------ full-size serving scenarios
+
+FULL = ["decode", "prefill", "prefill_chunk64", "mixed_rank_up", "mixed_rank_down", "mixed_serving"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_scenarios(B, name):
+    w = wl.north_star_workloads()[name]()
+    y, batch = _run_delta(B, w)
+    err = _assert_delta(w, y)
+    c = batch.counts()
+    assert c["device_error"] == 0
+    assert c["num_active"] == int(active_rows(w).sum())
+    print("%s: rel err %.3e" % (name, err))
+
+
+def test_mixed_rank_nan_padding_full_size(B):
+    w = wl.mixed_rank(proj="down", pad_value=float("nan"))
+    y, _ = _run_delta(B, w)
+    _assert_delta(w, y)
