@@ -140,8 +140,20 @@ def _dev_ptr(t: Optional[torch.Tensor], what: str, dtype=None) -> Optional[int]:
 
 
 def _inner_contig(t: torch.Tensor, what: str):
-    if t.dim() < 1 or t.stride(-1) != 1:
+    if t.dim() < 1:
+        raise ValueError("%s must have at least one dimension" % what)
+    if t.numel() and t.stride(-1) != 1:
         raise ValueError("%s must have a contiguous last dimension" % what)
+
+
+def _ld(t: torch.Tensor, dim: int = 0) -> int:
+    """Row stride of a tensor (the row length when it holds no elements)."""
+    if t.numel() == 0:
+        n = 1
+        for s in t.shape[dim + 1:]:
+            n *= s
+        return n
+    return t.stride(dim)
 
 
 class Batch:
@@ -235,8 +247,8 @@ def _slices(B_pools, y: torch.Tensor, y_cols, r_max: int, dtype):
             raise ValueError("B pool %d must be (n, d_out, r_max) of the input dtype" % t)
         _inner_contig(B, "B pool")
         arr[t].B_pool = _dev_ptr(B, "B pool")
-        arr[t].stride_adapter = B.stride(0)
-        arr[t].stride_n = B.stride(1)
+        arr[t].stride_adapter = _ld(B)
+        arr[t].stride_n = _ld(B, 1)
         arr[t].d_out = B.shape[1]
         arr[t].y_col = int(y_cols[t]) if y_cols is not None else col
         col += B.shape[1]
@@ -260,10 +272,10 @@ def lora_shrink(batch: Batch, x: torch.Tensor, A_pool: torch.Tensor,
         h = torch.zeros((batch.M, r_max), dtype=torch.float32, device=x.device)
     _inner_contig(h, "h")
     rp, _ = _ranks_scale(ranks, None)
-    _check(lib().lora_shrink(ctypes.byref(batch.raw), _dtype_code(x), _dev_ptr(x, "x"), x.stride(0),
-                             d_in, _dev_ptr(A_pool, "A_pool", x.dtype), A_pool.stride(0),
-                             A_pool.stride(1), r_max, rp, _dev_ptr(h, "h", torch.float32),
-                             h.stride(0), int(path), _stream(stream)))
+    _check(lib().lora_shrink(ctypes.byref(batch.raw), _dtype_code(x), _dev_ptr(x, "x"), _ld(x),
+                             d_in, _dev_ptr(A_pool, "A_pool", x.dtype), _ld(A_pool),
+                             _ld(A_pool, 1), r_max, rp, _dev_ptr(h, "h", torch.float32),
+                             _ld(h), int(path), _stream(stream)))
     return h
 
 
@@ -278,8 +290,8 @@ def lora_expand(batch: Batch, h: torch.Tensor, B_pools, y: torch.Tensor, scale: 
     arr, ns = _slices(B_pools, y, y_cols, r_max, y.dtype)
     rp, sp = _ranks_scale(ranks, adapter_scale)
     _check(lib().lora_expand(ctypes.byref(batch.raw), _dtype_code(y), _dev_ptr(h, "h", torch.float32),
-                             h.stride(0), r_max, arr, ns, rp, float(scale), sp, _dev_ptr(y, "y"),
-                             y.stride(0), int(path), _stream(stream)))
+                             _ld(h), r_max, arr, ns, rp, float(scale), sp, _dev_ptr(y, "y"),
+                             _ld(y), int(path), _stream(stream)))
     return y
 
 
@@ -294,8 +306,8 @@ def lora_delta(batch: Batch, x: torch.Tensor, A_pool: torch.Tensor, B_pools, y: 
     n, r_max, d_in = A_pool.shape
     arr, ns = _slices(B_pools, y, y_cols, r_max, x.dtype)
     rp, sp = _ranks_scale(ranks, adapter_scale)
-    _check(lib().lora_delta(ctypes.byref(batch.raw), _dtype_code(x), _dev_ptr(x, "x"), x.stride(0), d_in,
-                            _dev_ptr(A_pool, "A_pool", x.dtype), A_pool.stride(0), A_pool.stride(1),
+    _check(lib().lora_delta(ctypes.byref(batch.raw), _dtype_code(x), _dev_ptr(x, "x"), _ld(x), d_in,
+                            _dev_ptr(A_pool, "A_pool", x.dtype), _ld(A_pool), _ld(A_pool, 1),
                             r_max, arr, ns, rp, float(scale), sp, _dev_ptr(y, "y", x.dtype),
-                            y.stride(0), int(path), _stream(stream)))
+                            _ld(y), int(path), _stream(stream)))
     return y
