@@ -91,6 +91,7 @@ typedef int lora_status_t;
 #define LORA_MAX_TOKENS (1 << 24)
 #define LORA_MAX_RANK 128
 #define LORA_MAX_SLICES 4
+#define LORA_DESC_INLINE_ROWS 28 /* token rows held inline in a segment descriptor */
 
 /* Device counters written by lora_prepare_batch (int32 each, in order). */
 #define LORA_COUNT_SEGS 0       /* number of segments S */
@@ -117,8 +118,16 @@ typedef int lora_status_t;
  *   seg_indptr[max_segs+1]  start of segment s in sorted_token_ids
  *   seg_lens[max_segs]      rows in segment s (> 0)
  *   weight_indices[max_segs] adapter slot of segment s
- *   small_segs[max_segs]    ids of segments with < tc_min_rows rows
- *   tc_segs[max_segs]       ids of segments with >= tc_min_rows rows
+ *   seg_records[max_segs][32] per segment s a 128-byte descriptor
+ *                             {start, len, adapter, s, rows[28]}: rows
+ *                             holds the segment's first min(len, 28)
+ *                             token rows; entries s >= num_segs have
+ *                             len 0
+ *   small_segs[max_segs][4]   records {start, len, adapter, s} of the
+ *                             segments with < tc_min_rows rows, in
+ *                             segment order
+ *   tc_segs[max_segs][4]      records of the segments with >= tc_min_rows
+ *                             rows, in segment order
  *   tc_indptr[max_segs+1]   prefix sum of rows over tc_segs
  *   counts[LORA_NUM_COUNTS] see LORA_COUNT_*
  * Host fields describe the batch the metadata was built for.
@@ -128,6 +137,7 @@ typedef struct lora_batch {
     int32_t *seg_indptr;
     int32_t *seg_lens;
     int32_t *weight_indices;
+    int32_t *seg_records;
     int32_t *small_segs;
     int32_t *tc_segs;
     int32_t *tc_indptr;

@@ -50,7 +50,7 @@ class LoraError(RuntimeError):
 class _Batch(ctypes.Structure):
     _fields_ = [("sorted_token_ids", ctypes.c_void_p), ("seg_indptr", ctypes.c_void_p),
                 ("seg_lens", ctypes.c_void_p), ("weight_indices", ctypes.c_void_p),
-                ("small_segs", ctypes.c_void_p), ("tc_segs", ctypes.c_void_p),
+                ("seg_records", ctypes.c_void_p), ("small_segs", ctypes.c_void_p), ("tc_segs", ctypes.c_void_p),
                 ("tc_indptr", ctypes.c_void_p), ("counts", ctypes.c_void_p),
                 ("M", ctypes.c_int32), ("n_adapters", ctypes.c_int32),
                 ("chunk_size", ctypes.c_int32), ("max_segs", ctypes.c_int32),
@@ -196,8 +196,9 @@ class Batch:
             "seg_indptr": self._view("seg_indptr", S + 1).cpu(),
             "seg_lens": self._view("seg_lens", S).cpu(),
             "weight_indices": self._view("weight_indices", S).cpu(),
-            "small_segs": self._view("small_segs", c["num_small_segs"]).cpu(),
-            "tc_segs": self._view("tc_segs", c["num_tc_segs"]).cpu(),
+            "seg_records": self._view("seg_records", 32 * self.max_segs).cpu().view(-1, 32),
+            "small_segs": self._view("small_segs", 4 * c["num_small_segs"]).cpu().view(-1, 4),
+            "tc_segs": self._view("tc_segs", 4 * c["num_tc_segs"]).cpu().view(-1, 4),
             "tc_indptr": self._view("tc_indptr", c["num_tc_segs"] + 1).cpu(),
             **c,
         }

@@ -129,9 +129,7 @@ lora_status_t check_slices(const lora_batch_t *b, int32_t dtype, const lora_b_sl
 
 void fill_batch(const lora_batch_t *b, DeltaArgs &p) {
     p.sorted = b->sorted_token_ids;
-    p.indptr = b->seg_indptr;
-    p.lens = b->seg_lens;
-    p.widx = b->weight_indices;
+    p.tc_indptr = b->tc_indptr;
     p.counts = b->counts;
 }
 
@@ -144,31 +142,43 @@ lora_status_t dispatch(const lora_batch_t *b, int32_t dtype, int mode, int32_t p
     const int cluster = cc_cluster_size(mode == kExpand ? 1 : d_in, p.d_out_total ? p.d_out_total : 1);
     cudaError_t e = cudaSuccess;
     const bool tensor_ok = dtype == LORA_BF16 && tc_available();
+    p.desc = reinterpret_cast<const SegDesc *>(b->seg_records);
+    p.max_list = b->max_segs;
+    p.M_rows = b->M;
+    p.n_adapters = b->n_adapters;
     if (path == LORA_PATH_TENSOR) {
-        if (!tensor_ok) return fail(LORA_ERR_UNSUPPORTED, "the tensor-core path is not available for this call");
-        p.seg_list = nullptr;
-        p.count_index = LORA_COUNT_SEGS;
-        p.max_list = b->max_segs;
+        if (!tensor_ok || mode != kFused)
+            return fail(LORA_ERR_UNSUPPORTED, "the tensor-core path computes the fused bf16 delta only");
+        if (p.r_max > kTcMaxRankCommon && !p.ranks)
+            return fail(LORA_ERR_UNSUPPORTED, "the tensor-core path takes ranks up to %d", kTcMaxRankCommon);
+        // every segment: the row space is the sorted rows themselves
+        p.tc_ptr = b->seg_indptr;
+        p.tc_start = b->seg_indptr;
+        p.tc_adapter = b->weight_indices;
+        p.tc_rec_stride = 1;
+        p.tc_count_index = LORA_COUNT_SEGS;
+        p.tc_rows_index = LORA_COUNT_ACTIVE;
+        p.tc_only = 1;
         e = launch_tc(p, mode, sms, stream);
         if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
-    } else if (path == LORA_PATH_AUTO && tensor_ok) {
-        p.seg_list = b->small_segs;
-        p.count_index = LORA_COUNT_SMALL_SEGS;
-        p.max_list = b->max_segs;
+    } else {
+        const bool split = path == LORA_PATH_AUTO && tensor_ok && mode == kFused;
+        p.min_len = 0;
+        p.max_len = split ? b->tc_min_rows : 0x7fffffff;
+        p.split_tc = split ? 1 : 0;
         e = launch_cc(p, dtype, mode, cluster, sms, stream);
         if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
-        if (e == cudaSuccess && b->M >= b->tc_min_rows) {
-            p.seg_list = b->tc_segs;
-            p.count_index = LORA_COUNT_TC_SEGS;
+        if (e == cudaSuccess && split && b->M >= b->tc_min_rows) {
+            p.tc_ptr = b->tc_indptr;
+            p.tc_start = b->tc_segs;
+            p.tc_adapter = b->tc_segs + 2;
+            p.tc_rec_stride = 4;
+            p.tc_count_index = LORA_COUNT_TC_SEGS;
+            p.tc_rows_index = LORA_COUNT_TC_ROWS;
+            p.tc_only = 0;
             e = launch_tc(p, mode, sms, stream);
             if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
         }
-    } else {
-        p.seg_list = nullptr;
-        p.count_index = LORA_COUNT_SEGS;
-        p.max_list = b->max_segs;
-        e = launch_cc(p, dtype, mode, cluster, sms, stream);
-        if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
     }
     if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
     return LORA_OK;

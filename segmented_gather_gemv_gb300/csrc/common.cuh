@@ -16,7 +16,7 @@ namespace lora {
 // boundary so that the device arrays are aligned for vector access.
 // ---------------------------------------------------------------------------
 struct WsLayout {
-    size_t sorted, indptr, lens, widx, small, tc, tcptr, counts;
+    size_t sorted, indptr, lens, widx, rec, small, tc, tcptr, counts;
     size_t first_pos, adapter_cnt, adapter_group;   // per adapter [n]
     size_t group_adapter, group_row, group_seg;      // per group [g_max]
     size_t warp_hist;                                // [32][g_max]
@@ -47,8 +47,9 @@ static inline WsLayout ws_layout(int32_t M, int32_t n, int32_t chunk) {
     L.indptr = take((size_t)ms + 1);
     L.lens = take((size_t)ms);
     L.widx = take((size_t)ms);
-    L.small = take((size_t)ms);
-    L.tc = take((size_t)ms);
+    L.rec = take((size_t)ms * 32);
+    L.small = take((size_t)ms * 4);
+    L.tc = take((size_t)ms * 4);
     L.tcptr = take((size_t)ms + 1);
     L.counts = take(LORA_NUM_COUNTS);
     L.first_pos = take((size_t)n);
@@ -84,6 +85,9 @@ std::atomic<int64_t> &launch_counter();
 
 constexpr uint32_t kBatchMagic = 0x4C6F5241u;  // "LoRA"
 constexpr int kDefaultTcMinRows = 64;
+constexpr int kTcMaxRankCommon = 64;
+// Ranks the tensor-core kernel computes (exact 8-column masking, <= 64).
+__host__ __device__ __forceinline__ bool tc_rank_ok(int r) { return r > 0 && r <= kTcMaxRankCommon && (r & 7) == 0; }
 
 // ---------------------------------------------------------------------------
 // Device helpers.
@@ -150,10 +154,96 @@ __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
     return v;
 }
 
+// Programmatic dependent launch: let the next grid in the stream start its
+// prologue early / wait until the previous grid has completed and its
+// memory is visible.  Both are no-ops when the launch did not opt in.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
+// mbarrier helpers (shared::cta barriers, transaction-count based).
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+// Longest a kernel waits on one barrier before it gives up (ns).  Real waits
+// last microseconds; the limit only ends a wait that can no longer complete.
+constexpr uint64_t kWaitLimitNs = 100ull * 1000 * 1000;
+// Bounded wait for phase `parity` of `bar`.  Returns false if the barrier did
+// not complete in time (the caller flags an error; it never spins forever).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() > deadline) return false;
+    }
+}
+// As mbar_wait, but also gives up as soon as another role of the CTA has
+// set `*abort`, and sets it on its own timeout.
+__device__ __forceinline__ bool mbar_wait_abort(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() > deadline) {
+            *abort = 1;
+            return false;
+        }
+    }
+}
+// Bulk (non-tensor) async copy global -> shared, completing on `bar`.
+// Both addresses 16-byte aligned, `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+// Store to the same shared-memory location in another CTA of the cluster.
+__device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;\n" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
 // Element helpers: a 16-byte vector holds 8 bf16 or 4 fp32 values.
 template <typename T> struct Elem;
 template <> struct Elem<float> {
     static constexpr int kVec = 4;
+    using PairT = float2;  // two consecutive elements
+    __device__ __forceinline__ static float2 pair_to_f32(const float2 &v) { return v; }
+    __device__ __forceinline__ static void store_pair(float *p, const float2 &v) {
+        *reinterpret_cast<float2 *>(p) = v;
+    }
     __device__ __forceinline__ static void to_f32(const uint4 &v, float *o) {
         o[0] = __uint_as_float(v.x); o[1] = __uint_as_float(v.y);
         o[2] = __uint_as_float(v.z); o[3] = __uint_as_float(v.w);
@@ -163,6 +253,13 @@ template <> struct Elem<float> {
 };
 template <> struct Elem<__nv_bfloat16> {
     static constexpr int kVec = 8;
+    using PairT = uint32_t;  // two consecutive elements
+    __device__ __forceinline__ static float2 pair_to_f32(uint32_t w) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    }
+    __device__ __forceinline__ static void store_pair(__nv_bfloat16 *p, const float2 &v) {
+        *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(v.x, v.y);
+    }
     __device__ __forceinline__ static void to_f32(const uint4 &v, float *o) {
         // bf16 -> fp32 is exact: the bf16 bits are the high half of the fp32.
         o[0] = __uint_as_float(v.x << 16); o[1] = __uint_as_float(v.x & 0xFFFF0000u);
@@ -173,6 +270,18 @@ template <> struct Elem<__nv_bfloat16> {
     __device__ __forceinline__ static float load1(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
     __device__ __forceinline__ static void store1(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
 };
+
+// Two consecutive elements of a 16-byte vector as a float2 (word q holds
+// elements 2q and 2q+1 for bf16; for fp32 the pair is elements 2q, 2q+1).
+template <typename T> __device__ __forceinline__ float2 pair_of(const uint4 &v, int q);
+template <> __device__ __forceinline__ float2 pair_of<__nv_bfloat16>(const uint4 &v, int q) {
+    const uint32_t w = q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+template <> __device__ __forceinline__ float2 pair_of<float>(const uint4 &v, int q) {
+    return q == 0 ? make_float2(__uint_as_float(v.x), __uint_as_float(v.y))
+                  : make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+}
 
 __device__ __forceinline__ void raise_deverr(int32_t *counts, int bit) {
     if (counts) atomicOr(reinterpret_cast<unsigned int *>(counts + LORA_COUNT_DEVERR), (unsigned)bit);
@@ -187,12 +296,31 @@ struct SliceDesc {
     int32_t d_out, y_col, col_begin;  // col_begin: first column in the concatenated N range
 };
 
+// 128-byte segment descriptor written by prepare: header + inline rows.
+constexpr int kInlineRows = LORA_DESC_INLINE_ROWS;
+struct SegDesc {
+    int32_t start, len, adapter, seg;
+    int32_t rows[kInlineRows];
+};
+static_assert(sizeof(SegDesc) == 128, "segment descriptor is 128 bytes");
+
 struct DeltaArgs {
     // batch
-    const int32_t *sorted, *indptr, *lens, *widx, *seg_list;
+    const int32_t *sorted;   // sorted_token_ids
+    const SegDesc *desc;     // all segment descriptors (len 0 past the last)
+    const int4 *recs;        // records {start, len, adapter, s} (tensor-core list)
+    const int32_t *tc_indptr;
     int32_t *counts;
-    int32_t count_index;   // which counter holds the number of entries in seg_list
-    int32_t max_list;      // host-side capacity of seg_list
+    int32_t count_index;     // which counter holds the number of records in recs
+    int32_t max_list;        // host-side capacity of desc / recs
+    int32_t min_len, max_len;  // the CUDA-core kernel takes segments with min_len <= len < max_len
+    int32_t split_tc;          // 1: segments >= max_len with a tensor-core rank go to the tensor-core kernel
+    int32_t M_rows;            // rows of x and y
+    int32_t n_adapters;
+    // tensor-core row space: segment i covers rows [tc_ptr[i], tc_ptr[i+1]),
+    // starts at sorted position tc_start[i * tc_rec_stride], adapter tc_adapter[...]
+    const int32_t *tc_ptr, *tc_start, *tc_adapter;
+    int32_t tc_rec_stride, tc_count_index, tc_rows_index, tc_only;
     // operands
     const void *x;
     int64_t ldx;

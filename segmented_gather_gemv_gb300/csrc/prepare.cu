@@ -3,8 +3,10 @@
 // prepare_lora_batch regroups tokens by adapter and can cut the regrouped
 // stream into fixed-size chunks; section SGMV: the segment boundary array).
 //
-// One CTA builds the whole batch in seven phases separated by block
-// barriers; nothing is read back by the host.
+// One CTA builds the whole batch; every working array lives in shared
+// memory when it fits (the ids, the per-adapter and per-group tables and
+// the per-warp histograms), so the phases below cost shared-memory latency,
+// not global-memory round trips.  Nothing is read back by the host.
 //   1. per adapter: first row it appears in (atomicMin) and its row count;
 //      ids outside [-1, n) are counted as invalid.
 //   2. group number of each adapter = number of adapters that appear
@@ -12,14 +14,13 @@
 //   3. per group: row base and segment base (block scans of the row count
 //      and of ceil(count / chunk)).
 //   4. per segment: start, length and adapter (binary search of the
-//      segment's group).
-//   5. path split: segments below / at or above the tensor-core row
-//      threshold, with a row prefix over the latter.
-//   6. stable row positions: every warp owns a contiguous range of rows,
+//      segment's group), written as arrays and 16-byte records, and split
+//      by the tensor-core row threshold (block scans).
+//   5. stable row positions: every warp owns a contiguous range of rows,
 //      counts its rows per group (warp match), the per-group counts are
 //      scanned across warps, then each warp re-walks its range and places
 //      its rows -- rows inside a group keep ascending order.
-//   7. counters.
+//   6. counters.
 #include <climits>
 
 #include "common.cuh"
@@ -28,12 +29,18 @@ namespace lora {
 
 struct PrepArgs {
     const int32_t *ids;
-    int32_t M, n, chunk, tc_min;
-    int32_t *sorted, *indptr, *lens, *widx, *small, *tc, *tcptr, *counts;
-    int32_t *first_pos, *acnt, *agroup;  // global copies, used when not in smem
+    int32_t M, n, chunk, tc_min, gcap;
+    int32_t *sorted, *indptr, *lens, *widx, *counts;
+    SegDesc *desc;
+    int32_t max_segs;
+    int4 *small, *tc;
+    int32_t *tcptr;
+    // global fall-backs for tables that do not fit in shared memory
+    int32_t *first_pos, *acnt, *agroup;
     int32_t *gadapter, *grow, *gseg;
-    int32_t *whist;                      // global copy, used when not in smem
-    int32_t adapters_in_smem, hist_in_smem;
+    int32_t *whist;
+    // shared-memory placement (byte offsets into dynamic shared memory, -1 = global)
+    int32_t off_ids, off_adapters, off_groups, off_hist;
 };
 
 // Block-wide exclusive scan of one value per thread.  `ws` is shared scratch
@@ -67,19 +74,34 @@ __device__ __forceinline__ int block_excl_scan(int v, int *total, int *ws) {
     return res;
 }
 
-__global__ void prepare_kernel(const PrepArgs p) {
-    extern __shared__ int32_t sm[];
+__global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ int scan_ws[33];
     __shared__ int s_invalid;
+
+    // Let the next kernel in the stream start its prologue; it waits for
+    // this grid's completion before it reads what this grid writes.
+    griddep_launch_dependents();
+    griddep_wait();
 
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
     const int M = p.M, n = p.n;
+    const int G_cap = p.gcap;
 
-    int32_t *first_pos = p.adapters_in_smem ? sm : p.first_pos;
-    int32_t *acnt = p.adapters_in_smem ? sm + n : p.acnt;
-    int32_t *agroup = p.adapters_in_smem ? sm + 2 * n : p.agroup;
-    int32_t *whist = p.hist_in_smem ? sm + (p.adapters_in_smem ? 3 * n : 0) : p.whist;
+    int32_t *first_pos = p.off_adapters >= 0 ? reinterpret_cast<int32_t *>(smem_raw + p.off_adapters) : p.first_pos;
+    int32_t *acnt = p.off_adapters >= 0 ? first_pos + n : p.acnt;
+    int32_t *agroup = p.off_adapters >= 0 ? first_pos + 2 * n : p.agroup;
+    int32_t *gadapter = p.off_groups >= 0 ? reinterpret_cast<int32_t *>(smem_raw + p.off_groups) : p.gadapter;
+    int32_t *grow = p.off_groups >= 0 ? gadapter + G_cap : p.grow;
+    int32_t *gseg = p.off_groups >= 0 ? grow + G_cap + 1 : p.gseg;
+    int32_t *whist = p.off_hist >= 0 ? reinterpret_cast<int32_t *>(smem_raw + p.off_hist) : p.whist;
+    const int32_t *ids = p.ids;
+    if (p.off_ids >= 0) {
+        int32_t *ids_s = reinterpret_cast<int32_t *>(smem_raw + p.off_ids);
+        for (int i = tid; i < M; i += nthr) ids_s[i] = p.ids[i];
+        ids = ids_s;
+    }
 
     // Phase 1: first appearance and row count per adapter.
     for (int a = tid; a < n; a += nthr) {
@@ -90,7 +112,7 @@ __global__ void prepare_kernel(const PrepArgs p) {
     __syncthreads();
     int bad = 0;
     for (int i = tid; i < M; i += nthr) {
-        const int a = p.ids[i];
+        const int a = ids[i];
         if (a == -1) continue;
         if (a < 0 || a >= n) {
             ++bad;
@@ -108,13 +130,13 @@ __global__ void prepare_kernel(const PrepArgs p) {
     int G = 0;
     for (int base = 0; base < M; base += nthr) {
         const int i = base + tid;
-        const int a = i < M ? p.ids[i] : -1;
+        const int a = i < M ? ids[i] : -1;
         const int flag = (i < M && a >= 0 && a < n && first_pos[a] == i) ? 1 : 0;
         int tot;
         const int ex = block_excl_scan(flag, &tot, scan_ws);
         if (flag) {
             agroup[a] = G + ex;
-            p.gadapter[G + ex] = a;
+            gadapter[G + ex] = a;
         }
         G += tot;
     }
@@ -126,71 +148,77 @@ __global__ void prepare_kernel(const PrepArgs p) {
         const int g = base + tid;
         int len = 0, ns = 0;
         if (g < G) {
-            len = acnt[p.gadapter[g]];
+            len = acnt[gadapter[g]];
             ns = p.chunk > 0 ? (len + p.chunk - 1) / p.chunk : 1;
         }
         int tl, tn;
         const int el = block_excl_scan(len, &tl, scan_ws);
         const int en = block_excl_scan(ns, &tn, scan_ws);
         if (g < G) {
-            p.grow[g] = rows_run + el;
-            p.gseg[g] = segs_run + en;
+            grow[g] = rows_run + el;
+            gseg[g] = segs_run + en;
         }
         rows_run += tl;
         segs_run += tn;
     }
     if (tid == 0) {
-        p.grow[G] = rows_run;
-        p.gseg[G] = segs_run;
+        grow[G] = rows_run;
+        gseg[G] = segs_run;
     }
     __syncthreads();
     const int S = segs_run, ACT = rows_run;
 
-    // Phase 4: segments.
-    for (int s = tid; s < S; s += nthr) {
-        int lo = 0, hi = G - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (p.gseg[mid] <= s) lo = mid;
-            else hi = mid - 1;
-        }
-        const int g = lo, c = s - p.gseg[g];
-        const int start = p.grow[g], len = p.grow[g + 1] - start;
-        int seg_start = start, seg_len = len;
-        if (p.chunk > 0) {
-            seg_start = start + c * p.chunk;
-            seg_len = min(p.chunk, len - c * p.chunk);
-        }
-        p.indptr[s] = seg_start;
-        p.lens[s] = seg_len;
-        p.widx[s] = p.gadapter[g];
-    }
-    if (tid == 0) p.indptr[S] = ACT;
-    __syncthreads();
-
-    // Phase 5: split by the tensor-core row threshold.
+    // Phase 4: segments, records and the tensor-core split.
     int n_small = 0, n_tc = 0, tc_rows = 0;
     for (int base = 0; base < S; base += nthr) {
         const int s = base + tid;
-        const int len = s < S ? p.lens[s] : 0;
-        const int is_tc = (s < S && len >= p.tc_min) ? 1 : 0;
+        int seg_start = 0, seg_len = 0, adapter = 0;
+        if (s < S) {
+            int lo = 0, hi = G - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (gseg[mid] <= s) lo = mid;
+                else hi = mid - 1;
+            }
+            const int g = lo, c = s - gseg[g];
+            const int start = grow[g], len = grow[g + 1] - start;
+            seg_start = start;
+            seg_len = len;
+            if (p.chunk > 0) {
+                seg_start = start + c * p.chunk;
+                seg_len = min(p.chunk, len - c * p.chunk);
+            }
+            adapter = gadapter[g];
+            p.indptr[s] = seg_start;
+            p.lens[s] = seg_len;
+            p.widx[s] = adapter;
+            *reinterpret_cast<int4 *>(&p.desc[s]) = make_int4(seg_start, seg_len, adapter, s);
+        }
+        const int is_tc = (s < S && seg_len >= p.tc_min) ? 1 : 0;
         const int is_small = (s < S && !is_tc) ? 1 : 0;
         int t1, t2, t3;
         const int es = block_excl_scan(is_small, &t1, scan_ws);
         const int et = block_excl_scan(is_tc, &t2, scan_ws);
-        const int er = block_excl_scan(is_tc ? len : 0, &t3, scan_ws);
-        if (is_small) p.small[n_small + es] = s;
+        const int er = block_excl_scan(is_tc ? seg_len : 0, &t3, scan_ws);
+        const int4 rec = make_int4(seg_start, seg_len, adapter, s);
+        if (is_small) p.small[n_small + es] = rec;
         if (is_tc) {
-            p.tc[n_tc + et] = s;
+            p.tc[n_tc + et] = rec;
             p.tcptr[n_tc + et] = tc_rows + er;
         }
         n_small += t1;
         n_tc += t2;
         tc_rows += t3;
     }
-    if (tid == 0) p.tcptr[n_tc] = tc_rows;
+    if (tid == 0) {
+        p.indptr[S] = ACT;
+        p.tcptr[n_tc] = tc_rows;
+    }
+    // Descriptors past the last segment end the list (len 0).
+    for (int s = S + tid; s < p.max_segs; s += nthr)
+        *reinterpret_cast<int4 *>(&p.desc[s]) = make_int4(0, 0, 0, s);
 
-    // Phase 6: stable row positions.
+    // Phase 5: stable row positions.
     for (int k = tid; k < nwarps * G; k += nthr) whist[k] = 0;
     __syncthreads();
     const int per_warp = (M + nwarps - 1) / nwarps;
@@ -201,7 +229,7 @@ __global__ void prepare_kernel(const PrepArgs p) {
         const int i = b + lane;
         int g = -1;
         if (i < w1) {
-            const int a = p.ids[i];
+            const int a = ids[i];
             if (a >= 0 && a < n) g = agroup[a];
         }
         const unsigned peers = __match_any_sync(0xffffffffu, g);
@@ -210,7 +238,7 @@ __global__ void prepare_kernel(const PrepArgs p) {
     }
     __syncthreads();
     for (int g = tid; g < G; g += nthr) {
-        int run = p.grow[g];
+        int run = grow[g];
         for (int w = 0; w < nwarps; ++w) {
             const int t = whist[w * G + g];
             whist[w * G + g] = run;
@@ -222,20 +250,26 @@ __global__ void prepare_kernel(const PrepArgs p) {
         const int i = b + lane;
         int g = -1;
         if (i < w1) {
-            const int a = p.ids[i];
+            const int a = ids[i];
             if (a >= 0 && a < n) g = agroup[a];
         }
         const unsigned peers = __match_any_sync(0xffffffffu, g);
         const int base_pos = g >= 0 ? wh[g] : 0;
         __syncwarp();
         if (g >= 0) {
-            p.sorted[base_pos + __popc(peers & ((1u << lane) - 1u))] = i;
+            const int pos = base_pos + __popc(peers & ((1u << lane) - 1u));
+            p.sorted[pos] = i;
             if (lane == __ffs(peers) - 1) wh[g] = base_pos + __popc(peers);
+            // first rows of every segment, inline in its descriptor
+            const int off = pos - grow[g];
+            const int s = gseg[g] + (p.chunk > 0 ? off / p.chunk : 0);
+            const int k = p.chunk > 0 ? off - (off / p.chunk) * p.chunk : off;
+            if (k < kInlineRows) p.desc[s].rows[k] = i;
         }
         __syncwarp();
     }
 
-    // Phase 7: counters.
+    // Phase 6: counters.
     if (tid == 0) {
         p.counts[LORA_COUNT_SEGS] = S;
         p.counts[LORA_COUNT_ACTIVE] = ACT;
@@ -249,7 +283,7 @@ __global__ void prepare_kernel(const PrepArgs p) {
 }
 
 // Shared-memory budget of the prepare kernel.
-constexpr size_t kPrepSmemMax = 160 * 1024;
+constexpr size_t kPrepSmemMax = 200 * 1024;
 
 cudaError_t launch_prepare(const int32_t *ids, int32_t M, int32_t n, int32_t chunk,
                            int32_t tc_min, char *ws, const WsLayout &L,
@@ -260,13 +294,16 @@ cudaError_t launch_prepare(const int32_t *ids, int32_t M, int32_t n, int32_t chu
     p.n = n;
     p.chunk = chunk;
     p.tc_min = tc_min;
+    p.gcap = L.g_max;
     auto at = [&](size_t off) { return reinterpret_cast<int32_t *>(ws + off); };
     p.sorted = at(L.sorted);
     p.indptr = at(L.indptr);
     p.lens = at(L.lens);
     p.widx = at(L.widx);
-    p.small = at(L.small);
-    p.tc = at(L.tc);
+    p.desc = reinterpret_cast<SegDesc *>(ws + L.rec);
+    p.max_segs = L.max_segs;
+    p.small = reinterpret_cast<int4 *>(ws + L.small);
+    p.tc = reinterpret_cast<int4 *>(ws + L.tc);
     p.tcptr = at(L.tcptr);
     p.counts = at(L.counts);
     p.first_pos = at(L.first_pos);
@@ -277,14 +314,21 @@ cudaError_t launch_prepare(const int32_t *ids, int32_t M, int32_t n, int32_t chu
     p.gseg = at(L.group_seg);
     p.whist = at(L.warp_hist);
 
-    const int threads = M > 4096 ? 1024 : (M > 512 ? 512 : 256);
-    const size_t adapter_bytes = size_t(3) * n * 4;
-    const size_t hist_bytes = size_t(threads / 32) * L.g_max * 4;
+    const int threads = M > 8192 ? 1024 : (M > 1024 ? 512 : 256);
+    const int gcap = L.g_max;
+    // Place tables in shared memory, most latency-critical first.
     size_t smem = 0;
-    p.adapters_in_smem = adapter_bytes <= kPrepSmemMax / 2;
-    if (p.adapters_in_smem) smem += adapter_bytes;
-    p.hist_in_smem = smem + hist_bytes <= kPrepSmemMax;
-    if (p.hist_in_smem) smem += hist_bytes;
+    auto place = [&](size_t bytes) -> int32_t {
+        bytes = (bytes + 15) & ~size_t(15);
+        if (smem + bytes > kPrepSmemMax) return -1;
+        const int32_t off = (int32_t)smem;
+        smem += bytes;
+        return off;
+    };
+    p.off_groups = place(size_t(3 * gcap + 2) * 4);
+    p.off_hist = place(size_t(threads / 32) * gcap * 4);
+    p.off_adapters = place(size_t(3) * n * 4);
+    p.off_ids = place(size_t(M) * 4);
 
     static DeviceOnce configured;
     cudaError_t e = configured.run([] {
@@ -292,16 +336,27 @@ cudaError_t launch_prepare(const int32_t *ids, int32_t M, int32_t n, int32_t chu
                                     (int)kPrepSmemMax);
     });
     if (e != cudaSuccess) return e;
-    prepare_kernel<<<1, threads, smem, stream>>>(p);
-    e = cudaGetLastError();
+
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, prepare_kernel, p);
     if (e != cudaSuccess) return e;
 
     b->sorted_token_ids = p.sorted;
     b->seg_indptr = p.indptr;
     b->seg_lens = p.lens;
     b->weight_indices = p.widx;
-    b->small_segs = p.small;
-    b->tc_segs = p.tc;
+    b->seg_records = reinterpret_cast<int32_t *>(p.desc);
+    b->small_segs = reinterpret_cast<int32_t *>(p.small);
+    b->tc_segs = reinterpret_cast<int32_t *>(p.tc);
     b->tc_indptr = p.tcptr;
     b->counts = p.counts;
     return cudaSuccess;

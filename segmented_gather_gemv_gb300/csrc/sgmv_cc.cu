@@ -7,54 +7,59 @@
 // the segment).  CTA q of the cluster owns
 //   - the K slice q of d_in for the shrink (A rows r x K/CL, x rows R x K/CL),
 //   - the N slice q of d_out for the expand (B rows N/CL x r, y rows R x N/CL),
-// so every byte of x, A, B and y is read exactly once per segment.  The
-// partial h of the K slices is summed across the cluster through distributed
-// shared memory (fixed order, so every CTA holds the same h); h never leaves
-// the chip.
+// so every byte of x, A, B and y is read once per segment tile.  The partial
+// h of the K slices is pushed to every CTA of the cluster through
+// distributed shared memory and summed in a fixed order, so every CTA holds
+// the same h; h never leaves the chip.
 //
-// Loads: 16-byte cp.async into a ring of kCcStages stages.  All x/A (shrink)
-// and y/B (expand) tiles of a segment are "jobs"; the first kCcStages-1 jobs
-// are issued before any compute, so the expand's B and y tiles are in flight
-// while the shrink runs.  Gathered rows (sorted_token_ids) cost nothing
-// extra: every 16-byte copy carries its own address.  B rows are read only up
-// to the adapter's rank (the rest of the last vector is zero-filled).
+// Latency: a segment is reached through one 128-byte descriptor that holds
+// its first rows inline, so every load address of the tile is known after a
+// single dependent read.  All x/A (shrink) and y/B (expand) bytes of a tile
+// are then requested at once: x, A and y rows by bulk async copies completing
+// on one mbarrier per ring stage, B rows by 16-byte cp.async into an
+// XOR-swizzled layout, reading B only up to the adapter's rank.
 //
-// Compute (fp32 FMA): shrink -- warp w owns rank rows j = w + 8*jj, lanes
-// stride over the K vectors, a transposing butterfly reduces the lanes;
-// expand -- every thread owns CPT output columns and all rows of the tile.
+// Compute (fp32, packed FFMA2): shrink -- every thread owns a 4-row x 4-rank
+// block of h and strides over K with its accumulators live across all K
+// chunks; lanes sharing a block are reduced once, at the end.  Expand --
+// every thread owns two adjacent output columns and all rows of the tile.
 #include "common.cuh"
 
 namespace lora {
 
-constexpr int kCcThreads = 256;
-constexpr int kCcWarps = kCcThreads / 32;
-constexpr int kCcStages = 8;
-constexpr int kCcCpt = 4;  // output columns per thread per expand pass
+constexpr int kCcThreads = 512;
+constexpr int kCcStages = 3;
+constexpr int kCcMaxCluster = 8;
 
-__host__ __device__ __forceinline__ int cc_hp(int r_max) { return (r_max + 7) & ~7; }
+// Shared-memory layout of one launch (computed on the host).
+struct CcGeom {
+    int RT;           // rows per tile (multiple of 4, <= kInlineRows)
+    int HP;           // r_max rounded up to 8
+    int stage_bytes;  // bytes per ring stage (multiple of 128)
+    int off_bars, off_desc, off_rows, off_slots, off_recv, off_hfull, off_ring;
+    int total;
+};
 
-template <int RT>
-static inline size_t cc_smem_bytes(int stage_bytes, int r_max) {
-    return (size_t)kCcStages * stage_bytes + (size_t)3 * RT * cc_hp(r_max) * 4 + RT * 4;
+__host__ __device__ __forceinline__ int cc_rows_per_tile(int r_max) {
+    int rt = 1024 / (r_max > 0 ? r_max : 1);
+    rt = rt > kInlineRows ? kInlineRows : rt;
+    rt = rt < 8 ? 8 : rt;
+    return rt & ~3;
 }
 
-// After this, lane l holds in v[0 .. NV/32) the sums over the 32 lanes of the
-// original entries i + (NV/32) * l.
-template <int NV>
-__device__ __forceinline__ void warp_transpose_reduce(float (&v)[NV], int lane) {
-    static_assert(NV >= 32 && (NV & (NV - 1)) == 0, "NV must be a power of two >= 32");
-#pragma unroll
-    for (int stage = 0; stage < 5; ++stage) {
-        const int off = 16 >> stage;
-        const int half = NV >> (stage + 1);
-        const bool upper = (lane & off) != 0;
-#pragma unroll
-        for (int i = 0; i < half; ++i) {
-            const float send = upper ? v[i] : v[i + half];
-            const float keep = upper ? v[i + half] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-        }
-    }
+__device__ __forceinline__ int next_pow2(int v) {
+    int p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+__device__ __forceinline__ int ilog2(int v) { return 31 - __clz(v); }
+
+// Position of 16-byte chunk c of B row n in a stage whose rows hold rvp
+// chunks: an XOR swizzle that spreads rows read together over the banks.
+__device__ __forceinline__ int b_swizzle(int n, int c, int rvp) {
+    if (rvp >= 8) return c ^ (n & 7);
+    const int sh = rvp == 1 ? 3 : rvp == 2 ? 2 : 1;
+    return c ^ ((n >> sh) & (rvp - 1));
 }
 
 // Maps a column of the concatenated output range to its slice.
@@ -66,131 +71,217 @@ __device__ __forceinline__ int slice_of(const DeltaArgs &p, int col) {
     return t;
 }
 
-template <typename T, int MODE, int JW, int RT>
+// Reduces 16 values over groups of KS adjacent lanes (KS a power of two,
+// 1..32).  Afterwards v[i] (i < 16 >> min(log2 KS, 4)) holds the group total
+// of entry idx(i, lane) = i + sum_s bit_{S-1-s}(lane) * (16 >> (s+1)).
+__device__ __forceinline__ void group_reduce16(float (&v)[16], int lane, int S) {
+#pragma unroll
+    for (int st = 0; st < 5; ++st) {
+        if (st >= S) break;
+        const int off = 1 << (S - 1 - st);
+        if (st < 4) {
+            const int half = 8 >> st;
+            const bool upper = (lane & off) != 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (i < half) {
+                    const float send = upper ? v[i] : v[i + half];
+                    const float keep = upper ? v[i + half] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                }
+            }
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+        }
+    }
+}
+
+template <typename T, int MODE>
 __global__ void __launch_bounds__(kCcThreads, 1)
-    sgmv_cc_kernel(const __grid_constant__ DeltaArgs p, const int stage_bytes) {
+    sgmv_cc_kernel(const __grid_constant__ DeltaArgs p, const __grid_constant__ CcGeom g) {
     using E = Elem<T>;
     constexpr int V = E::kVec;
-    constexpr int NA = RT * JW;
-    constexpr int NV = NA < 32 ? 32 : NA;
-    extern __shared__ __align__(16) unsigned char smem[];
-
-    const int HP = cc_hp(p.r_max);
-    unsigned char *ring = smem;
-    float *h_part = reinterpret_cast<float *>(smem + (size_t)kCcStages * stage_bytes);
-    float *h_full = h_part + 2 * RT * HP;
-    int32_t *rows_s = reinterpret_cast<int32_t *>(h_full + RT * HP);
+    constexpr int PV = V / 2;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + g.off_bars);
+    int32_t *desc_s = reinterpret_cast<int32_t *>(smem + g.off_desc);  // [32]
+    int32_t *rows_s = reinterpret_cast<int32_t *>(smem + g.off_rows);  // [RT]
+    float *slots = reinterpret_cast<float *>(smem + g.off_slots);      // [warp][16]
+    float *recv = reinterpret_cast<float *>(smem + g.off_recv);        // [CL][RT][HP]
+    float *h_full = reinterpret_cast<float *>(smem + g.off_hfull);     // [RT][HP]
+    unsigned char *ring = smem + g.off_ring;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t CL = cluster_nctarank(), q = cluster_ctarank();
     const uint32_t cid = cluster_id_x(), ncl = nclusters_x();
+    const int RT = g.RT, HP = g.HP, SB = g.stage_bytes;
 
-    int nlist = p.counts[p.count_index];
-    if (nlist > p.max_list) nlist = p.max_list;
+    if (tid == 0) {
+        for (int s = 0; s < kCcStages; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    griddep_launch_dependents();
+    griddep_wait();
 
     const int kv_total = p.d_in / V;
     const int kv0 = (int)((int64_t)kv_total * q / CL), kv1 = (int)((int64_t)kv_total * (q + 1) / CL);
     const int nv_total = p.d_out_total / V;
     const int nv0 = (int)((int64_t)nv_total * q / CL), nv1 = (int)((int64_t)nv_total * (q + 1) / CL);
+    const T *xg = static_cast<const T *>(p.x);
+    const T *Ag = static_cast<const T *>(p.A);
+    uint32_t gjob = 0;  // jobs issued so far by this CTA (ring position and barrier phase)
+    bool wait_ok = true;
 
-    int hbuf = 0;
-    for (int li = (int)cid; li < nlist; li += (int)ncl) {
-        const int s = p.seg_list ? p.seg_list[li] : li;
-        const int a = p.widx[s], len = p.lens[s], start = p.indptr[s];
+    for (int li = (int)cid; li < p.max_list; li += (int)ncl) {
+        __syncthreads();  // the previous segment is done with desc_s / rows_s
+        if (tid < 32) desc_s[tid] = reinterpret_cast<const int32_t *>(p.desc + li)[tid];
+        __syncthreads();
+        const int start = desc_s[0], len = desc_s[1], a = desc_s[2];
+        if (len == 0) break;  // descriptors are compacted: the list ends here
         const int r = p.ranks ? p.ranks[a] : p.r_max;
+        // Long segments belong to the tensor-core kernel when it can take
+        // their rank.
+        if (len < p.min_len || (len >= p.max_len && (!p.split_tc || tc_rank_ok(r)))) continue;
+        if (r == 0 && MODE != kShrink) continue;  // rank 0: nothing to add
         if (r < 0 || r > p.r_max) {
             if (q == 0 && tid == 0) raise_deverr(p.counts, LORA_DEVERR_RANK);
             continue;
         }
         const float sc = p.adapter_scale ? p.adapter_scale[a] : p.scale;
-        const int rv = (r + V - 1) / V;  // 16-byte vectors per B row
+        const int rv = (r + V - 1) / V;
+        const int rvp = next_pow2(rv > 0 ? rv : 1);
+        const int njg = (r + 3) / 4;
 
         for (int t0 = 0; t0 < len; t0 += RT) {
             const int R = min(RT, len - t0);
-            __syncthreads();  // the previous tile is done with rows_s and h_full
-            if (tid < R) rows_s[tid] = p.sorted[start + t0 + tid];
+            const int nrb = (R + 3) / 4, Rp = nrb * 4;
+            if (t0 > 0) __syncthreads();  // the previous tile is done with rows_s
+            if (tid < R) rows_s[tid] = t0 + tid < kInlineRows ? desc_s[4 + t0 + tid] : p.sorted[start + t0 + tid];
             __syncthreads();
 
-            int kc = stage_bytes / ((R + r) * 16);
-            int nc = stage_bytes / ((R + V * rv) * 16);
-            kc = kc < 1 ? 1 : kc;
-            nc = nc < 1 ? 1 : nc;
-            const int nK = (MODE == kExpand) ? 0 : (kv1 - kv0 + kc - 1) / kc;
-            const int nN = (MODE == kShrink) ? 0 : (nv1 - nv0 + nc - 1) / nc;
+            // Shrink thread map: block ob = (row block, rank group) of 4x4
+            // outputs, KS lanes per block striding over K.
+            const int n_ob = nrb * (njg > 0 ? njg : 1);
+            const int KS = kCcThreads / next_pow2(n_ob);
+            const int ob = tid / KS, ks = tid - ob * KS;
+            const int my_rb = ob / (njg > 0 ? njg : 1), my_jg = ob - my_rb * (njg > 0 ? njg : 1);
+            const bool has_block = ob < n_ob && njg > 0;
+
+            int nK = 0, kc = 1, nN = 0, nc = 1;
+            if (MODE != kExpand && kv1 > kv0) {
+                const int kcmax = max(1, SB / ((Rp + r) * 16));
+                nK = (kv1 - kv0 + kcmax - 1) / kcmax;
+                kc = (kv1 - kv0 + nK - 1) / nK;
+            }
+            if (MODE != kShrink && nv1 > nv0) {
+                const int ncmax = max(1, SB / ((R + V * rvp) * 16));
+                nN = (nv1 - nv0 + ncmax - 1) / ncmax;
+                nc = (nv1 - nv0 + nN - 1) / nN;
+            }
             const int total = nK + nN;
 
-            float acc[RT][JW];
-#pragma unroll
-            for (int i = 0; i < RT; ++i)
-#pragma unroll
-                for (int jj = 0; jj < JW; ++jj) acc[i][jj] = 0.f;
-
-            // ---- job issue: all 16-byte copies of one job into its stage.
+            // ---- issue one job into its stage (called by every thread).
             auto issue = [&](int j) {
-                unsigned char *st = ring + (size_t)(j % kCcStages) * stage_bytes;
+                const uint32_t G = gjob + j;
+                unsigned char *sb = ring + (size_t)(G % kCcStages) * SB;
+                uint64_t *bar = &bars[G % kCcStages];
                 if (j < nK) {
                     const int kb = kv0 + j * kc, kn = min(kc, kv1 - kb);
-                    for (int row = warp; row < R + r; row += kCcWarps) {
-                        const T *src;
-                        if (row < R)
-                            src = static_cast<const T *>(p.x) + (int64_t)rows_s[row] * p.ldx + (int64_t)kb * V;
-                        else
-                            src = static_cast<const T *>(p.A) + (int64_t)a * p.a_stride_adapter +
-                                  (int64_t)(row - R) * p.a_stride_r + (int64_t)kb * V;
-                        unsigned char *dst = st + (size_t)row * kc * 16;
-                        for (int c = lane; c < kn; c += 32) cp_async16(dst + c * 16, src + c * V, 16);
+                    if (warp == 0) {
+                        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)((R + r) * kn * 16));
+                        __syncwarp();
+                        for (int row = lane; row < R + r; row += 32) {
+                            const T *src = row < R ? xg + (int64_t)rows_s[row] * p.ldx + (int64_t)kb * V
+                                                   : Ag + (int64_t)a * p.a_stride_adapter +
+                                                         (int64_t)(row - R) * p.a_stride_r + (int64_t)kb * V;
+                            const int srow = row < R ? row : Rp + (row - R);
+                            bulk_g2s(sb + (size_t)srow * kc * 16, src, (uint32_t)kn * 16, bar);
+                        }
                     }
                 } else {
                     const int nb = nv0 + (j - nK) * nc, nn = min(nc, nv1 - nb);
-                    for (int row = warp; row < R; row += kCcWarps) {
-                        const int64_t yrow = (int64_t)rows_s[row] * p.ldy;
-                        unsigned char *dst = st + (size_t)row * nc * 16;
-                        for (int c = lane; c < nn; c += 32) {
-                            const int col = (nb + c) * V;
-                            const SliceDesc &S = p.slices[slice_of(p, col)];
-                            const T *src = static_cast<const T *>(p.y) + yrow + S.y_col + (col - S.col_begin);
-                            cp_async16(dst + c * 16, src, 16);
+                    const int c0 = nb * V, c1 = (nb + nn) * V;
+                    if (warp == 0) {
+                        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(R * nn * 16));
+                        __syncwarp();
+                        for (int t = 0; t < p.n_slices; ++t) {
+                            const SliceDesc &S = p.slices[t];
+                            const int lo = max(c0, S.col_begin), hi = min(c1, S.col_begin + S.d_out);
+                            if (lo >= hi) continue;
+                            for (int row = lane; row < R; row += 32) {
+                                const T *src = static_cast<const T *>(p.y) + (int64_t)rows_s[row] * p.ldy + S.y_col +
+                                               (lo - S.col_begin);
+                                bulk_g2s(sb + (size_t)row * nc * 16 + (size_t)(lo - c0) * sizeof(T), src,
+                                         (uint32_t)((hi - lo) * sizeof(T)), bar);
+                            }
                         }
                     }
-                    unsigned char *bst = st + (size_t)R * nc * 16;
+                    unsigned char *bst = sb + (size_t)R * nc * 16;
                     const int nrows = nn * V;
+                    const int rv_shift = (rv & (rv - 1)) == 0 ? ilog2(rv) : -1;
                     for (int e = tid; e < nrows * rv; e += kCcThreads) {
-                        const int br = e / rv, c = e - br * rv;
-                        const int col = nb * V + br;
+                        const int br = rv_shift >= 0 ? e >> rv_shift : e / rv;
+                        const int c = e - br * rv;
+                        const int col = c0 + br;
                         const SliceDesc &S = p.slices[slice_of(p, col)];
                         const T *src = static_cast<const T *>(S.B) + (int64_t)a * S.stride_adapter +
                                        (int64_t)(col - S.col_begin) * S.stride_n + c * V;
                         const int bytes = min(16, (r - c * V) * (int)sizeof(T));
-                        cp_async16(bst + (size_t)e * 16, src, bytes);
+                        cp_async16(bst + (size_t)(br * rvp + b_swizzle(br, c, rvp)) * 16, src, bytes);
                     }
                 }
+                cp_async_commit();
             };
 
-            // ---- h reduction across the cluster (shrink/fused only).
-            auto reduce_h = [&]() {
-                float v[NV];
+            float2 acc[4][4];
 #pragma unroll
-                for (int i = 0; i < NV; ++i) v[i] = i < NA ? acc[i / JW][i % JW] : 0.f;
-                warp_transpose_reduce<NV>(v, lane);
-                float *hp = h_part + hbuf * RT * HP;
+            for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int i = 0; i < NV / 32; ++i) {
-                    const int idx = i + (NV / 32) * lane;
-                    if (idx < NA) {
-                        const int row = idx / JW, j = warp + kCcWarps * (idx % JW);
-                        if (row < R && j < r) hp[row * HP + j] = v[i];
+                for (int jj = 0; jj < 4; ++jj) acc[i][jj] = make_float2(0.f, 0.f);
+
+            // ---- partial h of this CTA -> every CTA of the cluster -> h_full.
+            auto finish_shrink = [&]() {
+                float v[16];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) v[i * 4 + jj] = acc[i][jj].x + acc[i][jj].y;
+                const int S = ilog2(KS < 32 ? KS : 32);
+                group_reduce16(v, lane, S);
+                const int nvals = 16 >> (S < 4 ? S : 4);
+                const int wpb = KS > 32 ? KS / 32 : 1;  // warps per block
+                if (has_block) {
+                    // this lane's share of the block's 16 totals
+                    int base = 0;
+#pragma unroll
+                    for (int st = 0; st < 4; ++st)
+                        if (st < S) base += ((lane >> (S - 1 - st)) & 1) * (16 >> (st + 1));
+                    const bool writer = S <= 4 || (lane & 1) == 0;
+                    if (writer) {
+                        const int wslot = ob * wpb + (KS > 32 ? (ks >> 5) : 0);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (i < nvals) slots[wslot * 16 + base + i] = v[i];
                     }
                 }
                 __syncthreads();
-                cluster_sync();
-                for (int e = tid; e < R * HP; e += kCcThreads) {
+                for (int e = tid; e < R * r; e += kCcThreads) {
+                    const int row = e / r, j = e - row * r;
+                    const int b = (row >> 2) * njg + (j >> 2), idx = (row & 3) * 4 + (j & 3);
+                    float s = 0.f;
+                    for (int w = 0; w < wpb; ++w) s += slots[(b * wpb + w) * 16 + idx];
+                    const uint32_t local = smem_u32(recv + ((int)q * RT + row) * HP + j);
+                    for (uint32_t pr = 0; pr < CL; ++pr) st_dsmem_f32(map_to_rank(local, pr), s);
+                }
+                cluster_arrive_release();
+                cluster_wait_acquire();
+                for (int e = tid; e < RT * HP; e += kCcThreads) {
                     const int row = e / HP, j = e - row * HP;
-                    float sum = 0.f;
-                    if (j < r) {
-                        const uint32_t addr = smem_u32(hp + row * HP + j);
-                        for (uint32_t pr = 0; pr < CL; ++pr) sum += ld_dsmem_f32(map_to_rank(addr, pr));
-                    }
-                    h_full[e] = (MODE == kFused) ? sum * sc : sum;
+                    float s = 0.f;
+                    if (row < R && j < r)
+                        for (uint32_t pq = 0; pq < CL; ++pq) s += recv[((int)pq * RT + row) * HP + j];
+                    h_full[e] = (MODE == kFused) ? s * sc : s;
                 }
                 __syncthreads();
                 if (MODE == kShrink && q == 0) {
@@ -199,207 +290,210 @@ __global__ void __launch_bounds__(kCcThreads, 1)
                         p.h[(int64_t)rows_s[row] * p.ldh + j] = j < r ? h_full[row * HP + j] : 0.f;
                     }
                 }
-                hbuf ^= 1;
             };
 
             if (MODE == kExpand) {
-                for (int e = tid; e < R * HP; e += kCcThreads) {
+                for (int e = tid; e < RT * HP; e += kCcThreads) {
                     const int row = e / HP, j = e - row * HP;
-                    h_full[e] = j < r ? p.h[(int64_t)rows_s[row] * p.ldh + j] * sc : 0.f;
+                    h_full[e] = (row < R && j < r) ? p.h[(int64_t)rows_s[row] * p.ldh + j] * sc : 0.f;
                 }
-                __syncthreads();
             }
 
 #pragma unroll 1
-            for (int j = 0; j < kCcStages - 1; ++j) {
+            for (int j = 0; j < kCcStages; ++j) {
                 if (j < total) issue(j);
-                cp_async_commit();
+                else cp_async_commit();
             }
-            if (MODE != kExpand && nK == 0) reduce_h();
+            if (MODE != kExpand && nK == 0) finish_shrink();
 
 #pragma unroll 1
             for (int j = 0; j < total; ++j) {
-                const int jn = j + kCcStages - 1;
-                if (jn < total) issue(jn);
-                cp_async_commit();
+                const uint32_t G = gjob + j;
+                if (tid == 0 && !mbar_wait(&bars[G % kCcStages], (G / kCcStages) & 1)) wait_ok = false;
                 cp_async_wait<kCcStages - 1>();
                 __syncthreads();
-                const unsigned char *st = ring + (size_t)(j % kCcStages) * stage_bytes;
+                const unsigned char *sb = ring + (size_t)(G % kCcStages) * SB;
                 if (j < nK) {
-                    // ---- shrink job: acc[row][jj] += x[row, K] . A[j, K]
-                    const int kb = kv0 + j * kc, kn = min(kc, kv1 - kb);
-                    const unsigned char *xs = st;
-                    const unsigned char *As = st + (size_t)R * kc * 16;
-                    if (warp < r) {
-                        for (int c = lane; c < kn; c += 32) {
-                            float af[JW][V];
+                    // ---- shrink job: acc += x[rows of my block, K] . A[ranks of my block, K]
+                    const int kn = min(kc, kv1 - (kv0 + j * kc));
+                    if (has_block) {
+                        const uint4 *xs = reinterpret_cast<const uint4 *>(sb) + (my_rb * 4) * kc;
+                        const uint4 *As = reinterpret_cast<const uint4 *>(sb + (size_t)Rp * kc * 16) + (my_jg * 4) * kc;
+                        const int jvalid = r - my_jg * 4;  // ranks of this block that exist
+                        for (int kv = ks; kv < kn; kv += KS) {
+                            uint4 av[4], xv[4];
 #pragma unroll
-                            for (int jj = 0; jj < JW; ++jj) {
-                                const int jr = warp + kCcWarps * jj;
-                                if (jr < r) {
-                                    const uint4 u = *reinterpret_cast<const uint4 *>(As + ((size_t)jr * kc + c) * 16);
-                                    E::to_f32(u, af[jj]);
-                                } else {
+                            for (int jj = 0; jj < 4; ++jj) av[jj] = jj < jvalid ? As[jj * kc + kv] : make_uint4(0, 0, 0, 0);
 #pragma unroll
-                                    for (int e = 0; e < V; ++e) af[jj][e] = 0.f;
-                                }
-                            }
+                            for (int i = 0; i < 4; ++i) xv[i] = xs[i * kc + kv];
 #pragma unroll
-                            for (int row = 0; row < RT; ++row) {
-                                if (row < R) {
-                                    const uint4 u = *reinterpret_cast<const uint4 *>(xs + ((size_t)row * kc + c) * 16);
-                                    float xf[V];
-                                    E::to_f32(u, xf);
+                            for (int qq = 0; qq < PV; ++qq) {
+                                float2 ap[4], xp[4];
 #pragma unroll
-                                    for (int jj = 0; jj < JW; ++jj)
+                                for (int jj = 0; jj < 4; ++jj) ap[jj] = pair_of<T>(av[jj], qq);
 #pragma unroll
-                                        for (int e = 0; e < V; ++e) acc[row][jj] = fmaf(xf[e], af[jj][e], acc[row][jj]);
-                                }
+                                for (int i = 0; i < 4; ++i) xp[i] = pair_of<T>(xv[i], qq);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                                    for (int jj = 0; jj < 4; ++jj) acc[i][jj] = __ffma2_rn(xp[i], ap[jj], acc[i][jj]);
                             }
                         }
                     }
-                    if (j == nK - 1) reduce_h();
+                    if (j == nK - 1) finish_shrink();
                 } else {
-                    // ---- expand job: y[row, col] += h[row, :] . B[col, :]
+                    // ---- expand job: y[rows, c..c+1] += h . B[c..c+1]^T
                     const int nb = nv0 + (j - nK) * nc, nn = min(nc, nv1 - nb);
-                    T *ys = reinterpret_cast<T *>(const_cast<unsigned char *>(st));
-                    const unsigned char *bs = st + (size_t)R * nc * 16;
-                    const int ncols = nn * V, ystride = nc * V;
-                    for (int c0 = tid; c0 < ncols; c0 += kCcThreads * kCcCpt) {
-                        float out[kCcCpt][RT];
+                    const int npairs = nn * V / 2;
+                    const uint4 *Bs = reinterpret_cast<const uint4 *>(sb + (size_t)R * nc * 16);
+                    const typename E::PairT *ys = reinterpret_cast<const typename E::PairT *>(sb);
+                    const int ystride = nc * V / 2;
+                    for (int cp = tid; cp < npairs; cp += kCcThreads) {
+                        const int c0 = 2 * cp, c1 = c0 + 1;
+                        const int col = nb * V + c0;
+                        const SliceDesc &S = p.slices[slice_of(p, col)];
+                        T *yg = static_cast<T *>(p.y) + S.y_col + (col - S.col_begin);
+                        for (int rb = 0; rb < nrb; ++rb) {
+                            float2 o0[4], o1[4];
 #pragma unroll
-                        for (int u = 0; u < kCcCpt; ++u)
+                            for (int i = 0; i < 4; ++i) o0[i] = o1[i] = make_float2(0.f, 0.f);
+                            for (int jc = 0; jc < rv; ++jc) {
+                                const uint4 b0 = Bs[c0 * rvp + b_swizzle(c0, jc, rvp)];
+                                const uint4 b1 = Bs[c1 * rvp + b_swizzle(c1, jc, rvp)];
 #pragma unroll
-                            for (int row = 0; row < RT; ++row) out[u][row] = 0.f;
-                        for (int cv = 0; cv < rv; ++cv) {
-                            float bf[kCcCpt][V];
+                                for (int qq = 0; qq < PV; qq += 2) {
+                                    const float2 p00 = pair_of<T>(b0, qq), p01 = pair_of<T>(b0, qq + 1);
+                                    const float2 p10 = pair_of<T>(b1, qq), p11 = pair_of<T>(b1, qq + 1);
 #pragma unroll
-                            for (int u = 0; u < kCcCpt; ++u) {
-                                const int col = c0 + u * kCcThreads;
-                                if (col < ncols) {
-                                    const uint4 w = *reinterpret_cast<const uint4 *>(bs + ((size_t)col * rv + cv) * 16);
-                                    E::to_f32(w, bf[u]);
-                                } else {
-#pragma unroll
-                                    for (int e = 0; e < V; ++e) bf[u][e] = 0.f;
-                                }
-                            }
-#pragma unroll
-                            for (int e = 0; e < V; e += 4) {
-                                const int jb = cv * V + e;
-#pragma unroll
-                                for (int row = 0; row < RT; ++row) {
-                                    if (row < R) {
-                                        const float4 h4 = *reinterpret_cast<const float4 *>(h_full + row * HP + jb);
-#pragma unroll
-                                        for (int u = 0; u < kCcCpt; ++u) {
-                                            float t = out[u][row];
-                                            t = fmaf(h4.x, bf[u][e + 0], t);
-                                            t = fmaf(h4.y, bf[u][e + 1], t);
-                                            t = fmaf(h4.z, bf[u][e + 2], t);
-                                            t = fmaf(h4.w, bf[u][e + 3], t);
-                                            out[u][row] = t;
-                                        }
+                                    for (int i = 0; i < 4; ++i) {
+                                        const float4 hh = *reinterpret_cast<const float4 *>(
+                                            h_full + (rb * 4 + i) * HP + jc * V + 2 * qq);
+                                        const float2 h0 = make_float2(hh.x, hh.y), h1 = make_float2(hh.z, hh.w);
+                                        o0[i] = __ffma2_rn(p00, h0, o0[i]);
+                                        o0[i] = __ffma2_rn(p01, h1, o0[i]);
+                                        o1[i] = __ffma2_rn(p10, h0, o1[i]);
+                                        o1[i] = __ffma2_rn(p11, h1, o1[i]);
                                     }
                                 }
                             }
-                        }
 #pragma unroll
-                        for (int u = 0; u < kCcCpt; ++u) {
-                            const int col = c0 + u * kCcThreads;
-                            if (col < ncols) {
-#pragma unroll
-                                for (int row = 0; row < RT; ++row) {
-                                    if (row < R) {
-                                        T *yp = ys + row * ystride + col;
-                                        E::store1(yp, E::load1(yp) + out[u][row]);
-                                    }
+                            for (int i = 0; i < 4; ++i) {
+                                const int row = rb * 4 + i;
+                                if (row < R) {
+                                    float2 yv = E::pair_to_f32(ys[row * ystride + cp]);
+                                    yv.x += o0[i].x + o0[i].y;
+                                    yv.y += o1[i].x + o1[i].y;
+                                    E::store_pair(yg + (int64_t)rows_s[row] * p.ldy, yv);
                                 }
                             }
-                        }
-                    }
-                    __syncthreads();
-                    for (int row = warp; row < R; row += kCcWarps) {
-                        const int64_t yrow = (int64_t)rows_s[row] * p.ldy;
-                        const unsigned char *src = st + (size_t)row * nc * 16;
-                        for (int c = lane; c < nn; c += 32) {
-                            const int col = (nb + c) * V;
-                            const SliceDesc &S = p.slices[slice_of(p, col)];
-                            T *dst = static_cast<T *>(p.y) + yrow + S.y_col + (col - S.col_begin);
-                            *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src + c * 16);
                         }
                     }
                 }
                 __syncthreads();
+                if (j + kCcStages < total) issue(j + kCcStages);
+                else cp_async_commit();
+            }
+            gjob += (uint32_t)total;
+            // Every CTA is done reading its receive buffer before any CTA
+            // pushes the next tile's partial h into it.
+            if (MODE != kExpand) {
+                cluster_arrive_release();
+                cluster_wait_acquire();
             }
         }
     }
-    // Keep this CTA's shared memory alive until every peer has finished its
-    // distributed-shared-memory reads.
-    if (MODE != kExpand) cluster_sync();
+    if (!wait_ok) raise_deverr(p.counts, LORA_DEVERR_WAIT);
 }
 
 // ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
-template <typename T, int MODE, int JW, int RT>
+static CcGeom cc_geometry(int r_max, int cluster) {
+    CcGeom g{};
+    g.RT = cc_rows_per_tile(r_max);
+    g.HP = (r_max + 7) & ~7;
+    int o = 0;
+    auto take = [&](int bytes) {
+        const int at = o;
+        o = (o + bytes + 127) & ~127;
+        return at;
+    };
+    g.off_bars = take(kCcStages * 8);
+    g.off_desc = take(32 * 4);
+    g.off_rows = take(g.RT * 4);
+    g.off_slots = take(256 * 16 * 4);
+    g.off_recv = take(cluster * g.RT * g.HP * 4);
+    g.off_hfull = take(g.RT * g.HP * 4);
+    g.off_ring = o;
+    const int budget = 225 * 1024;
+    g.stage_bytes = ((budget - o) / kCcStages) & ~127;
+    g.total = o + kCcStages * g.stage_bytes;
+    return g;
+}
+
+// Co-resident clusters for a kernel / cluster size / shared-memory size,
+// queried once and cached.
+struct ResidencyCache {
+    struct Entry {
+        const void *fn;
+        int dev, cluster, smem, value;
+    };
+    Entry e[64] = {};
+    int n = 0;
+    int get(const void *fn, int dev, int cluster, int smem) const {
+        for (int i = 0; i < n; ++i)
+            if (e[i].fn == fn && e[i].dev == dev && e[i].cluster == cluster && e[i].smem == smem) return e[i].value;
+        return -1;
+    }
+    void put(const void *fn, int dev, int cluster, int smem, int v) {
+        if (n < 64) e[n++] = {fn, dev, cluster, smem, v};
+    }
+};
+
+template <typename T, int MODE>
 static cudaError_t launch_cc_t(const DeltaArgs &p, int cluster, int sms, cudaStream_t stream) {
-    auto kern = sgmv_cc_kernel<T, MODE, JW, RT>;
-    constexpr int kSmemBudget = 200 * 1024;
-    const int fixed = 3 * RT * cc_hp(p.r_max) * 4 + RT * 4;
-    int stage_bytes = ((kSmemBudget - fixed) / kCcStages) & ~127;
-    const size_t smem = cc_smem_bytes<RT>(stage_bytes, p.r_max);
+    auto kern = sgmv_cc_kernel<T, MODE>;
+    const CcGeom g = cc_geometry(p.r_max, cluster);
     static DeviceOnce once;
     cudaError_t e = once.run([&] {
         return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     });
     if (e != cudaSuccess) return e;
 
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kCcThreads);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = g.total;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
 
-    // Co-resident clusters for this shape (queried once per device and
-    // cluster size; the answer does not depend on the batch).
-    static int resident[64][9] = {};
+    static ResidencyCache cache;
     int dev = 0;
     cudaGetDevice(&dev);
-    int max_clusters = sms / cluster;
-    if (dev >= 0 && dev < 64 && cluster <= 8) {
-        if (!resident[dev][cluster]) {
-            cfg.gridDim = dim3(cluster);
-            int active = 0;
-            if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess || active <= 0) {
-                cudaGetLastError();
-                active = sms / cluster;
-            }
-            resident[dev][cluster] = active;
+    int max_clusters = cache.get((const void *)kern, dev, cluster, g.total);
+    if (max_clusters < 0) {
+        cfg.gridDim = dim3(cluster);
+        cfg.numAttrs = 1;
+        int active = 0;
+        if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess || active <= 0) {
+            cudaGetLastError();
+            active = sms / cluster;
         }
-        max_clusters = resident[dev][cluster];
+        cfg.numAttrs = 2;
+        max_clusters = active;
+        cache.put((const void *)kern, dev, cluster, g.total, active);
     }
     int nclusters = p.max_list < max_clusters ? p.max_list : max_clusters;
     if (nclusters < 1) nclusters = 1;
     cfg.gridDim = dim3(nclusters * cluster);
-    e = cudaLaunchKernelEx(&cfg, kern, p, stage_bytes);
-    return e;
-}
-
-template <typename T, int MODE>
-static cudaError_t launch_cc_mode(const DeltaArgs &p, int cluster, int sms, cudaStream_t stream) {
-    const int jw = (p.r_max + kCcWarps - 1) / kCcWarps;
-    if (jw <= 1) return launch_cc_t<T, MODE, 1, 16>(p, cluster, sms, stream);
-    if (jw <= 2) return launch_cc_t<T, MODE, 2, 16>(p, cluster, sms, stream);
-    if (jw <= 4) return launch_cc_t<T, MODE, 4, 16>(p, cluster, sms, stream);
-    if (jw <= 8) return launch_cc_t<T, MODE, 8, 8>(p, cluster, sms, stream);
-    return launch_cc_t<T, MODE, 16, 4>(p, cluster, sms, stream);
+    return cudaLaunchKernelEx(&cfg, kern, p, g);
 }
 
 // Cluster size: enough CTAs per segment to spread one adapter's weights over
@@ -413,14 +507,15 @@ int cc_cluster_size(int d_in, int d_out) {
 }
 
 cudaError_t launch_cc(const DeltaArgs &p, int dtype, int mode, int cluster, int sms, cudaStream_t stream) {
+    if (cluster > kCcMaxCluster) cluster = kCcMaxCluster;
     if (dtype == LORA_F32) {
-        if (mode == kFused) return launch_cc_mode<float, kFused>(p, cluster, sms, stream);
-        if (mode == kShrink) return launch_cc_mode<float, kShrink>(p, cluster, sms, stream);
-        return launch_cc_mode<float, kExpand>(p, cluster, sms, stream);
+        if (mode == kFused) return launch_cc_t<float, kFused>(p, cluster, sms, stream);
+        if (mode == kShrink) return launch_cc_t<float, kShrink>(p, cluster, sms, stream);
+        return launch_cc_t<float, kExpand>(p, cluster, sms, stream);
     }
-    if (mode == kFused) return launch_cc_mode<__nv_bfloat16, kFused>(p, cluster, sms, stream);
-    if (mode == kShrink) return launch_cc_mode<__nv_bfloat16, kShrink>(p, cluster, sms, stream);
-    return launch_cc_mode<__nv_bfloat16, kExpand>(p, cluster, sms, stream);
+    if (mode == kFused) return launch_cc_t<__nv_bfloat16, kFused>(p, cluster, sms, stream);
+    if (mode == kShrink) return launch_cc_t<__nv_bfloat16, kShrink>(p, cluster, sms, stream);
+    return launch_cc_t<__nv_bfloat16, kExpand>(p, cluster, sms, stream);
 }
 
 }  // namespace lora

@@ -40,8 +40,18 @@ def _check_prepare(B, ids_np, n, chunk, tc_min=0):
     # path split: every segment in exactly one list, by its length
     thr = tc_min if tc_min > 0 else batch.raw.tc_min_rows
     lens = ref["seg_lens"]
-    assert np.array_equal(got["small_segs"].numpy(), np.nonzero(lens < thr)[0])
-    assert np.array_equal(got["tc_segs"].numpy(), np.nonzero(lens >= thr)[0])
+    recs = np.stack([ref["seg_indptr"][:-1], lens, ref["weight_indices"],
+                     np.arange(len(lens))], axis=1).astype(np.int32).reshape(-1, 4)
+    desc = got["seg_records"].numpy()
+    S = len(lens)
+    assert np.array_equal(desc[:S, :4], recs)
+    assert np.all(desc[S:, 1] == 0), "descriptors past the last segment must have len 0"
+    for s_ in range(S):
+        k = min(int(lens[s_]), 28)
+        st = int(ref["seg_indptr"][s_])
+        assert np.array_equal(desc[s_, 4:4 + k], ref["sorted_token_ids"][st:st + k])
+    assert np.array_equal(got["small_segs"].numpy().reshape(-1, 4), recs[lens < thr])
+    assert np.array_equal(got["tc_segs"].numpy().reshape(-1, 4), recs[lens >= thr])
     big = lens[lens >= thr]
     assert np.array_equal(got["tc_indptr"].numpy(), np.concatenate([[0], np.cumsum(big)]).astype(np.int32))
     assert got["device_error"] == 0

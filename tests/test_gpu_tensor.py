@@ -1,0 +1,108 @@
+"""GPU parity of the tensor-core (tcgen05) path against the CPU oracle,
+forced (PATH_TENSOR) and through the automatic split by segment length."""
+import numpy as np
+import pytest
+import torch
+
+from segmented_gather_gemv_gb300 import workloads as wl
+from tests._lora_case import TOL, active_rows, oracle_delta, rel_err, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from segmented_gather_gemv_gb300 import binding
+    binding.lib()
+    return binding
+
+
+def _run(B, w, path, tc_min=0):
+    d = to_dev(w)
+    batch = B.lora_prepare_batch(d["ids"], w.n_adapters, w.chunk_size, tc_min_rows=tc_min)
+    y = d["y"]
+    B.lora_delta(batch, d["x"], d["A"], d["B"], y, scale=w.scale, adapter_scale=d["adapter_scale"],
+                 ranks=d["ranks"], path=path)
+    torch.cuda.synchronize()
+    return y.float().cpu().numpy().astype(np.float64), batch
+
+
+def _check(w, y):
+    y_ref = oracle_delta(w)
+    act = active_rows(w)
+    err = rel_err(y, y_ref, w.y.astype(np.float64), act)
+    assert err <= TOL[w.dtype], "rel err %.3e" % err
+    assert np.array_equal(y[~act], w.y[~act].astype(np.float64)), "inactive rows changed"
+    assert np.isfinite(y).all()
+    return err
+
+
+TC_CASES = [
+    dict(M=128, d_in=256, d_outs=[128], n_pool=1, r_max=16, run_len=128),        # one full tile
+    dict(M=200, d_in=512, d_outs=[384], n_pool=3, r_max=16, run_len=50),         # several segments
+    dict(M=300, d_in=1000, d_outs=[776], n_pool=4, r_max=32, run_len=100),       # ragged d_in / d_out
+    dict(M=333, d_in=4096, d_outs=[4096], n_pool=6, r_max=16, run_len=111),      # decode-like widths
+    dict(M=257, d_in=520, d_outs=[264, 64, 136], n_pool=5, r_max=64, run_len=40,
+         ranks=[8, 16, 32, 64], per_adapter_scale=True),                         # slices, mixed ranks
+    dict(M=180, d_in=192, d_outs=[256], n_pool=7, r_max=24, run_len=3),          # scattered rows
+    dict(M=64, d_in=128, d_outs=[128], n_pool=2, r_max=8, run_len=64),
+]
+
+
+@pytest.mark.parametrize("ci", range(len(TC_CASES)))
+def test_tensor_path_forced(B, ci):
+    w = wl.random_batch(seed=400 + ci, dtype="bf16", **TC_CASES[ci])
+    y, batch = _run(B, w, path=B.PATH_TENSOR)
+    _check(w, y)
+    assert batch.counts()["device_error"] == 0
+
+
+@pytest.mark.parametrize("chunk", [0, 64, 48])
+def test_tensor_path_chunks_merge(B, chunk):
+    w = wl.random_batch(seed=420, M=700, d_in=384, d_outs=[512], n_pool=5, r_max=16,
+                        run_len=175, dtype="bf16", chunk_size=chunk)
+    y, _ = _run(B, w, path=B.PATH_TENSOR)
+    _check(w, y)
+
+
+def test_tensor_path_nan_padding(B):
+    w = wl.random_batch(seed=430, M=256, d_in=512, d_outs=[384], n_pool=8, r_max=64,
+                        ranks=[8, 16, 32, 64], run_len=32, dtype="bf16", pad_value=float("nan"),
+                        per_adapter_scale=True)
+    y, _ = _run(B, w, path=B.PATH_TENSOR)
+    _check(w, y)
+
+
+def test_tensor_path_rank_too_large_flags(B):
+    w = wl.random_batch(seed=431, M=128, d_in=256, d_outs=[128], n_pool=2, r_max=128,
+                        run_len=64, dtype="bf16", ranks=np.array([128, 64], np.int32))
+    y, batch = _run(B, w, path=B.PATH_TENSOR)
+    assert batch.counts()["device_error"] & B.DEVERR_RANK
+
+
+@pytest.mark.parametrize("tc_min", [1, 16, 40])
+def test_auto_split_mixed_lengths(B, tc_min):
+    # prefill-like runs and decode-like single rows in one batch
+    w = wl.mixed_serving(n_prefill_seq=3, prefill_rows=600, len_lo=64, len_hi=400, n_decode=90,
+                         n_pool=16, r=32, d_in=1024, d_outs=(512, 256, 256))
+    y, batch = _run(B, w, path=B.PATH_AUTO, tc_min=tc_min)
+    _check(w, y)
+    c = batch.counts()
+    assert c["num_tc_segs"] + c["num_small_segs"] == c["num_segs"]
+
+
+def test_auto_split_odd_rank_goes_to_cuda_cores(B):
+    w = wl.random_batch(seed=440, M=300, d_in=256, d_outs=[256], n_pool=4, r_max=16, run_len=100,
+                        ranks=np.array([12, 16, 4, 8], np.int32), dtype="bf16")
+    y, batch = _run(B, w, path=B.PATH_AUTO, tc_min=16)
+    _check(w, y)
+    assert batch.counts()["device_error"] == 0
+
+
+def test_tensor_and_cuda_core_paths_agree(B):
+    w = wl.prefill(n_seq=4, len_lo=100, len_hi=300, d_in=1024, d_out=2048)
+    y_tc, _ = _run(B, w, path=B.PATH_TENSOR)
+    y_cc, _ = _run(B, w, path=B.PATH_CUDA_CORE)
+    base = w.y.astype(np.float64)
+    assert rel_err(y_tc, y_cc, base) <= 1e-2
+    _check(w, y_tc)
