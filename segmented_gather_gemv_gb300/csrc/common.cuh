@@ -85,8 +85,8 @@ std::atomic<int64_t> &launch_counter();
 
 constexpr uint32_t kBatchMagic = 0x4C6F5241u;  // "LoRA"
 constexpr int kDefaultTcMinRows = 64;
-constexpr int kTcMaxRankCommon = 64;
-// Ranks the tensor-core kernel computes (exact 8-column masking, <= 64).
+constexpr int kTcMaxRankCommon = 32;
+// Ranks the tensor-core kernel computes (exact 8-column masking, <= 32).
 __host__ __device__ __forceinline__ bool tc_rank_ok(int r) { return r > 0 && r <= kTcMaxRankCommon && (r & 7) == 0; }
 
 // ---------------------------------------------------------------------------
@@ -102,6 +102,11 @@ __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc, int
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(smem_dst)),
                  "l"(gsrc), "r"(src_bytes)
                  : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the arrival is counted in the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar)) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>
@@ -183,38 +188,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
-    return t;
-}
-// Longest a kernel waits on one barrier before it gives up (ns).  Real waits
-// last microseconds; the limit only ends a wait that can no longer complete.
-constexpr uint64_t kWaitLimitNs = 100ull * 1000 * 1000;
+// Longest a kernel waits on one barrier before it gives up, in SM clock
+// cycles (about 0.1 s at 2 GHz).  Real waits last microseconds; the limit only
+// ends a wait that can no longer complete.  The SM-local cycle counter is
+// read every 64 polls so that polling stays cheap.
+constexpr long long kWaitLimitCycles = 200ll * 1000 * 1000;
 // Bounded wait for phase `parity` of `bar`.  Returns false if the barrier did
 // not complete in time (the caller flags an error; it never spins forever).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
+    const long long deadline = clock64() + kWaitLimitCycles;
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() > deadline) return false;
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (clock64() > deadline) return false;
     }
 }
 // As mbar_wait, but also gives up as soon as another role of the CTA has
 // set `*abort`, and sets it on its own timeout.
 __device__ __forceinline__ bool mbar_wait_abort(uint64_t *bar, uint32_t parity, volatile int *abort) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
+    const long long deadline = clock64() + kWaitLimitCycles;
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (globaltimer_ns() > deadline) {
+        if (clock64() > deadline) {
             *abort = 1;
             return false;
         }
     }
 }
+
 // Bulk (non-tensor) async copy global -> shared, completing on `bar`.
 // Both addresses 16-byte aligned, `bytes` a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {

@@ -15,9 +15,10 @@
 // Latency: a segment is reached through one 128-byte descriptor that holds
 // its first rows inline, so every load address of the tile is known after a
 // single dependent read.  All x/A (shrink) and y/B (expand) bytes of a tile
-// are then requested at once: x, A and y rows by bulk async copies completing
-// on one mbarrier per ring stage, B rows by 16-byte cp.async into an
-// XOR-swizzled layout, reading B only up to the adapter's rank.
+// are then requested at once with 16-byte cp.async (gathered rows cost the
+// same as contiguous ones; bulk async copies of row pieces are far slower on
+// row-gathered data); B rows land in an XOR-swizzled layout and are read only
+// up to the adapter's rank.
 //
 // Compute (fp32, packed FFMA2): shrink -- every thread owns a 4-row x 4-rank
 // block of h and strides over K with its accumulators live across all K
@@ -103,7 +104,6 @@ __global__ void __launch_bounds__(kCcThreads, 1)
     constexpr int V = E::kVec;
     constexpr int PV = V / 2;
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + g.off_bars);
     int32_t *desc_s = reinterpret_cast<int32_t *>(smem + g.off_desc);  // [32]
     int32_t *rows_s = reinterpret_cast<int32_t *>(smem + g.off_rows);  // [RT]
     float *slots = reinterpret_cast<float *>(smem + g.off_slots);      // [warp][16]
@@ -116,11 +116,6 @@ __global__ void __launch_bounds__(kCcThreads, 1)
     const uint32_t cid = cluster_id_x(), ncl = nclusters_x();
     const int RT = g.RT, HP = g.HP, SB = g.stage_bytes;
 
-    if (tid == 0) {
-        for (int s = 0; s < kCcStages; ++s) mbar_init(&bars[s], 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
     griddep_launch_dependents();
     griddep_wait();
 
@@ -131,7 +126,6 @@ __global__ void __launch_bounds__(kCcThreads, 1)
     const T *xg = static_cast<const T *>(p.x);
     const T *Ag = static_cast<const T *>(p.A);
     uint32_t gjob = 0;  // jobs issued so far by this CTA (ring position and barrier phase)
-    bool wait_ok = true;
 
     for (int li = (int)cid; li < p.max_list; li += (int)ncl) {
         __syncthreads();  // the previous segment is done with desc_s / rows_s
@@ -181,40 +175,31 @@ __global__ void __launch_bounds__(kCcThreads, 1)
             }
             const int total = nK + nN;
 
-            // ---- issue one job into its stage (called by every thread).
+            // ---- issue one job into its stage (called by every thread): all
+            // loads are 16-byte cp.async, so rows gathered from anywhere cost
+            // no more than contiguous ones.
             auto issue = [&](int j) {
                 const uint32_t G = gjob + j;
                 unsigned char *sb = ring + (size_t)(G % kCcStages) * SB;
-                uint64_t *bar = &bars[G % kCcStages];
                 if (j < nK) {
                     const int kb = kv0 + j * kc, kn = min(kc, kv1 - kb);
-                    if (warp == 0) {
-                        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)((R + r) * kn * 16));
-                        __syncwarp();
-                        for (int row = lane; row < R + r; row += 32) {
-                            const T *src = row < R ? xg + (int64_t)rows_s[row] * p.ldx + (int64_t)kb * V
-                                                   : Ag + (int64_t)a * p.a_stride_adapter +
-                                                         (int64_t)(row - R) * p.a_stride_r + (int64_t)kb * V;
-                            const int srow = row < R ? row : Rp + (row - R);
-                            bulk_g2s(sb + (size_t)srow * kc * 16, src, (uint32_t)kn * 16, bar);
-                        }
+                    for (int row = warp; row < R + r; row += kCcThreads / 32) {
+                        const T *src = row < R ? xg + (int64_t)rows_s[row] * p.ldx + (int64_t)kb * V
+                                               : Ag + (int64_t)a * p.a_stride_adapter +
+                                                     (int64_t)(row - R) * p.a_stride_r + (int64_t)kb * V;
+                        unsigned char *dst = sb + (size_t)(row < R ? row : Rp + (row - R)) * kc * 16;
+                        for (int c = lane; c < kn; c += 32) cp_async16(dst + c * 16, src + c * V, 16);
                     }
                 } else {
                     const int nb = nv0 + (j - nK) * nc, nn = min(nc, nv1 - nb);
-                    const int c0 = nb * V, c1 = (nb + nn) * V;
-                    if (warp == 0) {
-                        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(R * nn * 16));
-                        __syncwarp();
-                        for (int t = 0; t < p.n_slices; ++t) {
-                            const SliceDesc &S = p.slices[t];
-                            const int lo = max(c0, S.col_begin), hi = min(c1, S.col_begin + S.d_out);
-                            if (lo >= hi) continue;
-                            for (int row = lane; row < R; row += 32) {
-                                const T *src = static_cast<const T *>(p.y) + (int64_t)rows_s[row] * p.ldy + S.y_col +
-                                               (lo - S.col_begin);
-                                bulk_g2s(sb + (size_t)row * nc * 16 + (size_t)(lo - c0) * sizeof(T), src,
-                                         (uint32_t)((hi - lo) * sizeof(T)), bar);
-                            }
+                    const int c0 = nb * V;
+                    for (int row = warp; row < R; row += kCcThreads / 32) {
+                        const int64_t yrow = (int64_t)rows_s[row] * p.ldy;
+                        unsigned char *dst = sb + (size_t)row * nc * 16;
+                        for (int c = lane; c < nn; c += 32) {
+                            const int col = c0 + c * V;
+                            const SliceDesc &S = p.slices[slice_of(p, col)];
+                            cp_async16(dst + c * 16, static_cast<const T *>(p.y) + yrow + S.y_col + (col - S.col_begin), 16);
                         }
                     }
                     unsigned char *bst = sb + (size_t)R * nc * 16;
@@ -309,7 +294,6 @@ __global__ void __launch_bounds__(kCcThreads, 1)
 #pragma unroll 1
             for (int j = 0; j < total; ++j) {
                 const uint32_t G = gjob + j;
-                if (tid == 0 && !mbar_wait(&bars[G % kCcStages], (G / kCcStages) & 1)) wait_ok = false;
                 cp_async_wait<kCcStages - 1>();
                 __syncthreads();
                 const unsigned char *sb = ring + (size_t)(G % kCcStages) * SB;
@@ -402,7 +386,6 @@ __global__ void __launch_bounds__(kCcThreads, 1)
             }
         }
     }
-    if (!wait_ok) raise_deverr(p.counts, LORA_DEVERR_WAIT);
 }
 
 // ---------------------------------------------------------------------------

@@ -13,40 +13,47 @@
 //
 // Per tile:
 //   shrink  D1[128 x r] (TMEM, fp32) = x_tile[128 x d_in] . A_a^T, K in
-//           64-element blocks, operands staged by TMA (128-byte swizzle);
+//           64-element blocks, operands staged in the 128-byte swizzle;
 //   scale   the epilogue warps read D1, multiply by s_a, round to bf16 and
 //           write H[128 x r] to shared memory (never to global memory);
-//   expand  per 128-column n-tile: D2[128 x 128] (TMEM, double buffered)
-//           = H . B_a[cols]^T, B staged by TMA;
-//   store   y_tile += D2 in fp32, rounded once to bf16; y rows are loaded and
-//           stored with bulk async copies.
+//   expand  per 128-column n-tile: D2[128 x 128] (TMEM, triple buffered)
+//           = H . B_a[cols]^T;
+//   store   y_tile += D2 in fp32, rounded once to bf16, stored from registers.
 // Ranks are masked exactly: A rows / B columns at or past the adapter's rank
-// are either never read into a live accumulator column or fetched from an
-// out-of-range TMA coordinate (zero fill), so padding never reaches y.
+// are zero-filled in shared memory (never read), so padding never reaches y.
 //
-// Warp roles (224 threads): warp 0 x/A/B producer, warp 1 MMA issuer (one
-// thread) and TMEM owner, warp 2 y producer, warps 3..6 epilogue (warp w
-// owns TMEM lanes 32 (w % 4) .. +31, i.e. tile rows).
-#include <cudaTypedefs.h>
-
+// Warp roles (448 threads): warps 0-1 x/A loaders, warp 2 MMA issuer (one
+// thread) and TMEM owner, warp 3 B loader, warps 4-5 y loaders, warps 6..13
+// epilogue (warp w
+// owns TMEM lanes 32 (w % 4) .. +31, i.e. tile rows, and one half of the
+// columns of every n-tile; four of them also build H).
+//
+// Loads are 16-byte cp.async issued by the loader warps (they write the
+// swizzled operand layouts themselves and signal the stage barrier with
+// cp.async.mbarrier.arrive.noinc): rows gathered through sorted_token_ids
+// are 128- or 256-byte pieces of rows far apart, and bulk / tensor async
+// copies of such pieces run several times slower than 16-byte copies.
 #include "common.cuh"
 
 namespace lora {
 
-constexpr int kTcThreads = 224;
+constexpr int kTcThreads = 448;
 constexpr int kBM = 128;        // tile rows (MMA M)
-constexpr int kBK = 64;         // shrink K block (128 bytes of bf16)
+constexpr int kBK = 128;        // shrink K block: two 64-element (128-byte) swizzle atoms
 constexpr int kBN = 128;        // expand n-tile (MMA N)
-constexpr int kSX = 4;          // x/A stages
-constexpr int kSB = 2;          // B stages
-constexpr int kSY = 2;          // y stages
+constexpr int kSX = 2;          // x/A stages
+constexpr int kSB = 4;          // B stages
+constexpr int kSY = 3;          // y stages
 constexpr int kST = 3;          // TMEM D2 buffers
-constexpr int kTcMaxRank = 64;  // ranks above this use the CUDA-core kernel
+constexpr int kTcMaxRank = 32;  // ranks above this use the CUDA-core kernel
+constexpr int kSnapRows = 16;   // CTA row ranges end on a segment boundary this close
 constexpr int kYPitch = kBN * 2 + 16;  // bytes per y row in a y stage (padded)
 
 // Shared-memory layout (bytes, from a 1024-aligned base).
-constexpr int kXBytes = kBM * 128;                   // 16 KB
-constexpr int kABytes = kTcMaxRank * 128;            // 8 KB
+constexpr int kXAtom = kBM * 128;                    // 16 KB: 128 rows x 64 columns
+constexpr int kAAtom = kTcMaxRank * 128;             // 4 KB: 32 rank rows x 64 columns
+constexpr int kXBytes = 2 * kXAtom;                  // 32 KB
+constexpr int kABytes = 2 * kAAtom;                  // 8 KB
 constexpr int kXStage = kXBytes + kABytes;           // 24 KB
 constexpr int kBChunk = kBN * 16;                    // 2 KB: 8 rank columns x 128 rows
 constexpr int kBStage = (kTcMaxRank / 8) * kBChunk;  // 16 KB
@@ -57,36 +64,16 @@ constexpr int kOffX = 0;
 constexpr int kOffB = kOffX + kSX * kXStage;
 constexpr int kOffH = kOffB + kSB * kBStage;
 constexpr int kOffY = kOffH + kHBytes;
-constexpr int kOffRows = kOffY + kSY * kYStage;      // 3 x 128 ints (per role)
+constexpr int kOffRows = kOffY + kSY * kYStage;      // 3 x 128 ints (per loader role)
 constexpr int kOffBars = kOffRows + 3 * kBM * 4;
 constexpr int kNumBars = 2 * kSX + 2 * kSB + 2 * kSY + 3 + 2 * kST + 1;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kTcSmem = kOffMisc + 64 + 1024;        // + alignment slack
 
-struct TcMaps {
-    CUtensorMap x8;                      // x, box {64, 8}, 128B swizzle
-    CUtensorMap x1;                      // x, box {64, 1}, 128B swizzle
-    CUtensorMap a;                       // A pool [n][r_max][d_in], box {64, 16, 1}, 128B swizzle
-    CUtensorMap b[LORA_MAX_SLICES];      // B pools [n][d_out][r_max], box {8, 128, 1}, no swizzle
-};
 
 // ---------------------------------------------------------------------------
 // Device helpers.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void tma2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
-            smem_u32(dst)),
-        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-__device__ __forceinline__ void tma3d(void *dst, const CUtensorMap *map, int x, int y, int z, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-        "[%5];\n" ::"r"(smem_u32(dst)),
-        "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-        : "memory");
-}
 __device__ __forceinline__ void bulk_s2g(void *gdst, const void *ssrc, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(gdst), "r"(smem_u32(ssrc)),
                  "r"(bytes)
@@ -218,7 +205,7 @@ __device__ __forceinline__ void ntile_cols(const DeltaArgs &p, int nt, int &slic
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
-    sgmv_tc_kernel(const __grid_constant__ DeltaArgs p, const __grid_constant__ TcMaps maps) {
+    sgmv_tc_kernel(const __grid_constant__ DeltaArgs p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBars);
@@ -230,18 +217,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
-        for (int s = 0; s < kSX; ++s) { mbar_init(&xf[s], 1); mbar_init(&xe[s], 1); }
-        for (int s = 0; s < kSB; ++s) { mbar_init(&bf[s], 1); mbar_init(&be[s], 1); }
-        for (int s = 0; s < kSY; ++s) { mbar_init(&yf[s], 1); mbar_init(&ye[s], 128); }
+        for (int s = 0; s < kSX; ++s) { mbar_init(&xf[s], 64); mbar_init(&xe[s], 1); }
+        for (int s = 0; s < kSB; ++s) { mbar_init(&bf[s], 32); mbar_init(&be[s], 1); }
+        for (int s = 0; s < kSY; ++s) { mbar_init(&yf[s], 64); mbar_init(&ye[s], 256); }
         mbar_init(d1f, 1);
         mbar_init(hr, 128);
         mbar_init(he, 1);
-        for (int s = 0; s < kST; ++s) { mbar_init(&tf[s], 1); mbar_init(&te[s], 128); }
+        for (int s = 0; s < kST; ++s) { mbar_init(&tf[s], 1); mbar_init(&te[s], 256); }
         mbar_init(fin, 1);
         fence_mbar_init();
         *abort = 0;
     }
-    if (warp == 1) {
+    if (warp == 2) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(smem_u32(tmem_slot))
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
@@ -257,73 +244,107 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int nseg = min(p.counts[p.tc_count_index], p.max_list);
     const int Mrows = p.counts[p.tc_rows_index];
     const int G = gridDim.x, b = blockIdx.x;
-    TileWalker walker{&p, (int)((int64_t)Mrows * b / G), (int)((int64_t)Mrows * (b + 1) / G), nseg};
-    if (nseg <= 0) walker.r = walker.r1;
+    TileWalker walker{&p, 0, 0, nseg};
+    if (nseg > 0) {
+        // Equal row shares, each end moved to a segment boundary that lies
+        // within kSnapRows: a tile costs a full pass over the K blocks and
+        // n-tiles however few rows it holds, so a CTA should not end a few
+        // rows into the next segment.  Both neighbours compute the same end.
+        auto snap = [&](int r) {
+            if (r <= 0 || r >= Mrows) return r <= 0 ? 0 : Mrows;
+            const int i = walker.seg_of(r);
+            const int lo = p.tc_ptr[i], hi = p.tc_ptr[i + 1];
+            if (r - lo <= kSnapRows) return lo;
+            if (hi - r <= kSnapRows) return hi;
+            return r;
+        };
+        walker.r = snap((int)((int64_t)Mrows * b / G));
+        walker.r1 = snap((int)((int64_t)Mrows * (b + 1) / G));
+        if (walker.r1 < walker.r) walker.r1 = walker.r;
+    }
 
     int n_nt = 0;
     for (int t = 0; t < p.n_slices; ++t) n_nt += (p.slices[t].d_out + kBN - 1) / kBN;
     const int nkb = (p.d_in + kBK - 1) / kBK;
-    const int rk8_oob = (p.r_max + 7) & ~7;  // a column coordinate past every rank column
+    // Every CTA walks the K blocks and the n-tiles from its own starting
+    // point.  Rows of x and y are a power-of-two stride apart; if all CTAs
+    // read the same column block at the same time, their requests fall on the
+    // same memory channels.
+    const int kb_rot = (int)(((uint32_t)b * 2654435761u) >> 7) % nkb;
+    const int nt_rot = (int)(((uint32_t)b * 2246822519u) >> 7) % (n_nt > 0 ? n_nt : 1);
     bool ok = true;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ x/A/B producer
+    if (warp < 2) {
+        // ------------------------------------------------------------ x/A loaders
+        const int lt = tid;  // 0..63
         int32_t *rows = reinterpret_cast<int32_t *>(smem + kOffRows);
-        uint32_t xs = 0, bs = 0;
+        const __nv_bfloat16 *xg = static_cast<const __nv_bfloat16 *>(p.x);
+        const __nv_bfloat16 *Ag = static_cast<const __nv_bfloat16 *>(p.A);
+        uint32_t xs = 0;
         Tile t;
         while (walker.next(t)) {
             const int r = p.ranks ? p.ranks[t.a] : p.r_max;
             const bool live = r <= p.r_max && tc_rank_ok(r);
             if (!live) continue;
-            __syncwarp();
-            for (int i = lane; i < t.n; i += 32) rows[i] = p.sorted[t.pos + i];
-            __syncwarp();
+            asm volatile("bar.sync 1, 64;\n" ::: "memory");  // previous tile done with rows
+            for (int i = lt; i < t.n; i += 64) rows[i] = p.sorted[t.pos + i];
+            asm volatile("bar.sync 1, 64;\n" ::: "memory");
             const int n16 = (r + 15) / 16;
-            for (int kb = 0; kb < nkb; ++kb, ++xs) {
+            const __nv_bfloat16 *Aa = Ag + (int64_t)t.a * p.a_stride_adapter;
+            for (int kbi = 0; kbi < nkb; ++kbi, ++xs) {
+                const int kb = kbi + kb_rot < nkb ? kbi + kb_rot : kbi + kb_rot - nkb;
                 const int s = xs % kSX;
                 if (!wait_warp(&xe[s], ((xs / kSX) & 1) ^ 1, ok, abort)) goto role_done;
                 unsigned char *xst = smem + kOffX + s * kXStage;
-                if (lane == 0) {
-                    const int ngroups = (t.n + 7) / 8;
-                    uint32_t bytes = (uint32_t)n16 * 16 * 128;
-                    for (int g8 = 0; g8 < ngroups; ++g8) {
-                        const int nv = min(8, t.n - 8 * g8);
-                        const bool contig = rows[8 * g8 + nv - 1] - rows[8 * g8] == nv - 1;
-                        bytes += contig ? 8 * 128 : nv * 128;
-                    }
-                    mbar_arrive_expect_tx(&xf[s], bytes);
-                    for (int g8 = 0; g8 < ngroups; ++g8) {
-                        const int nv = min(8, t.n - 8 * g8);
-                        const int r0 = rows[8 * g8];
-                        if (rows[8 * g8 + nv - 1] - r0 == nv - 1) {
-                            tma2d(xst + g8 * 1024, &maps.x8, kb * kBK, r0, &xf[s]);
-                        } else {
-                            for (int i = 0; i < nv; ++i)
-                                tma2d(xst + (8 * g8 + i) * 128, &maps.x1, kb * kBK, rows[8 * g8 + i], &xf[s]);
-                        }
-                    }
-                    for (int j = 0; j < n16; ++j)
-                        tma3d(xst + kXBytes + j * 16 * 128, &maps.a, kb * kBK, 16 * j, t.a, &xf[s]);
+                // x rows: 16 chunks of 16 bytes per row (256 contiguous bytes),
+                // two 64-column atoms in the 128-byte swizzle
+                for (int e = lt; e < t.n * 16; e += 64) {
+                    const int i = e >> 4, c = e & 15, k = kb * kBK + c * 8;
+                    const __nv_bfloat16 *row = xg + (int64_t)rows[i] * p.ldx;
+                    cp_async16(xst + (c >> 3) * kXAtom + i * 128 + (((c & 7) ^ (i & 7)) << 4), k < p.d_in ? row + k : row,
+                               k < p.d_in ? 16 : 0);
                 }
-                __syncwarp();
-            }
-            const int n8 = r / 8, n8mma = 2 * n16;  // loaded rank chunks / chunks the MMA reads
-            for (int nt = 0; nt < n_nt; ++nt, ++bs) {
-                const int s = bs % kSB;
-                if (!wait_warp(&be[s], ((bs / kSB) & 1) ^ 1, ok, abort)) goto role_done;
-                if (lane == 0) {
-                    int sl, c0, nc;
-                    ntile_cols(p, nt, sl, c0, nc);
-                    unsigned char *bst = smem + kOffB + s * kBStage;
-                    mbar_arrive_expect_tx(&bf[s], (uint32_t)n8mma * kBChunk);
-                    for (int c = 0; c < n8mma; ++c)
-                        tma3d(bst + c * kBChunk, &maps.b[sl], c < n8 ? 8 * c : rk8_oob, c0, t.a, &bf[s]);
+                // A rows of the adapter (rows >= rank zero-filled)
+                for (int e = lt; e < 16 * n16 * 16; e += 64) {
+                    const int j = e >> 4, c = e & 15, k = kb * kBK + c * 8;
+                    const bool in = j < r && k < p.d_in;
+                    cp_async16(xst + kXBytes + (c >> 3) * kAAtom + j * 128 + (((c & 7) ^ (j & 7)) << 4),
+                               in ? Aa + (int64_t)j * p.a_stride_r + k : Aa, in ? 16 : 0);
                 }
-                __syncwarp();
+                cp_async_arrive_noinc(&xf[s]);
             }
         }
-    } else if (warp == 2) {
-        // ------------------------------------------------------------ y producer
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ B loader
+        uint32_t bs = 0;
+        Tile t;
+        while (walker.next(t)) {
+            const int r = p.ranks ? p.ranks[t.a] : p.r_max;
+            const bool live = r <= p.r_max && tc_rank_ok(r);
+            if (!live) continue;
+            const int n16 = (r + 15) / 16, n8mma = 2 * n16, sh8 = n16 == 1 ? 1 : 2;
+            for (int nti = 0; nti < n_nt; ++nti, ++bs) {
+                const int nt = nti + nt_rot < n_nt ? nti + nt_rot : nti + nt_rot - n_nt;
+                int sl, c0, nc;
+                ntile_cols(p, nt, sl, c0, nc);
+                const SliceDesc &S = p.slices[sl];
+                // B rows c0 .. c0+127 of this slice, 8 rank columns per 2 KB chunk
+                const int sb = bs % kSB;
+                if (!wait_warp(&be[sb], ((bs / kSB) & 1) ^ 1, ok, abort)) goto role_done;
+                unsigned char *bst = smem + kOffB + sb * kBStage;
+                const __nv_bfloat16 *Ba = static_cast<const __nv_bfloat16 *>(S.B) + (int64_t)t.a * S.stride_adapter;
+                for (int e = lane; e < kBN * n8mma; e += 32) {
+                    const int n = e >> sh8, c = e & (n8mma - 1);
+                    const bool in = c0 + n < S.d_out && c * 8 < r;
+                    cp_async16(bst + c * kBChunk + n * 16, in ? Ba + (int64_t)(c0 + n) * S.stride_n + c * 8 : Ba,
+                               in ? 16 : 0);
+                }
+                cp_async_arrive_noinc(&bf[sb]);
+            }
+        }
+    } else if (warp == 4 || warp == 5) {
+        // ------------------------------------------------------------ y loaders
+        const int lt = tid - 128;  // 0..63
         int32_t *rows = reinterpret_cast<int32_t *>(smem + kOffRows + kBM * 4);
         uint32_t ys = 0;
         Tile t;
@@ -331,27 +352,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int r = p.ranks ? p.ranks[t.a] : p.r_max;
             const bool live = r <= p.r_max && tc_rank_ok(r);
             if (!live) continue;
-            __syncwarp();
-            for (int i = lane; i < t.n; i += 32) rows[i] = p.sorted[t.pos + i];
-            __syncwarp();
-            for (int nt = 0; nt < n_nt; ++nt, ++ys) {
-                const int s = ys % kSY;
-                if (!wait_warp(&ye[s], ((ys / kSY) & 1) ^ 1, ok, abort)) goto role_done;
+            asm volatile("bar.sync 2, 64;\n" ::: "memory");  // previous tile done with rows
+            for (int i = lt; i < t.n; i += 64) rows[i] = p.sorted[t.pos + i];
+            asm volatile("bar.sync 2, 64;\n" ::: "memory");
+            for (int nti = 0; nti < n_nt; ++nti, ++ys) {
+                const int nt = nti + nt_rot < n_nt ? nti + nt_rot : nti + nt_rot - n_nt;
                 int sl, c0, nc;
                 ntile_cols(p, nt, sl, c0, nc);
                 const SliceDesc &S = p.slices[sl];
-                if (lane == 0) mbar_arrive_expect_tx(&yf[s], (uint32_t)(t.n * nc * 2));
-                __syncwarp();
-                unsigned char *yst = smem + kOffY + s * kYStage;
-                for (int i = lane; i < t.n; i += 32) {
-                    const __nv_bfloat16 *src =
-                        static_cast<const __nv_bfloat16 *>(p.y) + (int64_t)rows[i] * p.ldy + S.y_col + c0;
-                    bulk_g2s(yst + i * kYPitch, src, (uint32_t)(nc * 2), &yf[s]);
+                const int sy = ys % kSY;
+                if (!wait_warp(&ye[sy], ((ys / kSY) & 1) ^ 1, ok, abort)) goto role_done;
+                unsigned char *yst = smem + kOffY + sy * kYStage;
+                const int nch = nc >> 3;
+                const __nv_bfloat16 *yc = static_cast<const __nv_bfloat16 *>(p.y) + S.y_col + c0;
+                if (nch == kBN / 8) {
+                    for (int e = lt; e < t.n * (kBN / 8); e += 64) {
+                        const int i = e >> 4, c = e & 15;
+                        cp_async16(yst + i * kYPitch + c * 16, yc + (int64_t)rows[i] * p.ldy + c * 8, 16);
+                    }
+                } else {
+                    for (int e = lt; e < t.n * nch; e += 64) {
+                        const int i = e / nch, c = e - i * nch;
+                        cp_async16(yst + i * kYPitch + c * 16, yc + (int64_t)rows[i] * p.ldy + c * 8, 16);
+                    }
                 }
-                __syncwarp();
+                cp_async_arrive_noinc(&yf[sy]);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 2) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             uint32_t xs = 0, bs = 0, ts = 0, tiles = 0;
@@ -367,15 +395,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint32_t id1 = idesc_bf16(kBM, 16 * n16);
                 // D1 is free again: the previous tile's expand was issued only
                 // after the epilogue had read D1 (hr).
-                for (int kb = 0; kb < nkb; ++kb, ++xs) {
+                for (int kbi = 0; kbi < nkb; ++kbi, ++xs) {
                     const int s = xs % kSX;
                     if (!wait1(&xf[s], (xs / kSX) & 1, ok, abort)) goto role_done;
                     tc_fence_after();
                     const uint32_t xa = x_base + s * kXStage, aa = xa + kXBytes;
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        umma(tmem, smem_desc(xa + kk * 32, 16, 1024, kLayoutSw128),
-                             smem_desc(aa + kk * 32, 16, 1024, kLayoutSw128), id1, (kb | kk) != 0);
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kXAtom + (kk & 3) * 32, aoff = (kk >> 2) * kAAtom + (kk & 3) * 32;
+                        umma(tmem, smem_desc(xa + off, 16, 1024, kLayoutSw128),
+                             smem_desc(aa + aoff, 16, 1024, kLayoutSw128), id1, (kbi | kk) != 0);
+                    }
                     umma_commit(&xe[s]);
                 }
                 umma_commit(d1f);
@@ -401,8 +431,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int q4 = warp & 3;            // TMEM lane quadrant
-        const int row = q4 * 32 + lane;     // tile row owned by this thread
+        const int q4 = warp & 3;              // TMEM lane quadrant
+        const int chalf = (warp - 6) >> 2;    // which 64 columns of an n-tile
+        const int row = q4 * 32 + lane;       // tile row owned by this thread
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         unsigned char *H = smem + kOffH;
         uint32_t ys = 0, ts = 0, tiles = 0;
@@ -413,43 +444,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!live) {
                 // Tiles the tensor cores cannot take are the CUDA-core
                 // kernel's; with the tensor-core path forced they are an error.
-                if (p.tc_only && row == 0 && r != 0) raise_deverr(p.counts, LORA_DEVERR_RANK);
+                if (p.tc_only && row == 0 && chalf == 0 && r != 0) raise_deverr(p.counts, LORA_DEVERR_RANK);
                 continue;
             }
             const float sc = p.adapter_scale ? p.adapter_scale[t.a] : p.scale;
             const int n16 = (r + 15) / 16;
             const int my_row = row < t.n ? p.sorted[t.pos + row] : 0;  // this thread's token row
-            // ---- D1 -> scale -> bf16 H (cols >= r are zero)
-            if (!wait_warp(d1f, tiles & 1, ok, abort)) goto role_done;
-            tc_fence_after();
-            if (tiles > 0) if (!wait_warp(he, (tiles - 1) & 1, ok, abort)) goto role_done;  // previous tile's expand is done with H
-            for (int c16 = 0; c16 < kTcMaxRank / 16; ++c16) {
-                uint32_t v[16];
-                if (c16 < n16) {
+            if (chalf == 0) {
+                // ---- D1 -> scale -> bf16 H (cols >= r are zero)
+                if (!wait_warp(d1f, tiles & 1, ok, abort)) goto role_done;
+                tc_fence_after();
+                if (tiles > 0)
+                    if (!wait_warp(he, (tiles - 1) & 1, ok, abort)) goto role_done;  // previous expand done with H
+                for (int c16 = 0; c16 < kTcMaxRank / 16; ++c16) {
+                    if (c16 >= n16) break;
+                    uint32_t v[16];
                     tmem_ld16(tmem + lane_off + 16 * c16, v);
                     tmem_wait_ld();
-                }
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const int c8 = 2 * c16 + half;
-                    if (c8 >= 2 * n16) break;
-                    uint32_t w[4];
+                    for (int half = 0; half < 2; ++half) {
+                        const int c8 = 2 * c16 + half;
+                        uint32_t w[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j = 8 * c8 + 2 * e;
-                        const float f0 = j < r ? __uint_as_float(v[8 * half + 2 * e]) * sc : 0.f;
-                        const float f1 = j + 1 < r ? __uint_as_float(v[8 * half + 2 * e + 1]) * sc : 0.f;
-                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(f0, f1);
-                        w[e] = *reinterpret_cast<const uint32_t *>(&h2);
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = 8 * c8 + 2 * e;
+                            const float f0 = j < r ? __uint_as_float(v[8 * half + 2 * e]) * sc : 0.f;
+                            const float f1 = j + 1 < r ? __uint_as_float(v[8 * half + 2 * e + 1]) * sc : 0.f;
+                            const __nv_bfloat162 h2 = __floats2bfloat162_rn(f0, f1);
+                            w[e] = *reinterpret_cast<const uint32_t *>(&h2);
+                        }
+                        *reinterpret_cast<uint4 *>(H + c8 * kHChunk + row * 16) = make_uint4(w[0], w[1], w[2], w[3]);
                     }
-                    *reinterpret_cast<uint4 *>(H + c8 * kHChunk + row * 16) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(hr);
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(hr);
-            // ---- expand n-tiles: y += D2
-            for (int nt = 0; nt < n_nt; ++nt, ++ys, ++ts) {
+            // ---- expand n-tiles: y += D2 (this thread: its row, 64 columns)
+            for (int nti = 0; nti < n_nt; ++nti, ++ys, ++ts) {
+                const int nt = nti + nt_rot < n_nt ? nti + nt_rot : nti + nt_rot - n_nt;
                 const int sy = ys % kSY, st = ts % kST;
                 int sl, c0, nc;
                 ntile_cols(p, nt, sl, c0, nc);
@@ -457,50 +490,50 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (!wait_warp(&tf[st], (ts / kST) & 1, ok, abort)) goto role_done;
                 if (!wait_warp(&yf[sy], (ys / kSY) & 1, ok, abort)) goto role_done;
                 tc_fence_after();
-                unsigned char *yrow = smem + kOffY + sy * kYStage + row * kYPitch;
-                for (int c32 = 0; c32 < kBN / 32; ++c32) {
+                const unsigned char *yrow = smem + kOffY + sy * kYStage + row * kYPitch;
+                __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.y) + (int64_t)my_row * p.ldy + S.y_col + c0;
+                uint4 outv[8];
+                const int cbase = 64 * chalf;
+#pragma unroll
+                for (int c32 = 0; c32 < 2; ++c32) {
                     uint32_t v0[16], v1[16];
-                    const uint32_t ta = tmem + 128 + 128 * st + lane_off + 32 * c32;
+                    const uint32_t ta = tmem + 128 + 128 * st + lane_off + cbase + 32 * c32;
                     tmem_ld16(ta, v0);
                     tmem_ld16(ta + 16, v1);
                     tmem_wait_ld();
-                    if (row < t.n && 32 * c32 < nc) {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint4 yv = *reinterpret_cast<const uint4 *>(yrow + c32 * 64 + q * 16);
-                            uint32_t *yw = reinterpret_cast<uint32_t *>(&yv);
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 yv = *reinterpret_cast<const uint4 *>(yrow + (cbase + 32 * c32) * 2 + q * 16);
+                        uint32_t *yw = reinterpret_cast<uint32_t *>(&yv);
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int j = q * 8 + 2 * e;
-                                const uint32_t a0 = j < 16 ? v0[j] : v1[j - 16];
-                                const uint32_t a1 = j + 1 < 16 ? v0[j + 1] : v1[j + 1 - 16];
-                                const float y0 = __uint_as_float(yw[e] << 16) + __uint_as_float(a0);
-                                const float y1 = __uint_as_float(yw[e] & 0xFFFF0000u) + __uint_as_float(a1);
-                                const __nv_bfloat162 o = __floats2bfloat162_rn(y0, y1);
-                                yw[e] = *reinterpret_cast<const uint32_t *>(&o);
-                            }
-                            *reinterpret_cast<uint4 *>(yrow + c32 * 64 + q * 16) = yv;
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = q * 8 + 2 * e;
+                            const uint32_t a0 = j < 16 ? v0[j] : v1[j - 16];
+                            const uint32_t a1 = j + 1 < 16 ? v0[j + 1] : v1[j + 1 - 16];
+                            const float y0 = __uint_as_float(yw[e] << 16) + __uint_as_float(a0);
+                            const float y1 = __uint_as_float(yw[e] & 0xFFFF0000u) + __uint_as_float(a1);
+                            const __nv_bfloat162 o = __floats2bfloat162_rn(y0, y1);
+                            yw[e] = *reinterpret_cast<const uint32_t *>(&o);
                         }
+                        outv[c32 * 4 + q] = yv;
                     }
                 }
+                // TMEM buffer and y stage are free as soon as they are read
                 tc_fence_before();
                 mbar_arrive(&te[st]);
-                if (row < t.n) {
-                    fence_proxy_async_smem();
-                    __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.y) + (int64_t)my_row * p.ldy + S.y_col + c0;
-                    bulk_s2g(dst, yrow, (uint32_t)(nc * 2));
-                    bulk_commit();
-                    bulk_wait_read0();
-                }
                 mbar_arrive(&ye[sy]);
+                if (row < t.n) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        if (cbase + 8 * k < nc) *reinterpret_cast<uint4 *>(dst + cbase + 8 * k) = outv[k];
+                }
             }
             ++tiles;
         }
-        bulk_wait0();
     }
 role_done:
     bulk_wait0();
-    if (warp == 1 && lane == 0) {
+    if (warp == 2 && lane == 0) {
         // every MMA this CTA issued has completed before TMEM is released
         umma_commit(fin);
         if (!mbar_wait(fin, 0)) ok = false;
@@ -508,73 +541,22 @@ role_done:
     if (!ok) raise_deverr(p.counts, LORA_DEVERR_WAIT);
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 2) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tmem) : "memory");
     }
 }
 
 // ---------------------------------------------------------------------------
-// Host side: tensor maps (cached) and launch.
+// Host side.
 // ---------------------------------------------------------------------------
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
-    return fn;
-}
-
-static bool encode(CUtensorMap *m, const void *base, int rank, const uint64_t *dims, const uint64_t *strides_bytes,
-                   const uint32_t *box, CUtensorMapSwizzle swz) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    uint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims, strides_bytes, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
-bool tc_available() { return encode_fn() != nullptr; }
-
-static size_t tc_smem_bytes() { return (size_t)kTcSmem; }
+bool tc_available() { return true; }
 
 cudaError_t launch_tc(const DeltaArgs &p, int mode, int sms, cudaStream_t stream) {
     if (mode != kFused) return cudaErrorNotSupported;
-    if (p.r_max > kTcMaxRank && !p.ranks) return cudaErrorNotSupported;
-    TcMaps maps;
-    memset(&maps, 0, sizeof(maps));
-    const int M = p.M_rows;
-    {
-        const uint64_t dims[2] = {(uint64_t)p.d_in, (uint64_t)(M > 0 ? M : 1)};
-        const uint64_t str[1] = {(uint64_t)p.ldx * 2};
-        const uint32_t box8[2] = {kBK, 8}, box1[2] = {kBK, 1};
-        if (!encode(&maps.x8, p.x, 2, dims, str, box8, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode(&maps.x1, p.x, 2, dims, str, box1, CU_TENSOR_MAP_SWIZZLE_128B))
-            return cudaErrorInvalidValue;
-    }
-    {
-        const uint64_t dims[3] = {(uint64_t)p.d_in, (uint64_t)p.r_max, (uint64_t)p.n_adapters};
-        const uint64_t str[2] = {(uint64_t)p.a_stride_r * 2, (uint64_t)p.a_stride_adapter * 2};
-        const uint32_t box[3] = {kBK, 16, 1};
-        if (!encode(&maps.a, p.A, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
-    }
-    for (int t = 0; t < p.n_slices; ++t) {
-        const SliceDesc &S = p.slices[t];
-        const uint64_t dims[3] = {(uint64_t)p.r_max, (uint64_t)S.d_out, (uint64_t)p.n_adapters};
-        const uint64_t str[2] = {(uint64_t)S.stride_n * 2, (uint64_t)S.stride_adapter * 2};
-        const uint32_t box[3] = {8, kBN, 1};
-        if (!encode(&maps.b[t], S.B, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;
-    }
     static DeviceOnce once;
     cudaError_t e = once.run([] {
-        return cudaFuncSetAttribute(sgmv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_bytes());
+        return cudaFuncSetAttribute(sgmv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
     });
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
@@ -583,11 +565,11 @@ cudaError_t launch_tc(const DeltaArgs &p, int mode, int sms, cudaStream_t stream
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(sms);
     cfg.blockDim = dim3(kTcThreads);
-    cfg.dynamicSmemBytes = tc_smem_bytes();
+    cfg.dynamicSmemBytes = kTcSmem;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, sgmv_tc_kernel, p, maps);
+    return cudaLaunchKernelEx(&cfg, sgmv_tc_kernel, p);
 }
 
 }  // namespace lora

@@ -42,8 +42,8 @@ TC_CASES = [
     dict(M=200, d_in=512, d_outs=[384], n_pool=3, r_max=16, run_len=50),         # several segments
     dict(M=300, d_in=1000, d_outs=[776], n_pool=4, r_max=32, run_len=100),       # ragged d_in / d_out
     dict(M=333, d_in=4096, d_outs=[4096], n_pool=6, r_max=16, run_len=111),      # decode-like widths
-    dict(M=257, d_in=520, d_outs=[264, 64, 136], n_pool=5, r_max=64, run_len=40,
-         ranks=[8, 16, 32, 64], per_adapter_scale=True),                         # slices, mixed ranks
+    dict(M=257, d_in=520, d_outs=[264, 64, 136], n_pool=5, r_max=32, run_len=40,
+         ranks=[8, 16, 24, 32], per_adapter_scale=True),                         # slices, mixed ranks
     dict(M=180, d_in=192, d_outs=[256], n_pool=7, r_max=24, run_len=3),          # scattered rows
     dict(M=64, d_in=128, d_outs=[128], n_pool=2, r_max=8, run_len=64),
 ]
@@ -66,8 +66,8 @@ def test_tensor_path_chunks_merge(B, chunk):
 
 
 def test_tensor_path_nan_padding(B):
-    w = wl.random_batch(seed=430, M=256, d_in=512, d_outs=[384], n_pool=8, r_max=64,
-                        ranks=[8, 16, 32, 64], run_len=32, dtype="bf16", pad_value=float("nan"),
+    w = wl.random_batch(seed=430, M=256, d_in=512, d_outs=[384], n_pool=8, r_max=32,
+                        ranks=[8, 16, 24, 32], run_len=32, dtype="bf16", pad_value=float("nan"),
                         per_adapter_scale=True)
     y, _ = _run(B, w, path=B.PATH_TENSOR)
     _check(w, y)
@@ -106,3 +106,11 @@ def test_tensor_and_cuda_core_paths_agree(B):
     base = w.y.astype(np.float64)
     assert rel_err(y_tc, y_cc, base) <= 1e-2
     _check(w, y_tc)
+
+
+def test_auto_split_rank64_long_segments_use_cuda_cores(B):
+    w = wl.random_batch(seed=441, M=400, d_in=512, d_outs=[256], n_pool=4, r_max=64, run_len=100,
+                        ranks=np.array([64, 16, 64, 32], np.int32), dtype="bf16", pad_value=float("nan"))
+    y, batch = _run(B, w, path=B.PATH_AUTO, tc_min=16)
+    _check(w, y)
+    assert batch.counts()["device_error"] == 0
