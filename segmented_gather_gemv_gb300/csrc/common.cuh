@@ -178,20 +178,24 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
 }
+// One test of phase `parity`; the thread may sleep up to kSuspendNs in it
+// until the phase completes (so waiting warps do not keep the shared-memory
+// pipe busy with polls while other warps issue copies).
+constexpr uint32_t kSuspendNs = 1000;
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
         : "memory");
     return ok != 0;
 }
 // Longest a kernel waits on one barrier before it gives up, in SM clock
 // cycles (about 0.1 s at 2 GHz).  Real waits last microseconds; the limit only
 // ends a wait that can no longer complete.  The SM-local cycle counter is
-// read every 64 polls so that polling stays cheap.
+// read every 64 tests.
 constexpr long long kWaitLimitCycles = 200ll * 1000 * 1000;
 // Bounded wait for phase `parity` of `bar`.  Returns false if the barrier did
 // not complete in time (the caller flags an error; it never spins forever).

@@ -111,15 +111,21 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
     if (tid == 0) s_invalid = 0;
     __syncthreads();
     int bad = 0;
-    for (int i = tid; i < M; i += nthr) {
-        const int a = ids[i];
-        if (a == -1) continue;
-        if (a < 0 || a >= n) {
+    for (int base = 0; base < M; base += nthr) {
+        // Warp-aggregated: the lanes holding the same adapter elect one lane,
+        // which adds their count and offers their first row (runs of equal
+        // ids, as in prefill batches, would otherwise serialize).
+        const int i = base + tid;
+        int a = i < M ? ids[i] : -1;
+        if (a != -1 && (a < 0 || a >= n)) {
             ++bad;
-            continue;
+            a = -1;
         }
-        atomicMin(&first_pos[a], i);
-        atomicAdd(&acnt[a], 1);
+        const unsigned peers = __match_any_sync(0xffffffffu, a);
+        if (a >= 0 && lane == __ffs(peers) - 1) {
+            atomicMin(&first_pos[a], i);
+            atomicAdd(&acnt[a], __popc(peers));
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
@@ -128,6 +134,27 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
 
     // Phase 2: group number by order of first appearance.
     int G = 0;
+    if (n <= nthr && n <= 512 && p.off_adapters >= 0) {
+        // Small pool: the group of adapter a is the number of present
+        // adapters that first appear before it (every thread reads the same
+        // entries in step, so the shared-memory reads are broadcasts).
+        for (int a0 = 0; a0 < n; a0 += nthr) {
+            const int a = a0 + tid;
+            const int fa = a < n && acnt[a] > 0 ? first_pos[a] : INT_MAX;
+            int rank = 0, present = 0;
+            for (int b2 = 0; b2 < n; ++b2) {
+                const int fb = first_pos[b2];
+                rank += fb < fa ? 1 : 0;
+                present += fb != INT_MAX ? 1 : 0;
+            }
+            if (fa != INT_MAX) {
+                agroup[a] = rank;
+                gadapter[rank] = a;
+            }
+            G = present;
+        }
+        __syncthreads();
+    } else
     for (int base = 0; base < M; base += nthr) {
         const int i = base + tid;
         const int a = i < M ? ids[i] : -1;

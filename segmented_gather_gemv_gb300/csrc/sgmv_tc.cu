@@ -6,82 +6,123 @@
 // unit.
 //
 // Work split: the rows of all segments routed here form one row space; CTA b
-// of a persistent grid takes rows [M b / G, M (b+1) / G), so every CTA moves
-// the same amount of x and y whatever the segment lengths.  Its rows are cut
-// into tiles of up to 128 rows that share one adapter (consecutive chunks of
-// the same adapter group merge into one tile).
+// of a persistent grid takes the equal share [M b / G, M (b+1) / G), so every
+// CTA moves the same amount of x and y whatever the segment lengths.  Its
+// rows are cut into tiles of up to 128 rows; a tile may span several
+// segments (pieces, see Tile below), so a share never costs two passes.
 //
 // Per tile:
-//   shrink  D1[128 x r] (TMEM, fp32) = x_tile[128 x d_in] . A_a^T, K in
-//           64-element blocks, operands staged in the 128-byte swizzle;
-//   scale   the epilogue warps read D1, multiply by s_a, round to bf16 and
-//           write H[128 x r] to shared memory (never to global memory);
+//   shrink  D1[128 x K] (TMEM, fp32) = x_tile[128 x d_in] . A^T, where A
+//           stacks the rank rows of the tile's adapters (K <= 32), K in
+//           128-element blocks, operands in the 128-byte swizzle;
+//   scale   the epilogue warps read D1, keep for each row only its own
+//           adapter's columns, multiply by s_a, round to bf16 and write
+//           H[128 x K] to shared memory (never to global memory);
 //   expand  per 128-column n-tile: D2[128 x 128] (TMEM, triple buffered)
-//           = H . B_a[cols]^T;
-//   store   y_tile += D2 in fp32, rounded once to bf16, stored from registers.
-// Ranks are masked exactly: A rows / B columns at or past the adapter's rank
-// are zero-filled in shared memory (never read), so padding never reaches y.
+//           = H . B^T, B stacking the adapters' rows of that n-tile;
+//   store   y_tile += D2 in fp32, rounded once to bf16.
+// Ranks are masked exactly: A rows / B columns past an adapter's rank are
+// never read, H columns past it are zero, so padding never reaches y.
 //
-// Warp roles (448 threads): warps 0-1 x/A loaders, warp 2 MMA issuer (one
-// thread) and TMEM owner, warp 3 B loader, warps 4-5 y loaders, warps 6..13
-// epilogue (warp w
-// owns TMEM lanes 32 (w % 4) .. +31, i.e. tile rows, and one half of the
-// columns of every n-tile; four of them also build H).
+// Data movement.  The kernel streams x once and y twice (read, write); the
+// adapter weights are small and stay in L2.  All staging goes through ONE
+// ring of stages, filled in program order: a tile's nkb "x jobs" (x rows of
+// one K block + the A block), then its n_nt "y jobs" (y rows of one n-tile +
+// the B block).  So the y of a tile is already on its way while its last K
+// blocks are multiplied, and the next tile's x while its last n-tiles are
+// stored.  An x stage is released by the MMA (tcgen05.commit); a y stage by
+// the epilogue warps once they have stored it.  A stage holds `cap` rows,
+// cap = the CTA's share rounded up to 8 (at most 128), so a short share gets
+// more, smaller stages: the bytes in flight per SM set the DRAM throughput,
+// and a job's round trip (load, MMA, epilogue, release) takes microseconds.
+// Rows of a tile past its end may hold anything: row i of D1 and D2 depends
+// only on row i of the operands, so the MMA may also read whatever lies in
+// shared memory past a stage's `cap` rows (up to 120 rows of 128 bytes, kept
+// inside the allocation by kOverrun).
 //
-// Loads are 16-byte cp.async issued by the loader warps (they write the
-// swizzled operand layouts themselves and signal the stage barrier with
-// cp.async.mbarrier.arrive.noinc): rows gathered through sorted_token_ids
-// are 128- or 256-byte pieces of rows far apart, and bulk / tensor async
-// copies of such pieces run several times slower than 16-byte copies.
+// Copies.  Rows of a tile that sit on consecutive token rows within one
+// piece (a prefill sequence keeps its tokens adjacent and in order in
+// sorted_token_ids) move by TMA: tiled copies of 64 columns x 64, 32 or 8
+// rows in the 128-byte swizzle, for x and y; the A block comes by TMA from a
+// 3-D map of the pool.  Rows that no box covers (a group of 8 split by a
+// piece boundary or by a break in the token rows) and the B block (16-byte
+// pieces of L2-resident rows) move by 16-byte cp.async.  A loader that
+// issues one cp.async per 16 bytes for everything spends its time issuing
+// and waiting on its own instruction stream, which is why the boxes matter.
+// y is stored with st.global, four 128-byte row pieces per instruction: TMA
+// stores mixed with such stores in one CTA stalled the CTA's loads.
+//
+// Warp roles (416 threads): warps 0-3 loaders (lane 0 of warps 0 and 1 issue
+// the boxes of atoms 0 and 1; warps 2-3 the cp.async copies), warp 4 MMA
+// issuer (one thread) and TMEM owner, warps 5..12 epilogue.  Epilogue warp w
+// owns TMEM lanes 32 (w % 4) .. +31 (tile rows) and one half of the columns
+// of every n-tile; four of them also build H.  Without tensor maps (or for
+// gathered tiles when they are missing) every loader thread copies by
+// cp.async.
+#include <cuda.h>
+#include <cstring>
+
 #include "common.cuh"
 
 namespace lora {
 
-constexpr int kTcThreads = 448;
+constexpr int kLoaderWarps = 4;                      // warps 0-3
+constexpr int kLoaderThreads = kLoaderWarps * 32;
+constexpr int kMmaWarp = 4;
+constexpr int kEpiWarp0 = 5;                         // warps 5..12
+constexpr int kEpiWarps = 8;
+constexpr int kTcThreads = (kEpiWarp0 + kEpiWarps) * 32;
 constexpr int kBM = 128;        // tile rows (MMA M)
 constexpr int kBK = 128;        // shrink K block: two 64-element (128-byte) swizzle atoms
 constexpr int kBN = 128;        // expand n-tile (MMA N)
-constexpr int kSX = 2;          // x/A stages
-constexpr int kSB = 4;          // B stages
-constexpr int kSY = 3;          // y stages
+constexpr int kMaxNS = 16;      // ring stages at most
 constexpr int kST = 3;          // TMEM D2 buffers
 constexpr int kTcMaxRank = 32;  // ranks above this use the CUDA-core kernel
-constexpr int kSnapRows = 16;   // CTA row ranges end on a segment boundary this close
-constexpr int kYPitch = kBN * 2 + 16;  // bytes per y row in a y stage (padded)
+// Tensor maps of x and of the y column block of every slice (bf16, 128-byte
+// swizzle), with boxes of 64 columns x 64, 32 and 8 rows; use = 0 when they
+// could not be made.
+// Also 3-D maps of the pools: A [adapter][rank row][d_in] in boxes of 64
+// columns x 8 rank rows (128-byte swizzle), and for every slice B
+// [adapter][d_out row][rank] in boxes of 8 rank columns x 128 rows (no
+// swizzle: one 2 KB chunk of the MMA's core-matrix layout).  A box placed
+// past the last rank row / column reads zeros.  use_ab = 0 when those maps
+// could not be made.
+struct TcMaps {
+    CUtensorMap x64, x32, x8;
+    CUtensorMap y64[LORA_MAX_SLICES], y32[LORA_MAX_SLICES], y8[LORA_MAX_SLICES];
+    CUtensorMap a8, b[LORA_MAX_SLICES];
+    int32_t use, use_ab, r_pad;  // r_pad: first rank index past every adapter's rank, a multiple of 8
+};
 
-// Shared-memory layout (bytes, from a 1024-aligned base).
-constexpr int kXAtom = kBM * 128;                    // 16 KB: 128 rows x 64 columns
-constexpr int kAAtom = kTcMaxRank * 128;             // 4 KB: 32 rank rows x 64 columns
-constexpr int kXBytes = 2 * kXAtom;                  // 32 KB
-constexpr int kABytes = 2 * kAAtom;                  // 8 KB
-constexpr int kXStage = kXBytes + kABytes;           // 24 KB
+
+// Shared-memory layout (bytes, from a 1024-aligned base).  A stage of a
+// CTA whose tiles have at most `cap` rows (a multiple of 8) and whose ranks
+// need n16 16-column MMA steps:
+//   x job: x   two 64-column atoms of cap rows x 128 bytes (128-byte swizzle),
+//          then A  two atoms of 16 n16 rank rows x 128 bytes;
+//   y job: y   two 64-column atoms of cap rows x 128 bytes (same swizzle),
+//          then B  2 n16 chunks of 128 rows x 16 bytes (8 rank columns each).
+// Both take cap * 256 + 4096 * n16 bytes: at most 40 KB.
 constexpr int kBChunk = kBN * 16;                    // 2 KB: 8 rank columns x 128 rows
-constexpr int kBStage = (kTcMaxRank / 8) * kBChunk;  // 16 KB
+constexpr int kRingBytes = 200 * 1024;
 constexpr int kHChunk = kBM * 16;                    // 2 KB
-constexpr int kHBytes = (kTcMaxRank / 8) * kHChunk;  // 16 KB
-constexpr int kYStage = kBM * kYPitch;               // 34 KB
-constexpr int kOffX = 0;
-constexpr int kOffB = kOffX + kSX * kXStage;
-constexpr int kOffH = kOffB + kSB * kBStage;
-constexpr int kOffY = kOffH + kHBytes;
-constexpr int kOffRows = kOffY + kSY * kYStage;      // 3 x 128 ints (per loader role)
-constexpr int kOffBars = kOffRows + 3 * kBM * 4;
-constexpr int kNumBars = 2 * kSX + 2 * kSB + 2 * kSY + 3 + 2 * kST + 1;
-constexpr int kOffMisc = kOffBars + kNumBars * 8;
-constexpr int kTcSmem = kOffMisc + 64 + 1024;        // + alignment slack
-
+constexpr int kHBytes = (kTcMaxRank / 8) * kHChunk;  // 8 KB
+constexpr int kOffH = kRingBytes;
+constexpr int kOffBars = kOffH + kHBytes;
+constexpr int kNumBars = 2 * kMaxNS + 3 + 2 * kST + 1;
+constexpr int kOffMisc = kOffBars + kNumBars * 8;    // TMEM address, abort flag, CTA row range
+constexpr int kOffLdr = kOffMisc + 64;               // loader tables: row tokens, group tokens, TMA boxes
+// loader tables, at kOffLdr: row tokens [4 warps][32] ints, group tokens
+// [2][16] ints, TMA boxes [2][16] uint2, then the helpers' row lists [2][128] int2
+constexpr int kLdrGtok = 4 * 32 * 4, kLdrBox = kLdrGtok + 2 * 16 * 4, kLdrRows = kLdrBox + 2 * 16 * 8;
+constexpr int kLdrBytes = kLdrRows + 2 * kBM * 8;
+constexpr int kOverrun = (kBM - 8) * 128;            // MMA reads past the last stage
+constexpr int kTcSmemUsed = kOffLdr + kLdrBytes > kRingBytes + kOverrun ? kOffLdr + kLdrBytes : kRingBytes + kOverrun;
+constexpr int kTcSmem = kTcSmemUsed + 1024;          // + alignment slack
 
 // ---------------------------------------------------------------------------
 // Device helpers.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void bulk_s2g(void *gdst, const void *ssrc, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(gdst), "r"(smem_u32(ssrc)),
-                 "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
@@ -129,6 +170,26 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 
+__device__ __forceinline__ void tma_load_2d(void *sdst, const CUtensorMap *map, int c, int r, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
+            smem_u32(sdst)),
+        "l"(map), "r"(c), "r"(r), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void *sdst, const CUtensorMap *map, int c0, int c1, int c2,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(
+            smem_u32(sdst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_n(uint64_t *bar, uint32_t n) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(n) : "memory");
+}
+
 // Bounded waits: false (and `ok` cleared) when the wait timed out or another
 // role aborted; the caller then leaves its loop.  wait1 is for a single
 // thread; wait_warp is called by all 32 lanes and returns the same answer on
@@ -145,47 +206,95 @@ __device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, bool &
     return all;
 }
 
-// One tile of the row space: `n` rows starting at sorted position `pos`,
-// all on adapter `a`.
-struct Tile {
-    int pos, n, a;
-};
+// Largest i in [0, nseg) with ptr[i] <= r (ptr[0] = 0 <= r).  Called by all
+// 32 lanes of a warp; each round probes 32 entries at once.
+__device__ __forceinline__ int warp_seg_of(const int32_t *ptr, int nseg, int r, int lane) {
+    int lo = 0, hi = nseg - 1;
+    while (hi > lo) {
+        const int step = (hi - lo + 32) >> 5;
+        const int q = lo + lane * step;
+        const bool le = q <= hi && ptr[q] <= r;
+        const unsigned m = __ballot_sync(0xffffffffu, le);
+        lo += (31 - __clz(m)) * step;
+        hi = min(hi, lo + step - 1);
+    }
+    return lo;
+}
 
-// Walks the tiles of one CTA's row range.  Every role runs its own copy and
-// sees the same sequence.
+// One tile: `n` consecutive rows of the row space (at most 128), made of up
+// to kMaxPieces pieces.  Piece q covers tile rows [off[q], off[q+1]); they
+// are the rows at sorted positions pos[q] .., all on adapter a[q], whose rank
+// is rank[q]; rk[q] = rank[q] if the tensor cores take it, else 0.  Piece q
+// owns rank columns [kofs[q], kofs[q] + rk[q]) of the tile's stacked A and B
+// blocks (K of them in all, at most 32): its rows see only its own adapter,
+// because H is zero outside those columns.  So a CTA's row range never has to
+// end at a segment boundary, and a tile costs one pass over the K blocks and
+// n-tiles however many adapters share it.
+constexpr int kMaxPieces = 4;
+struct Tile {
+    int n, np, K;
+    int off[kMaxPieces + 1], pos[kMaxPieces], a[kMaxPieces], rank[kMaxPieces], rk[kMaxPieces], kofs[kMaxPieces];
+    __device__ __forceinline__ int piece_of(int i) const {
+        int q = 0;
+#pragma unroll
+        for (int u = 1; u < kMaxPieces; ++u) q += (u < np && i >= off[u]) ? 1 : 0;
+        return q;
+    }
+};
+// arr[q] for a run-time q, with compile-time indices only (keeps tiles in registers)
+__device__ __forceinline__ int sel(const int (&arr)[kMaxPieces], int q) {
+    int v = arr[0];
+#pragma unroll
+    for (int u = 1; u < kMaxPieces; ++u) v = q == u ? arr[u] : v;
+    return v;
+}
+
+// Walks the tiles of one CTA's row range [r, r1); i is the segment holding
+// row r.  Every role runs its own copy and sees the same sequence.
 struct TileWalker {
     const DeltaArgs *p;
-    int r, r1, nseg;
-    __device__ __forceinline__ int seg_of(int row) const {
-        int lo = 0, hi = nseg - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (p->tc_ptr[mid] <= row) lo = mid;
-            else hi = mid - 1;
-        }
-        return lo;
-    }
+    int r, r1, i;
     __device__ __forceinline__ bool next(Tile &t) {
         if (r >= r1) return false;
-        int i = seg_of(r);
-        const int a = p->tc_adapter[(int64_t)i * p->tc_rec_stride];
-        const int start = p->tc_start[(int64_t)i * p->tc_rec_stride];
-        t.pos = start + (r - p->tc_ptr[i]);
-        t.a = a;
-        int end = p->tc_ptr[i + 1];  // row-space end of the current run
-        int run_end_pos = start + (end - p->tc_ptr[i]);
-        // Consecutive segments of the same adapter that continue the run
-        // (chunks of one adapter group) join the tile.
-        while (end < r1 && end - r < kBM && i + 1 < nseg) {
-            const int a2 = p->tc_adapter[(int64_t)(i + 1) * p->tc_rec_stride];
-            const int s2 = p->tc_start[(int64_t)(i + 1) * p->tc_rec_stride];
-            if (a2 != a || s2 != run_end_pos) break;
-            ++i;
-            run_end_pos += p->tc_ptr[i + 1] - p->tc_ptr[i];
-            end = p->tc_ptr[i + 1];
+        t.n = 0;
+        t.np = 0;
+        t.K = 0;
+#pragma unroll
+        for (int u = 0; u <= kMaxPieces; ++u) t.off[u] = 0;
+        int last_a = -1, last_end = -1;  // adapter and sorted end position of the last piece
+        while (r < r1 && t.n < kBM) {
+            while (p->tc_ptr[i + 1] <= r) ++i;
+            const int a = p->tc_adapter[(int64_t)i * p->tc_rec_stride];
+            const int pos = p->tc_start[(int64_t)i * p->tc_rec_stride] + (r - p->tc_ptr[i]);
+            const int cnt = min(min(p->tc_ptr[i + 1] - r, r1 - r), kBM - t.n);
+            // a new piece, unless this segment continues the last one (the
+            // next chunk of the same adapter group)
+            const bool fresh = !(a == last_a && pos == last_end);
+            const int rank = p->ranks ? p->ranks[a] : p->r_max;
+            const int rk = rank <= p->r_max && tc_rank_ok(rank) ? rank : 0;
+            if (fresh && (t.np == kMaxPieces || t.K + rk > kTcMaxRank)) break;
+#pragma unroll
+            for (int u = 0; u < kMaxPieces; ++u)
+                if (fresh && u == t.np) {
+                    t.pos[u] = pos;
+                    t.a[u] = a;
+                    t.rank[u] = rank;
+                    t.rk[u] = rk;
+                    t.kofs[u] = t.K;
+                    t.off[u] = t.n;
+                }
+            if (fresh) {
+                t.K += rk;
+                ++t.np;
+            }
+            last_a = a;
+            last_end = pos + cnt;
+            t.n += cnt;
+            r += cnt;
         }
-        t.n = min(min(kBM, r1 - r), end - r);
-        r += t.n;
+#pragma unroll
+        for (int u = 1; u <= kMaxPieces; ++u)
+            if (u == t.np) t.off[u] = t.n;
         return true;
     }
 };
@@ -204,31 +313,80 @@ __device__ __forceinline__ void ntile_cols(const DeltaArgs &p, int nt, int &slic
     ncols = min(kBN, p.slices[t].d_out - c0);
 }
 
+// Byte offset of 16-byte chunk c (of 16) of row i in an x or y stage: atom
+// c / 8, 128-byte rows, chunk index XORed with the row's low bits (the
+// 128-byte swizzle of TMA and of the MMA operands; a warp reading one chunk
+// of 32 rows, or 8 chunks of 4 rows, spreads over all banks).
+__device__ __forceinline__ int schunk(int xatom, int i, int c) { return (c >> 3) * xatom + i * 128 + (((c & 7) ^ (i & 7)) << 4); }
+
+// Token row (row of x and y) of tile row i.
+__device__ __forceinline__ int tile_token(const DeltaArgs &p, const Tile &t, int i) {
+    const int q = t.piece_of(i);
+    int pos = t.pos[0], off = t.off[0];
+#pragma unroll
+    for (int u = 1; u < kMaxPieces; ++u)
+        if (q == u) {
+            pos = t.pos[u];
+            off = t.off[u];
+        }
+    return p.sorted[pos + (i - off)];
+}
+
+// Which 8-row groups (bit g: tile rows 8g .. 8g+7, the last group possibly
+// partial), 32-row groups (bit j: rows 32j .. 32j+31, full) and 64-row
+// groups (bit h) lie in one piece on consecutive token rows, so that one TMA
+// box moves them.  Called by all 32 lanes of a warp; every lane gets the
+// same masks.
+__device__ __forceinline__ void tile_box_masks(const DeltaArgs &p, const TcMaps &m, const Tile &t, int lane,
+                                               uint32_t &mask8, uint32_t &mask32, uint32_t &mask64) {
+    bool ok = false;
+    if (m.use) {
+        int i0 = -1, i1 = 0;
+        if (lane < 16 && 8 * lane < t.n) {
+            i0 = 8 * lane;
+            i1 = min(i0 + 7, t.n - 1);
+        } else if (lane >= 16 && lane < 20 && 32 * (lane - 16) + 32 <= t.n) {
+            i0 = 32 * (lane - 16);
+            i1 = i0 + 31;
+        } else if (lane >= 20 && lane < 22 && 64 * (lane - 20) + 64 <= t.n) {
+            i0 = 64 * (lane - 20);
+            i1 = i0 + 63;
+        }
+        if (i0 >= 0) ok = t.piece_of(i0) == t.piece_of(i1) && tile_token(p, t, i1) - tile_token(p, t, i0) == i1 - i0;
+    }
+    const uint32_t b = __ballot_sync(0xffffffffu, ok);
+    mask8 = b & 0xFFFFu;
+    mask32 = (b >> 16) & 0xFu;
+    mask64 = (b >> 20) & 0x3u;
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1)
-    sgmv_tc_kernel(const __grid_constant__ DeltaArgs p) {
+    sgmv_tc_kernel(const __grid_constant__ DeltaArgs p, const __grid_constant__ TcMaps m) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBars);
-    uint64_t *xf = bars, *xe = xf + kSX, *bf = xe + kSX, *be = bf + kSB, *yf = be + kSB, *ye = yf + kSY;
-    uint64_t *d1f = ye + kSY, *hr = d1f + 1, *he = hr + 1, *tf = he + 1, *te = tf + kST, *fin = te + kST;
+    uint64_t *full = bars, *empty = full + kMaxNS;
+    uint64_t *d1f = empty + kMaxNS, *hr = d1f + 1, *he = hr + 1, *tf = he + 1, *te = tf + kST, *fin = te + kST;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 16);
+    int *range = reinterpret_cast<int *>(smem + kOffMisc + 32);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
-        for (int s = 0; s < kSX; ++s) { mbar_init(&xf[s], 64); mbar_init(&xe[s], 1); }
-        for (int s = 0; s < kSB; ++s) { mbar_init(&bf[s], 32); mbar_init(&be[s], 1); }
-        for (int s = 0; s < kSY; ++s) { mbar_init(&yf[s], 64); mbar_init(&ye[s], 256); }
+        for (int s = 0; s < kMaxNS; ++s) {
+            mbar_init(&full[s], kLoaderThreads + 2);  // + the two TMA issuers' expect_tx
+            mbar_init(&empty[s], kEpiWarps);  // 8 epilogue warps, or the MMA thread (7 arrivals + commit)
+        }
         mbar_init(d1f, 1);
-        mbar_init(hr, 128);
+        mbar_init(hr, 4);
         mbar_init(he, 1);
-        for (int s = 0; s < kST; ++s) { mbar_init(&tf[s], 1); mbar_init(&te[s], 256); }
+        for (int s = 0; s < kST; ++s) { mbar_init(&tf[s], 1); mbar_init(&te[s], kEpiWarps); }
         mbar_init(fin, 1);
         fence_mbar_init();
         *abort = 0;
     }
-    if (warp == 2) {
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(smem_u32(tmem_slot))
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
@@ -241,189 +399,375 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     griddep_launch_dependents();
     griddep_wait();
 
-    const int nseg = min(p.counts[p.tc_count_index], p.max_list);
-    const int Mrows = p.counts[p.tc_rows_index];
-    const int G = gridDim.x, b = blockIdx.x;
-    TileWalker walker{&p, 0, 0, nseg};
-    if (nseg > 0) {
-        // Equal row shares, each end moved to a segment boundary that lies
-        // within kSnapRows: a tile costs a full pass over the K blocks and
-        // n-tiles however few rows it holds, so a CTA should not end a few
-        // rows into the next segment.  Both neighbours compute the same end.
-        auto snap = [&](int r) {
-            if (r <= 0 || r >= Mrows) return r <= 0 ? 0 : Mrows;
-            const int i = walker.seg_of(r);
-            const int lo = p.tc_ptr[i], hi = p.tc_ptr[i + 1];
-            if (r - lo <= kSnapRows) return lo;
-            if (hi - r <= kSnapRows) return hi;
-            return r;
-        };
-        walker.r = snap((int)((int64_t)Mrows * b / G));
-        walker.r1 = snap((int)((int64_t)Mrows * (b + 1) / G));
-        if (walker.r1 < walker.r) walker.r1 = walker.r;
+    if (warp == kMmaWarp) {
+        // This CTA's row range: an equal share of the row space.
+        const int nseg = min(p.counts[p.tc_count_index], p.max_list);
+        const int Mrows = nseg > 0 ? p.counts[p.tc_rows_index] : 0;
+        const int G = gridDim.x, b = blockIdx.x;
+        const int r0 = (int)((int64_t)Mrows * b / G), r1 = (int)((int64_t)Mrows * (b + 1) / G);
+        const int i0 = r0 < r1 ? warp_seg_of(p.tc_ptr, nseg, r0, lane) : 0;
+        if (lane == 0) {
+            range[0] = r0;
+            range[1] = r1;
+            range[2] = i0;
+        }
     }
+    __syncthreads();
+    TileWalker walker{&p, range[0], range[1], range[2]};
+    // Stage geometry of this CTA (same in every role).
+    const int cap = min(kBM, (range[1] - range[0] + 7) & ~7);
+    const int xatom = cap * 128, xbytes = cap * 256, aatom = 4096;
+    const int stage_bytes = xbytes + 2 * aatom;
+    const int NS = cap > 0 ? min(kMaxNS, kRingBytes / stage_bytes) : 1;
 
     int n_nt = 0;
     for (int t = 0; t < p.n_slices; ++t) n_nt += (p.slices[t].d_out + kBN - 1) / kBN;
     const int nkb = (p.d_in + kBK - 1) / kBK;
     // Every CTA walks the K blocks and the n-tiles from its own starting
-    // point.  Rows of x and y are a power-of-two stride apart; if all CTAs
-    // read the same column block at the same time, their requests fall on the
-    // same memory channels.
-    const int kb_rot = (int)(((uint32_t)b * 2654435761u) >> 7) % nkb;
-    const int nt_rot = (int)(((uint32_t)b * 2246822519u) >> 7) % (n_nt > 0 ? n_nt : 1);
+    // point, so that the CTAs do not all hit the same column block at once.
+    const int kb_rot = (int)(((uint32_t)blockIdx.x * 2654435761u) >> 7) % nkb;
+    const int nt_rot = (int)(((uint32_t)blockIdx.x * 2246822519u) >> 7) % (n_nt > 0 ? n_nt : 1);
+    const __nv_bfloat16 *yg = static_cast<const __nv_bfloat16 *>(p.y);
     bool ok = true;
 
-    if (warp < 2) {
-        // ------------------------------------------------------------ x/A loaders
-        const int lt = tid;  // 0..63
-        int32_t *rows = reinterpret_cast<int32_t *>(smem + kOffRows);
+    if (warp < kLoaderWarps) {
+        // ------------------------------------------------------------ loaders
+        // Thread lt copies chunk (lt & 15) of tile rows (lt >> 4) + 8q (row
+        // group q) by cp.async where no TMA box covers them; lane 0 of warps
+        // 0 and 1 issues the TMA boxes of atoms 0 and 1.  Per tile, each warp
+        // writes its tables (row tokens; box list) to shared memory once, so
+        // the per-stage loop only reads them.
+        const int lt = tid, c = lt & 15, i0 = lt >> 4;
+        const int hq = warp;  // the atom of an issuing warp (0 or 1)
+        int32_t *lrow = reinterpret_cast<int32_t *>(smem + kOffLdr) + 32 * warp;      // [slot]: token row
+        int32_t *lgt = reinterpret_cast<int32_t *>(smem + kOffLdr + kLdrGtok) + 16 * (warp & 1);  // [g]: token of row 8g
+        uint2 *lbox = reinterpret_cast<uint2 *>(smem + kOffLdr + kLdrBox) + 16 * (warp & 1);     // {row | height code << 8, token}
         const __nv_bfloat16 *xg = static_cast<const __nv_bfloat16 *>(p.x);
         const __nv_bfloat16 *Ag = static_cast<const __nv_bfloat16 *>(p.A);
-        uint32_t xs = 0;
+        int s = 0;
+        uint32_t ph = 0;
         Tile t;
         while (walker.next(t)) {
-            const int r = p.ranks ? p.ranks[t.a] : p.r_max;
-            const bool live = r <= p.r_max && tc_rank_ok(r);
-            if (!live) continue;
-            asm volatile("bar.sync 1, 64;\n" ::: "memory");  // previous tile done with rows
-            for (int i = lt; i < t.n; i += 64) rows[i] = p.sorted[t.pos + i];
-            asm volatile("bar.sync 1, 64;\n" ::: "memory");
-            const int n16 = (r + 15) / 16;
-            const __nv_bfloat16 *Aa = Ag + (int64_t)t.a * p.a_stride_adapter;
-            for (int kbi = 0; kbi < nkb; ++kbi, ++xs) {
-                const int kb = kbi + kb_rot < nkb ? kbi + kb_rot : kbi + kb_rot - nkb;
-                const int s = xs % kSX;
-                if (!wait_warp(&xe[s], ((xs / kSX) & 1) ^ 1, ok, abort)) goto role_done;
-                unsigned char *xst = smem + kOffX + s * kXStage;
-                // x rows: 16 chunks of 16 bytes per row (256 contiguous bytes),
-                // two 64-column atoms in the 128-byte swizzle
-                for (int e = lt; e < t.n * 16; e += 64) {
-                    const int i = e >> 4, c = e & 15, k = kb * kBK + c * 8;
-                    const __nv_bfloat16 *row = xg + (int64_t)rows[i] * p.ldx;
-                    cp_async16(xst + (c >> 3) * kXAtom + i * 128 + (((c & 7) ^ (i & 7)) << 4), k < p.d_in ? row + k : row,
-                               k < p.d_in ? 16 : 0);
-                }
-                // A rows of the adapter (rows >= rank zero-filled)
-                for (int e = lt; e < 16 * n16 * 16; e += 64) {
-                    const int j = e >> 4, c = e & 15, k = kb * kBK + c * 8;
-                    const bool in = j < r && k < p.d_in;
-                    cp_async16(xst + kXBytes + (c >> 3) * kAAtom + j * 128 + (((c & 7) ^ (j & 7)) << 4),
-                               in ? Aa + (int64_t)j * p.a_stride_r + k : Aa, in ? 16 : 0);
-                }
-                cp_async_arrive_noinc(&xf[s]);
+            if (t.K == 0) continue;
+            uint32_t mask8, mask32, mask64;
+            tile_box_masks(p, m, t, lane, mask8, mask32, mask64);
+            // this lane's slot: tile row (2 warp + (lane & 1)) + 8 (lane >> 1)
+            {
+                const int i = 2 * warp + (lane & 1) + 8 * (lane >> 1);
+                __syncwarp();  // the previous tile's readers are done
+                lrow[lane] = i < t.n ? tile_token(p, t, i) : 0;
+                if (warp < 2 && lane < 16) lgt[lane] = 8 * lane < t.n ? tile_token(p, t, 8 * lane) : 0;
+                __syncwarp();
             }
-        }
-    } else if (warp == 3) {
-        // ------------------------------------------------------------ B loader
-        uint32_t bs = 0;
-        Tile t;
-        while (walker.next(t)) {
-            const int r = p.ranks ? p.ranks[t.a] : p.r_max;
-            const bool live = r <= p.r_max && tc_rank_ok(r);
-            if (!live) continue;
-            const int n16 = (r + 15) / 16, n8mma = 2 * n16, sh8 = n16 == 1 ? 1 : 2;
-            for (int nti = 0; nti < n_nt; ++nti, ++bs) {
-                const int nt = nti + nt_rot < n_nt ? nti + nt_rot : nti + nt_rot - n_nt;
-                int sl, c0, nc;
-                ntile_cols(p, nt, sl, c0, nc);
-                const SliceDesc &S = p.slices[sl];
-                // B rows c0 .. c0+127 of this slice, 8 rank columns per 2 KB chunk
-                const int sb = bs % kSB;
-                if (!wait_warp(&be[sb], ((bs / kSB) & 1) ^ 1, ok, abort)) goto role_done;
-                unsigned char *bst = smem + kOffB + sb * kBStage;
-                const __nv_bfloat16 *Ba = static_cast<const __nv_bfloat16 *>(S.B) + (int64_t)t.a * S.stride_adapter;
-                for (int e = lane; e < kBN * n8mma; e += 32) {
-                    const int n = e >> sh8, c = e & (n8mma - 1);
-                    const bool in = c0 + n < S.d_out && c * 8 < r;
-                    cp_async16(bst + c * kBChunk + n * 16, in ? Ba + (int64_t)(c0 + n) * S.stride_n + c * 8 : Ba,
-                               in ? 16 : 0);
+            // cp.async rows of this thread: bit q = row i0 + 8q
+            uint32_t mine = 0;
+#pragma unroll
+            for (int q = 0; q < kBM / 8; ++q) mine |= (i0 + 8 * q < t.n && !((mask8 >> q) & 1)) ? 1u << q : 0u;
+            int nbox = 0;
+            if (warp < 2 && lane == 0) {
+                for (int h = 0; h < 2; ++h) {
+                    if ((mask64 >> h) & 1) {
+                        lbox[nbox++] = make_uint2(64 * h | 2u << 8, lgt[8 * h]);
+                        continue;
+                    }
+                    for (int j = 2 * h; j < 2 * h + 2; ++j) {
+                        if ((mask32 >> j) & 1) {
+                            lbox[nbox++] = make_uint2(32 * j | 1u << 8, lgt[4 * j]);
+                            continue;
+                        }
+                        for (int g = 4 * j; g < 4 * j + 4; ++g)
+                            if ((mask8 >> g) & 1) lbox[nbox++] = make_uint2(8 * g, lgt[g]);
+                    }
                 }
-                cp_async_arrive_noinc(&bf[sb]);
             }
-        }
-    } else if (warp == 4 || warp == 5) {
-        // ------------------------------------------------------------ y loaders
-        const int lt = tid - 128;  // 0..63
-        int32_t *rows = reinterpret_cast<int32_t *>(smem + kOffRows + kBM * 4);
-        uint32_t ys = 0;
-        Tile t;
-        while (walker.next(t)) {
-            const int r = p.ranks ? p.ranks[t.a] : p.r_max;
-            const bool live = r <= p.r_max && tc_rank_ok(r);
-            if (!live) continue;
-            asm volatile("bar.sync 2, 64;\n" ::: "memory");  // previous tile done with rows
-            for (int i = lt; i < t.n; i += 64) rows[i] = p.sorted[t.pos + i];
-            asm volatile("bar.sync 2, 64;\n" ::: "memory");
-            for (int nti = 0; nti < n_nt; ++nti, ++ys) {
-                const int nt = nti + nt_rot < n_nt ? nti + nt_rot : nti + nt_rot - n_nt;
-                int sl, c0, nc;
-                ntile_cols(p, nt, sl, c0, nc);
-                const SliceDesc &S = p.slices[sl];
-                const int sy = ys % kSY;
-                if (!wait_warp(&ye[sy], ((ys / kSY) & 1) ^ 1, ok, abort)) goto role_done;
-                unsigned char *yst = smem + kOffY + sy * kYStage;
-                const int nch = nc >> 3;
-                const __nv_bfloat16 *yc = static_cast<const __nv_bfloat16 *>(p.y) + S.y_col + c0;
-                if (nch == kBN / 8) {
-                    for (int e = lt; e < t.n * (kBN / 8); e += 64) {
-                        const int i = e >> 4, c = e & 15;
-                        cp_async16(yst + i * kYPitch + c * 16, yc + (int64_t)rows[i] * p.ldy + c * 8, 16);
+            const uint32_t box_bytes = (uint32_t)__popc(mask8) * 8 * 128;  // per atom
+            // A rows j = i0 + 8q of the stacked block: adapter row, or -1 (zero)
+            const int K16 = (t.K + 15) & ~15;
+            int arow[kTcMaxRank / 8];
+            const __nv_bfloat16 *abase[kTcMaxRank / 8];
+#pragma unroll
+            for (int q = 0; q < kTcMaxRank / 8; ++q) {
+                const int j = i0 + 8 * q;
+                arow[q] = -1;
+                abase[q] = Ag;
+#pragma unroll
+                for (int u = 0; u < kMaxPieces; ++u)
+                    if (u < t.np && j >= t.kofs[u] && j < t.kofs[u] + t.rk[u]) {
+                        arow[q] = j - t.kofs[u];
+                        abase[q] = Ag + (int64_t)t.a[u] * p.a_stride_adapter;
+                    }
+            }
+            // this thread's B chunk (8 rank columns; the same in every y job):
+            // adapter and first column, or -1 (zero)
+            const int n8 = K16 / 8, sh8 = n8 == 2 ? 1 : 2;
+            const int bcb = lt & (n8 - 1);
+            int b_a = 0, b_j = -1;
+#pragma unroll
+            for (int u = 0; u < kMaxPieces; ++u)
+                if (u < t.np && 8 * bcb >= t.kofs[u] && 8 * bcb < t.kofs[u] + t.rk[u]) {
+                    b_a = t.a[u];
+                    b_j = 8 * bcb - t.kofs[u];
+                }
+            const int slot_hi = (lt >> 4) & 1;  // lrow index of row i0 + 8q is 2q + slot_hi
+            if (m.use_ab) {
+                // TMA path.  Lane 0 of warp 0 issues the boxes of atom 0, lane 0 of
+                // warp 1 those of atom 1, A block included.  The 64 threads of warps
+                // 2-3 copy the B block (small and in L2; a TMA box of it would move
+                // 16-byte pieces) and the rows that no box covers (a group split by
+                // a piece boundary or by a break in the token rows), from a list
+                // built once per tile.  Warp 0 stands in for the arrivals of the
+                // other loader threads, which sit these stages out.
+                const int njobs = nkb + n_nt;
+                int covered = 0;
+                for (int g = 0; g < 16; ++g)
+                    if ((mask8 >> g) & 1) covered += min(8, t.n - 8 * g);
+                const int nu = t.n - covered;  // rows moved by cp.async
+                if (warp < 2 && lane == 0) {
+                    const uint32_t stand_in = kLoaderThreads - 64;
+                    for (int jb = 0; jb < njobs; ++jb) {
+                        if (!wait1(&empty[s], ph ^ 1, ok, abort)) goto role_done;
+                        unsigned char *st = smem + s * stage_bytes;
+                        if (jb < nkb) {
+                            const int kb = jb + kb_rot < nkb ? jb + kb_rot : jb + kb_rot - nkb;
+                            const int col = kb * kBK + 64 * hq;
+                            mbar_arrive_expect_tx(&full[s], box_bytes + (uint32_t)(K16 / 8) * 1024);
+                            if (warp == 0) mbar_arrive_n(&full[s], stand_in);
+                            for (int e = 0; e < nbox; ++e) {
+                                const uint2 bx = lbox[e];
+                                const int code = bx.x >> 8, i = bx.x & 255;
+                                tma_load_2d(st + hq * xatom + i * 128, code == 2 ? &m.x64 : code == 1 ? &m.x32 : &m.x8, col,
+                                            (int)bx.y, &full[s]);
+                            }
+                            // the stacked A block of this atom: 8 rank rows per box
+                            unsigned char *abuf = st + xbytes + hq * aatom;
+                            for (int u = 0; u < t.np; ++u)
+                                for (int j = 0; j < sel(t.rk, u); j += 8)
+                                    tma_load_3d(abuf + (sel(t.kofs, u) + j) * 128, &m.a8, col, j, sel(t.a, u), &full[s]);
+                            for (int j = t.K; j < K16; j += 8) tma_load_3d(abuf + j * 128, &m.a8, col, m.r_pad, 0, &full[s]);
+                        } else {
+                            const int nti = jb - nkb, nt = nti + nt_rot < n_nt ? nti + nt_rot : nti + nt_rot - n_nt;
+                            int sl, c0, nc;
+                            ntile_cols(p, nt, sl, c0, nc);
+                            const int col = c0 + 64 * hq;
+                            mbar_arrive_expect_tx(&full[s], box_bytes);
+                            if (warp == 0) mbar_arrive_n(&full[s], stand_in);
+                            for (int e = 0; e < nbox; ++e) {
+                                const uint2 bx = lbox[e];
+                                const int code = bx.x >> 8, i = bx.x & 255;
+                                tma_load_2d(st + hq * xatom + i * 128,
+                                            code == 2 ? &m.y64[sl] : code == 1 ? &m.y32[sl] : &m.y8[sl], col, (int)bx.y,
+                                            &full[s]);
+                            }
+                        }
+                        if (++s == NS) {
+                            s = 0;
+                            ph ^= 1;
+                        }
+                    }
+                } else if (warp >= 2) {
+                    // the uncovered rows: tile row and token row, in this warp's list
+                    int2 *ul = reinterpret_cast<int2 *>(smem + kOffLdr + kLdrRows) + kBM * (warp - 2);
+                    {
+                        int cnt = 0;
+                        __syncwarp();
+                        for (int i0r = 0; i0r < t.n; i0r += 32) {
+                            const int i = i0r + lane;
+                            const bool need = i < t.n && !((mask8 >> (i >> 3)) & 1);
+                            const unsigned bal = __ballot_sync(0xffffffffu, need);
+                            if (need) ul[cnt + __popc(bal & ((1u << lane) - 1))] = make_int2(i, tile_token(p, t, i));
+                            cnt += __popc(bal);
+                        }
+                        __syncwarp();
+                    }
+                    const int hl = lt - 64, hc = hl & 15, hr0 = hl >> 4;  // chunk; first list entry (then every 4th)
+                    // B: chunk hb (8 rank columns) of rows hn0 + (64 / n8) k
+                    const int hb = hl & (n8 - 1), hn0 = hl >> (sh8), hstep = 64 >> sh8;
+                    int hb_a = 0, hb_j = -1;
+#pragma unroll
+                    for (int u = 0; u < kMaxPieces; ++u)
+                        if (u < t.np && 8 * hb >= t.kofs[u] && 8 * hb < t.kofs[u] + t.rk[u]) {
+                            hb_a = t.a[u];
+                            hb_j = 8 * hb - t.kofs[u];
+                        }
+                    for (int jb = 0; jb < njobs; ++jb) {
+                        if (!wait_warp(&empty[s], ph ^ 1, ok, abort)) goto role_done;
+                        unsigned char *st = smem + s * stage_bytes;
+                        if (jb < nkb) {
+                            const int kb = jb + kb_rot < nkb ? jb + kb_rot : jb + kb_rot - nkb;
+                            const int k = kb * kBK + hc * 8;
+                            const bool kin = k < p.d_in;
+                            for (int e = hr0; e < nu; e += 4) {
+                                const int2 ri = ul[e];
+                                const __nv_bfloat16 *row = xg + (int64_t)ri.y * p.ldx;
+                                cp_async16(st + schunk(xatom, ri.x, hc), kin ? row + k : row, kin ? 16 : 0);
+                            }
+                        } else {
+                            const int nti = jb - nkb, nt = nti + nt_rot < n_nt ? nti + nt_rot : nti + nt_rot - n_nt;
+                            int sl, c0, nc;
+                            ntile_cols(p, nt, sl, c0, nc);
+                            const SliceDesc &S = p.slices[sl];
+                            const __nv_bfloat16 *yc = yg + S.y_col + c0;
+                            if (hc * 8 < nc)
+                                for (int e = hr0; e < nu; e += 4) {
+                                    const int2 ri = ul[e];
+                                    cp_async16(st + schunk(xatom, ri.x, hc), yc + (int64_t)ri.y * p.ldy + hc * 8, 16);
+                                }
+                            // the stacked B block: rows c0 .. c0+nc-1 of the slice (columns of no piece zero-filled)
+                            const __nv_bfloat16 *Bb =
+                                static_cast<const __nv_bfloat16 *>(S.B) + (int64_t)hb_a * S.stride_adapter + hb_j;
+                            for (int n = hn0; n < nc; n += hstep)
+                                cp_async16(st + xbytes + hb * kBChunk + n * 16,
+                                           hb_j >= 0 ? Bb + (int64_t)(c0 + n) * S.stride_n : S.B, hb_j >= 0 ? 16 : 0);
+                        }
+                        cp_async_arrive_noinc(&full[s]);
+                        if (++s == NS) {
+                            s = 0;
+                            ph ^= 1;
+                        }
                     }
                 } else {
-                    for (int e = lt; e < t.n * nch; e += 64) {
-                        const int i = e / nch, c = e - i * nch;
-                        cp_async16(yst + i * kYPitch + c * 16, yc + (int64_t)rows[i] * p.ldy + c * 8, 16);
+                    for (int jb = 0; jb < njobs; ++jb)
+                        if (++s == NS) {
+                            s = 0;
+                            ph ^= 1;
+                        }
+                }
+                continue;
+            }
+            for (int kbi = 0; kbi < nkb; ++kbi) {
+                const int kb = kbi + kb_rot < nkb ? kbi + kb_rot : kbi + kb_rot - nkb;
+                if (!wait_warp(&empty[s], ph ^ 1, ok, abort)) goto role_done;
+                unsigned char *st = smem + s * stage_bytes;
+                const int k = kb * kBK + c * 8;
+                const bool kin = k < p.d_in;
+                if (warp < 2 && lane == 0) {
+                    // the expected bytes are announced before the boxes are issued
+                    mbar_arrive_expect_tx(&full[s], box_bytes);
+                    unsigned char *dst = st + hq * xatom;
+                    const int col = kb * kBK + 64 * hq;
+                    for (int e = 0; e < nbox; ++e) {
+                        const uint2 bx = lbox[e];
+                        const int code = bx.x >> 8, i = bx.x & 255;
+                        tma_load_2d(dst + i * 128, code == 2 ? &m.x64 : code == 1 ? &m.x32 : &m.x8, col, (int)bx.y,
+                                    &full[s]);
                     }
                 }
-                cp_async_arrive_noinc(&yf[sy]);
+                // x rows not moved by TMA: two 64-column atoms in the 128-byte swizzle
+                unsigned char *xd = st + (c >> 3) * xatom + (((c & 7) ^ (i0 & 7)) << 4);
+#pragma unroll
+                for (int q = 0; q < kBM / 8; ++q) {
+                    if (!((mine >> q) & 1)) continue;
+                    const __nv_bfloat16 *row = xg + (int64_t)lrow[2 * q + slot_hi] * p.ldx;
+                    cp_async16(xd + (i0 + 8 * q) * 128, kin ? row + k : row, kin ? 16 : 0);
+                }
+                // the stacked A block (rows of no piece, or past a rank, zero-filled)
+                unsigned char *ad = st + xbytes + (c >> 3) * aatom + (((c & 7) ^ (i0 & 7)) << 4);
+#pragma unroll
+                for (int q = 0; q < kTcMaxRank / 8; ++q) {
+                    if (i0 + 8 * q >= K16) break;
+                    const bool in = arow[q] >= 0 && kin;
+                    cp_async16(ad + (i0 + 8 * q) * 128, in ? abase[q] + (int64_t)arow[q] * p.a_stride_r + k : Ag,
+                               in ? 16 : 0);
+                }
+                cp_async_arrive_noinc(&full[s]);
+                if (++s == NS) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+            for (int nti = 0; nti < n_nt; ++nti) {
+                const int nt = nti + nt_rot < n_nt ? nti + nt_rot : nti + nt_rot - n_nt;
+                int sl, c0, nc;
+                ntile_cols(p, nt, sl, c0, nc);
+                const SliceDesc &S = p.slices[sl];
+                if (!wait_warp(&empty[s], ph ^ 1, ok, abort)) goto role_done;
+                unsigned char *st = smem + s * stage_bytes;
+                if (warp < 2 && lane == 0) {
+                    mbar_arrive_expect_tx(&full[s], box_bytes);
+                    unsigned char *dst = st + hq * xatom;
+                    const int col = c0 + 64 * hq;
+                    for (int e = 0; e < nbox; ++e) {
+                        const uint2 bx = lbox[e];
+                        const int code = bx.x >> 8, i = bx.x & 255;
+                        tma_load_2d(dst + i * 128, code == 2 ? &m.y64[sl] : code == 1 ? &m.y32[sl] : &m.y8[sl], col,
+                                    (int)bx.y, &full[s]);
+                    }
+                }
+                const __nv_bfloat16 *yc = yg + S.y_col + c0;
+                if (nc == kBN) {
+#pragma unroll
+                    for (int q = 0; q < kBM / 8; ++q) {
+                        if (!((mine >> q) & 1)) continue;
+                        cp_async16(st + schunk(xatom, i0 + 8 * q, c), yc + (int64_t)lrow[2 * q + slot_hi] * p.ldy + c * 8, 16);
+                    }
+                } else {
+                    const int nch = nc >> 3;
+                    for (int e = lt; e < t.n * nch; e += kLoaderThreads) {
+                        const int i = e / nch, cc = e % nch;
+                        if ((mask8 >> (i >> 3)) & 1) continue;
+                        cp_async16(st + schunk(xatom, i, cc), yc + (int64_t)tile_token(p, t, i) * p.ldy + cc * 8, 16);
+                    }
+                }
+                // the stacked B block: rows c0 .. c0+nc-1 of the slice, 8 rank
+                // columns per 2 KB chunk (columns of no piece zero-filled)
+                const __nv_bfloat16 *Bb = static_cast<const __nv_bfloat16 *>(S.B) + (int64_t)b_a * S.stride_adapter + b_j;
+                for (int e = lt; e < nc * n8; e += kLoaderThreads) {
+                    const int n = e >> sh8;
+                    cp_async16(st + xbytes + bcb * kBChunk + n * 16, b_j >= 0 ? Bb + (int64_t)(c0 + n) * S.stride_n : S.B,
+                               b_j >= 0 ? 16 : 0);
+                }
+                cp_async_arrive_noinc(&full[s]);
+                if (++s == NS) {
+                    s = 0;
+                    ph ^= 1;
+                }
             }
         }
-    } else if (warp == 2) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            uint32_t xs = 0, bs = 0, ts = 0, tiles = 0;
+            uint32_t job = 0, ts = 0, tiles = 0;
             const uint32_t id2 = idesc_bf16(kBM, kBN);
-            const uint32_t x_base = smem_u32(smem + kOffX), b_base = smem_u32(smem + kOffB);
-            const uint32_t h_base = smem_u32(smem + kOffH);
+            const uint32_t ring = smem_u32(smem), h_base = smem_u32(smem + kOffH);
             Tile t;
             while (walker.next(t)) {
-                const int r = p.ranks ? p.ranks[t.a] : p.r_max;
-                const bool live = r <= p.r_max && tc_rank_ok(r);
-                if (!live) continue;
-                const int n16 = (r + 15) / 16;
+                if (t.K == 0) continue;
+                const int n16 = (t.K + 15) / 16;
                 const uint32_t id1 = idesc_bf16(kBM, 16 * n16);
                 // D1 is free again: the previous tile's expand was issued only
                 // after the epilogue had read D1 (hr).
-                for (int kbi = 0; kbi < nkb; ++kbi, ++xs) {
-                    const int s = xs % kSX;
-                    if (!wait1(&xf[s], (xs / kSX) & 1, ok, abort)) goto role_done;
+                for (int kbi = 0; kbi < nkb; ++kbi, ++job) {
+                    const int s = job % NS;
+                    if (!wait1(&full[s], (job / NS) & 1, ok, abort)) goto role_done;
                     tc_fence_after();
-                    const uint32_t xa = x_base + s * kXStage, aa = xa + kXBytes;
+                    const uint32_t xa = ring + s * stage_bytes, aa = xa + xbytes;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * kXAtom + (kk & 3) * 32, aoff = (kk >> 2) * kAAtom + (kk & 3) * 32;
-                        umma(tmem, smem_desc(xa + off, 16, 1024, kLayoutSw128),
-                             smem_desc(aa + aoff, 16, 1024, kLayoutSw128), id1, (kbi | kk) != 0);
+                        const uint32_t off = (kk >> 2) * xatom + (kk & 3) * 32, aoff = (kk >> 2) * aatom + (kk & 3) * 32;
+                        // four accumulators (TMEM columns 32 q) take the K steps in
+                        // turn, so consecutive MMAs do not wait on one another
+                        umma(tmem + 32 * (kk & 3), smem_desc(xa + off, 16, 1024, kLayoutSw128),
+                             smem_desc(aa + aoff, 16, 1024, kLayoutSw128), id1, (kbi | (kk >> 2)) != 0);
                     }
-                    umma_commit(&xe[s]);
+                    // the stage is free once these MMAs have read it
+                    mbar_arrive_n(&empty[s], kEpiWarps - 1);
+                    umma_commit(&empty[s]);
                 }
                 umma_commit(d1f);
                 // H of this tile is ready once the epilogue has written it.
                 if (!wait1(hr, tiles & 1, ok, abort)) goto role_done;
                 tc_fence_after();
-                for (int nt = 0; nt < n_nt; ++nt, ++bs, ++ts) {
-                    const int sb = bs % kSB, st = ts % kST;
-                    if (!wait1(&bf[sb], (bs / kSB) & 1, ok, abort)) goto role_done;
-                    if (!wait1(&te[st], ((ts / kST) & 1) ^ 1, ok, abort)) goto role_done;
+                for (int nt = 0; nt < n_nt; ++nt, ++job, ++ts) {
+                    const int s = job % NS, sd = ts % kST;
+                    if (!wait1(&full[s], (job / NS) & 1, ok, abort)) goto role_done;
+                    if (!wait1(&te[sd], ((ts / kST) & 1) ^ 1, ok, abort)) goto role_done;
                     tc_fence_after();
-                    const uint32_t bb = b_base + sb * kBStage;
-                    const uint32_t d2 = tmem + 128 + 128 * st;
+                    const uint32_t bb = ring + s * stage_bytes + xbytes;
+                    const uint32_t d2 = tmem + 128 + 128 * sd;
                     for (int kc = 0; kc < n16; ++kc)
                         umma(d2, smem_desc(h_base + kc * 2 * kHChunk, kHChunk, 128, kLayoutNone),
                              smem_desc(bb + kc * 2 * kBChunk, kBChunk, 128, kLayoutNone), id2, kc != 0);
-                    umma_commit(&be[sb]);
-                    umma_commit(&tf[st]);
+                    umma_commit(&tf[sd]);
                 }
                 umma_commit(he);
                 ++tiles;
@@ -431,36 +775,46 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int q4 = warp & 3;              // TMEM lane quadrant
-        const int chalf = (warp - 6) >> 2;    // which 64 columns of an n-tile
-        const int row = q4 * 32 + lane;       // tile row owned by this thread
+        const int ew = warp - kEpiWarp0;     // 0..7
+        const int q4 = warp & 3;             // TMEM lane quadrant
+        const int chalf = ew >> 2;           // which 64 columns of an n-tile
+        const int row = q4 * 32 + lane;      // tile row owned by this thread
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         unsigned char *H = smem + kOffH;
-        uint32_t ys = 0, ts = 0, tiles = 0;
+        __nv_bfloat16 *yw = static_cast<__nv_bfloat16 *>(p.y);
+        uint32_t job = 0, ts = 0, tiles = 0;
         Tile t;
         while (walker.next(t)) {
-            const int r = p.ranks ? p.ranks[t.a] : p.r_max;
-            const bool live = r <= p.r_max && tc_rank_ok(r);
-            if (!live) {
-                // Tiles the tensor cores cannot take are the CUDA-core
-                // kernel's; with the tensor-core path forced they are an error.
-                if (p.tc_only && row == 0 && chalf == 0 && r != 0) raise_deverr(p.counts, LORA_DEVERR_RANK);
-                continue;
-            }
-            const float sc = p.adapter_scale ? p.adapter_scale[t.a] : p.scale;
-            const int n16 = (r + 15) / 16;
-            const int my_row = row < t.n ? p.sorted[t.pos + row] : 0;  // this thread's token row
+            // Pieces the tensor cores cannot take are the CUDA-core kernel's;
+            // with the tensor-core path forced they are an error.
+            if (p.tc_only && ew == 0 && lane < t.np && sel(t.rk, lane) == 0 && sel(t.rank, lane) != 0)
+                raise_deverr(p.counts, LORA_DEVERR_RANK);
+            if (t.K == 0) continue;
+            job += nkb;  // the x stages of this tile are the MMA's
+            const int K16 = (t.K + 15) & ~15;
+            // this thread's row: token row, piece, rank columns and scale
+            const int pq = row < t.n ? t.piece_of(row) : 0;
+            const bool live = row < t.n && sel(t.rk, pq) > 0;
+            const int my_tok = row < t.n ? tile_token(p, t, row) : 0;
+            const int k_lo = live ? sel(t.kofs, pq) : 0, k_hi = live ? sel(t.kofs, pq) + sel(t.rk, pq) : 0;
+            const float sc = live ? (p.adapter_scale ? p.adapter_scale[sel(t.a, pq)] : p.scale) : 0.f;
             if (chalf == 0) {
-                // ---- D1 -> scale -> bf16 H (cols >= r are zero)
+                // ---- D1 -> scale -> bf16 H (columns of other pieces are zero)
                 if (!wait_warp(d1f, tiles & 1, ok, abort)) goto role_done;
                 tc_fence_after();
                 if (tiles > 0)
                     if (!wait_warp(he, (tiles - 1) & 1, ok, abort)) goto role_done;  // previous expand done with H
                 for (int c16 = 0; c16 < kTcMaxRank / 16; ++c16) {
-                    if (c16 >= n16) break;
-                    uint32_t v[16];
+                    if (16 * c16 >= K16) break;
+                    uint32_t v[16], u[3][16];
                     tmem_ld16(tmem + lane_off + 16 * c16, v);
+#pragma unroll
+                    for (int q = 0; q < 3; ++q) tmem_ld16(tmem + lane_off + 32 * (q + 1) + 16 * c16, u[q]);
                     tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        v[e] = __float_as_uint((__uint_as_float(v[e]) + __uint_as_float(u[0][e])) +
+                                               (__uint_as_float(u[1][e]) + __uint_as_float(u[2][e])));
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         const int c8 = 2 * c16 + half;
@@ -468,8 +822,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int j = 8 * c8 + 2 * e;
-                            const float f0 = j < r ? __uint_as_float(v[8 * half + 2 * e]) * sc : 0.f;
-                            const float f1 = j + 1 < r ? __uint_as_float(v[8 * half + 2 * e + 1]) * sc : 0.f;
+                            const float f0 = j >= k_lo && j < k_hi ? __uint_as_float(v[8 * half + 2 * e]) * sc : 0.f;
+                            const float f1 = j + 1 >= k_lo && j + 1 < k_hi ? __uint_as_float(v[8 * half + 2 * e + 1]) * sc : 0.f;
                             const __nv_bfloat162 h2 = __floats2bfloat162_rn(f0, f1);
                             w[e] = *reinterpret_cast<const uint32_t *>(&h2);
                         }
@@ -478,62 +832,72 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(hr);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(hr);
             }
-            // ---- expand n-tiles: y += D2 (this thread: its row, 64 columns)
-            for (int nti = 0; nti < n_nt; ++nti, ++ys, ++ts) {
+            // ---- expand n-tiles: y += D2 (this warp: 32 rows x 64 columns)
+            for (int nti = 0; nti < n_nt; ++nti, ++job, ++ts) {
                 const int nt = nti + nt_rot < n_nt ? nti + nt_rot : nti + nt_rot - n_nt;
-                const int sy = ys % kSY, st = ts % kST;
+                const int s = job % NS, sd = ts % kST;
                 int sl, c0, nc;
                 ntile_cols(p, nt, sl, c0, nc);
                 const SliceDesc &S = p.slices[sl];
-                if (!wait_warp(&tf[st], (ts / kST) & 1, ok, abort)) goto role_done;
-                if (!wait_warp(&yf[sy], (ys / kSY) & 1, ok, abort)) goto role_done;
+                if (!wait_warp(&tf[sd], (ts / kST) & 1, ok, abort)) goto role_done;
+                if (!wait_warp(&full[s], (job / NS) & 1, ok, abort)) goto role_done;
                 tc_fence_after();
-                const unsigned char *yrow = smem + kOffY + sy * kYStage + row * kYPitch;
-                __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.y) + (int64_t)my_row * p.ldy + S.y_col + c0;
-                uint4 outv[8];
-                const int cbase = 64 * chalf;
+                uint32_t v[4][16];
+                const uint32_t ta = tmem + 128 + 128 * sd + lane_off + 64 * chalf;
 #pragma unroll
-                for (int c32 = 0; c32 < 2; ++c32) {
-                    uint32_t v0[16], v1[16];
-                    const uint32_t ta = tmem + 128 + 128 * st + lane_off + cbase + 32 * c32;
-                    tmem_ld16(ta, v0);
-                    tmem_ld16(ta + 16, v1);
-                    tmem_wait_ld();
+                for (int q = 0; q < 4; ++q) tmem_ld16(ta + 16 * q, v[q]);
+                tmem_wait_ld();
+                // the TMEM buffer is free as soon as it is read
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&te[sd]);
+                unsigned char *ys = smem + s * stage_bytes;
+                if (live) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint4 yv = *reinterpret_cast<const uint4 *>(yrow + (cbase + 32 * c32) * 2 + q * 16);
-                        uint32_t *yw = reinterpret_cast<uint32_t *>(&yv);
+                    for (int q = 0; q < 8; ++q) {
+                        uint4 *pq4 = reinterpret_cast<uint4 *>(ys + schunk(xatom, row, 8 * chalf + q));
+                        uint4 yv = *pq4;
+                        uint32_t *yw32 = reinterpret_cast<uint32_t *>(&yv);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int j = q * 8 + 2 * e;
-                            const uint32_t a0 = j < 16 ? v0[j] : v1[j - 16];
-                            const uint32_t a1 = j + 1 < 16 ? v0[j + 1] : v1[j + 1 - 16];
-                            const float y0 = __uint_as_float(yw[e] << 16) + __uint_as_float(a0);
-                            const float y1 = __uint_as_float(yw[e] & 0xFFFF0000u) + __uint_as_float(a1);
+                            const uint32_t a0 = v[q >> 1][(q & 1) * 8 + 2 * e];
+                            const uint32_t a1 = v[q >> 1][(q & 1) * 8 + 2 * e + 1];
+                            const float y0 = __uint_as_float(yw32[e] << 16) + __uint_as_float(a0);
+                            const float y1 = __uint_as_float(yw32[e] & 0xFFFF0000u) + __uint_as_float(a1);
                             const __nv_bfloat162 o = __floats2bfloat162_rn(y0, y1);
-                            yw[e] = *reinterpret_cast<const uint32_t *>(&o);
+                            yw32[e] = *reinterpret_cast<const uint32_t *>(&o);
                         }
-                        outv[c32 * 4 + q] = yv;
+                        *pq4 = yv;
                     }
                 }
-                // TMEM buffer and y stage are free as soon as they are read
-                tc_fence_before();
-                mbar_arrive(&te[st]);
-                mbar_arrive(&ye[sy]);
-                if (row < t.n) {
+                __syncwarp();
+                // store the warp's live rows: 4 rows x 128 bytes per instruction
+                // (st.global: TMA stores mixed with these in one CTA stalled its loads)
+                {
+                    const int cq = lane & 7, col = (8 * chalf + cq) * 8;
+                    __nv_bfloat16 *ydst = yw + S.y_col + c0 + col;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        if (cbase + 8 * k < nc) *reinterpret_cast<uint4 *>(dst + cbase + 8 * k) = outv[k];
+                    for (int k = 0; k < 8; ++k) {
+                        const int rl = 4 * k + (lane >> 3);
+                        const int tok = __shfl_sync(0xffffffffu, my_tok, rl);
+                        const bool lv = __shfl_sync(0xffffffffu, live, rl);
+                        if (lv && col < nc)
+                            *reinterpret_cast<uint4 *>(ydst + (int64_t)tok * p.ldy) =
+                                *reinterpret_cast<const uint4 *>(ys + schunk(xatom, q4 * 32 + rl, 8 * chalf + cq));
+                    }
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
             }
             ++tiles;
         }
     }
 role_done:
-    bulk_wait0();
-    if (warp == 2 && lane == 0) {
+    if (warp < kLoaderWarps) asm volatile("cp.async.wait_all;\n" ::: "memory");
+    if (warp == kMmaWarp && lane == 0) {
         // every MMA this CTA issued has completed before TMEM is released
         umma_commit(fin);
         if (!mbar_wait(fin, 0)) ok = false;
@@ -541,7 +905,7 @@ role_done:
     if (!ok) raise_deverr(p.counts, LORA_DEVERR_WAIT);
     tc_fence_before();
     __syncthreads();
-    if (warp == 2) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tmem) : "memory");
     }
@@ -552,6 +916,40 @@ role_done:
 // ---------------------------------------------------------------------------
 bool tc_available() { return true; }
 
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver (no link-time dependency on it).
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// Row-major bf16 matrix of `rows` x `cols` with row pitch `ld` elements;
+// boxes of 64 columns x box_rows rows, 128-byte swizzle, zero fill.
+bool encode_rows(EncodeTiledFn fn, CUtensorMap *map, const void *base, int64_t cols, int64_t rows, int64_t ld,
+                 int box_rows) {
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    const cuuint32_t elem[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, elem,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 cudaError_t launch_tc(const DeltaArgs &p, int mode, int sms, cudaStream_t stream) {
     if (mode != kFused) return cudaErrorNotSupported;
     static DeviceOnce once;
@@ -559,6 +957,45 @@ cudaError_t launch_tc(const DeltaArgs &p, int mode, int sms, cudaStream_t stream
         return cudaFuncSetAttribute(sgmv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
     });
     if (e != cudaSuccess) return e;
+    // Tensor maps for the TMA copies of contiguous row groups; without them
+    // (no driver entry point, a shape the encoder refuses) every row moves
+    // by cp.async.
+    TcMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    EncodeTiledFn fn = encode_fn();
+    bool use = fn != nullptr;
+    if (use)
+        use = encode_rows(fn, &maps.x64, p.x, p.d_in, p.M_rows, p.ldx, 64) &&
+              encode_rows(fn, &maps.x32, p.x, p.d_in, p.M_rows, p.ldx, 32) &&
+              encode_rows(fn, &maps.x8, p.x, p.d_in, p.M_rows, p.ldx, 8);
+    for (int t = 0; use && t < p.n_slices; ++t) {
+        const void *yb = static_cast<const __nv_bfloat16 *>(p.y) + p.slices[t].y_col;
+        use = encode_rows(fn, &maps.y64[t], yb, p.slices[t].d_out, p.M_rows, p.ldy, 64) &&
+              encode_rows(fn, &maps.y32[t], yb, p.slices[t].d_out, p.M_rows, p.ldy, 32) &&
+              encode_rows(fn, &maps.y8[t], yb, p.slices[t].d_out, p.M_rows, p.ldy, 8);
+    }
+    maps.use = use ? 1 : 0;
+    // A and B pools as 3-D maps (rank rows / columns past r_pad read zeros)
+    bool use_ab = use;
+    maps.r_pad = (p.r_max + 7) & ~7;
+    if (use_ab) {
+        const cuuint64_t dims[3] = {(cuuint64_t)p.d_in, (cuuint64_t)p.r_max, (cuuint64_t)p.n_adapters};
+        const cuuint64_t strides[2] = {(cuuint64_t)(p.a_stride_r * 2), (cuuint64_t)(p.a_stride_adapter * 2)};
+        const cuuint32_t box[3] = {64, 8, 1}, elem[3] = {1, 1, 1};
+        use_ab = fn(&maps.a8, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p.A), dims, strides, box, elem,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    for (int t = 0; use_ab && t < p.n_slices; ++t) {
+        const SliceDesc &S = p.slices[t];
+        const cuuint64_t dims[3] = {(cuuint64_t)p.r_max, (cuuint64_t)S.d_out, (cuuint64_t)p.n_adapters};
+        const cuuint64_t strides[2] = {(cuuint64_t)(S.stride_n * 2), (cuuint64_t)(S.stride_adapter * 2)};
+        const cuuint32_t box[3] = {8, (cuuint32_t)kBN, 1}, elem[3] = {1, 1, 1};
+        use_ab = fn(&maps.b[t], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(S.B), dims, strides, box, elem,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    maps.use_ab = use_ab ? 1 : 0;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -569,7 +1006,7 @@ cudaError_t launch_tc(const DeltaArgs &p, int mode, int sms, cudaStream_t stream
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, sgmv_tc_kernel, p);
+    return cudaLaunchKernelEx(&cfg, sgmv_tc_kernel, p, maps);
 }
 
 }  // namespace lora

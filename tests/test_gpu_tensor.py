@@ -46,6 +46,8 @@ TC_CASES = [
          ranks=[8, 16, 24, 32], per_adapter_scale=True),                         # slices, mixed ranks
     dict(M=180, d_in=192, d_outs=[256], n_pool=7, r_max=24, run_len=3),          # scattered rows
     dict(M=64, d_in=128, d_outs=[128], n_pool=2, r_max=8, run_len=64),
+    dict(M=400, d_in=328, d_outs=[200, 72], n_pool=3, r_max=16, run_len=77),     # 32-row groups + partial group, ragged slices
+    dict(M=1100, d_in=4096, d_outs=[1024], n_pool=2, r_max=16, run_len=550),     # long contiguous runs
 ]
 
 
