@@ -199,6 +199,42 @@ lora_status_t lora_prepare_batch(const int32_t *ids, int32_t M, int32_t n_adapte
                                  lora_batch_t *batch, void *stream);
 
 /*
+ * lora_prepare_batch with no caller workspace and no allocation: the
+ * metadata goes to a device array that this library owns
+ * (LORA_STATIC_WORKSPACE_BYTES on every GPU that loads the library, held
+ * until the process exits).  The pages have no counterpart of this call; it
+ * is for callers that cannot allocate device memory at the point where they
+ * build a batch: code running inside another framework that owns the
+ * device's memory through its own allocator and forbids direct cudaMalloc,
+ * or a serving loop that must not pay cudaMalloc's device-wide
+ * synchronisation on its step path.
+ *
+ * Arguments and result are those of lora_prepare_batch, without workspace
+ * and workspace_bytes.  The batch needs lora_workspace_size(M, n_adapters,
+ * chunk_size) <= LORA_STATIC_WORKSPACE_BYTES (4 MiB: for example M up to
+ * 131072 rows with 4096 adapters unchunked); a larger batch returns
+ * LORA_ERR_WORKSPACE and launches nothing.  The call allocates no memory:
+ * no cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * Set-up: the first call on a device (the current device) looks up the
+ * array's device address (cudaGetSymbolAddress); make that first call
+ * before any stream capture.  A failed look-up returns LORA_ERR_CUDA.
+ *
+ * Sharing: every call on a device writes the same array, and the array
+ * keeps the last call's contents.  A batch returned by this call stays
+ * valid only until the next lora_prepare_batch_static on that device has
+ * run; calls whose kernels can overlap on the GPU (different streams
+ * without ordering, or a later call before the previous batch's
+ * lora_shrink / lora_expand / lora_delta have run) race.  The kernel
+ * rewrites every value the batch reads, so nothing has to be cleared
+ * between calls.
+ */
+#define LORA_STATIC_WORKSPACE_BYTES (4u << 20)
+lora_status_t lora_prepare_batch_static(const int32_t *ids, int32_t M, int32_t n_adapters,
+                                        int32_t chunk_size, int32_t tc_min_rows, lora_batch_t *batch,
+                                        void *stream);
+
+/*
  * Shrink: h[i, j] = sum_k x[i, k] * A[a, j, k] for j < r_a, and 0 for
  * r_a <= j < r_max, for every row i in a segment (unscaled; "vLLM-Ascend
  * LoRA" article, section 3.2: first project d_in down to r).  Rows in no

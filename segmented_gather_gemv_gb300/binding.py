@@ -8,6 +8,7 @@ or if a call returns an error status; there is no fallback.
 Calls (same names as the C ABI):
   lora_workspace_size(M, n_adapters, chunk_size) -> int
   lora_prepare_batch(ids, n_adapters, chunk_size=0, tc_min_rows=0) -> Batch
+  lora_prepare_batch_static(ids, n_adapters, chunk_size=0, tc_min_rows=0) -> Batch
   lora_shrink(batch, x, A_pool, h=None, ranks=None, path=PATH_AUTO) -> h
   lora_expand(batch, h, B_pools, y, scale=1.0, adapter_scale=None,
               ranks=None, y_cols=None, path=PATH_AUTO) -> y
@@ -88,6 +89,8 @@ def lib() -> ctypes.CDLL:
             L.lora_prepare_batch.restype = ctypes.c_int
             L.lora_prepare_batch.argtypes = [vp, i32, i32, i32, i32, vp, ctypes.c_size_t,
                                              ctypes.POINTER(_Batch), vp]
+            L.lora_prepare_batch_static.restype = ctypes.c_int
+            L.lora_prepare_batch_static.argtypes = [vp, i32, i32, i32, i32, ctypes.POINTER(_Batch), vp]
             L.lora_shrink.restype = ctypes.c_int
             L.lora_shrink.argtypes = [ctypes.POINTER(_Batch), i32, vp, i64, i32, vp, i64, i64,
                                       i32, vp, vp, i64, i32, vp]
@@ -156,6 +159,13 @@ def _ld(t: torch.Tensor, dim: int = 0) -> int:
     return t.stride(dim)
 
 
+class _DeviceInts:
+    """n int32 at a device address, for torch.as_tensor (no copy)."""
+
+    def __init__(self, ptr: int, n: int):
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": "<i4", "data": (ptr, False), "version": 3}
+
+
 class Batch:
     """Device segment metadata of one batch (wraps ``lora_batch_t``).
 
@@ -176,8 +186,11 @@ class Batch:
         return self.raw.max_segs
 
     def _view(self, field: str, n: int) -> torch.Tensor:
+        ptr = getattr(self.raw, field)
+        if self.workspace is None:  # the library's own workspace: wrap the device pointer
+            return torch.as_tensor(_DeviceInts(ptr, n), device="cuda")
         base = self.workspace.data_ptr()
-        off = getattr(self.raw, field) - base
+        off = ptr - base
         assert off % 4 == 0 and off >= 0
         flat = self.workspace.view(torch.int32)
         return flat[off // 4: off // 4 + n]
@@ -233,6 +246,23 @@ def lora_prepare_batch(ids: torch.Tensor, n_adapters: int, chunk_size: int = 0,
                                     workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                     ctypes.byref(raw), _stream(stream)))
     return Batch(raw, workspace, ids)
+
+
+def lora_prepare_batch_static(ids: torch.Tensor, n_adapters: int, chunk_size: int = 0,
+                              tc_min_rows: int = 0, stream=None) -> Batch:
+    """lora_prepare_batch into the library's own device workspace (no
+    allocation); the batch is valid until the next call of this function on
+    the same device has run."""
+    if ids.dim() != 1:
+        raise ValueError("ids must be 1-D")
+    M = ids.shape[0]
+    ids_ptr = _dev_ptr(ids, "ids", torch.int32) if M else (ids.data_ptr() or None)
+    if M and not ids.is_contiguous():
+        raise ValueError("ids must be contiguous")
+    raw = _Batch()
+    _check(lib().lora_prepare_batch_static(ids_ptr, M, int(n_adapters), int(chunk_size), int(tc_min_rows),
+                                           ctypes.byref(raw), _stream(stream)))
+    return Batch(raw, None, ids)
 
 
 def _slices(B_pools, y: torch.Tensor, y_cols, r_max: int, dtype):

@@ -5,6 +5,7 @@
 #include <cstdio>
 #include <cstring>
 #include <atomic>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -298,3 +299,56 @@ int32_t lora_abi_version(void) { return 100; }
 int64_t lora_launch_count(void) { return launch_counter().load(std::memory_order_relaxed); }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// lora_prepare_batch_static: the workspace is a device array of this library.
+// ---------------------------------------------------------------------------
+// One copy per GPU that loads the library, alive until the process exits;
+// every call on a device shares it.  In host code the name stands for the
+// symbol only: its device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_static_workspace[LORA_STATIC_WORKSPACE_BYTES];
+
+namespace {
+
+std::mutex g_static_mu;
+void *g_static_addr[64];  // device address of g_static_workspace, per device
+
+// Device address of the array on the current device, looked up once per
+// device (the first call on a device, which should precede any capture).
+lora_status_t static_workspace(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(LORA_ERR_UNSUPPORTED, "device %d: at most 64 devices", dev);
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_addr[dev]) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_static_workspace);
+        if (e != cudaSuccess || !ptr)
+            return fail(LORA_ERR_CUDA, "cudaGetSymbolAddress of the static workspace failed: %s",
+                        cudaGetErrorString(e));
+        g_static_addr[dev] = ptr;
+    }
+    *out = g_static_addr[dev];
+    return LORA_OK;
+}
+
+}  // namespace
+
+extern "C" lora_status_t lora_prepare_batch_static(const int32_t *ids, int32_t M, int32_t n_adapters,
+                                                   int32_t chunk_size, int32_t tc_min_rows, lora_batch_t *batch,
+                                                   void *stream) {
+    g_err[0] = 0;
+    if (M < 0 || M > LORA_MAX_TOKENS || n_adapters < 1 || chunk_size < 0)
+        return fail(LORA_ERR_INVALID, "M %d, n_adapters %d or chunk_size %d out of range", M, n_adapters, chunk_size);
+    const size_t need = ws_layout(M, n_adapters, chunk_size).total;
+    if (need > LORA_STATIC_WORKSPACE_BYTES)
+        return fail(LORA_ERR_WORKSPACE,
+                    "batch needs %zu workspace bytes; the static workspace holds %u (LORA_STATIC_WORKSPACE_BYTES)",
+                    need, (unsigned)LORA_STATIC_WORKSPACE_BYTES);
+    void *ws = nullptr;
+    const lora_status_t st = static_workspace(&ws);
+    if (st != LORA_OK) return st;
+    return lora_prepare_batch(ids, M, n_adapters, chunk_size, tc_min_rows, ws, LORA_STATIC_WORKSPACE_BYTES, batch,
+                              stream);
+}
