@@ -206,6 +206,27 @@ def cpu_baseline(w: wl.Workload, seconds: float) -> dict:
                       % (reps, w.M, dt)}
 
 
+def replica_seed(rank: int) -> int:
+    """Seed of rank `rank`'s batch: every replica draws its own batch (weak scaling)."""
+    return 42 + rank
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest x over all ranks (the job's time is its slowest rank's)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tokens_per_s(world: int, steps: int, rows_per_step: int, elapsed_ms: float) -> float:
+    """Tokens of all ranks' timed steps over the slowest rank's time."""
+    return world * steps * rows_per_step / (elapsed_ms / 1e3)
+
+
 def run_reference(args, rank: int, world: int):
     if rank != 0:
         return
@@ -264,7 +285,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     factory, default_steps = WORKLOADS[args.workload]
     K = args.steps if args.steps is not None else default_steps
     W = max(3, args.warmup)
-    w = factory(42 + rank)  # every rank its own batch (weak scaling)
+    w = factory(replica_seed(rank))
     es = 2 if w.dtype == "bf16" else 4
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     ab = algorithmic_bytes(w)
@@ -380,11 +401,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         dist.barrier()
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
 
     # Kernel durations: the same steps replayed once more with event nodes
     # around every kernel, right after the timed region.
@@ -397,7 +414,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             prep_us.append(1e3 * e0.elapsed_time(e1))
             delta_us.append(1e3 * e1.elapsed_time(e2))
     ms_per_step = elapsed_ms / K
-    value = world * K * w.M / (elapsed_ms / 1e3)
+    value = whole_job_tokens_per_s(world, K, w.M, elapsed_ms)
 
     # e2e: the public API from pinned host buffers, copies inside the region.
     x_h = torch.from_numpy(w.x).to(tdt).pin_memory()
@@ -427,7 +444,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     peak, peak_kind = load_peaks()
     d_us = statistics.mean(delta_us) if delta_us else None
     achieved = ab["total"] / (d_us * 1e-6) / 1e9 if d_us else None
-    kernel = "sgmv_cc_kernel"
+    # dominant kernel: the tensor-core one when most active rows are in its segments
+    kernel = "sgmv_tc_kernel" if 2 * counts["tc_rows"] > max(1, counts["num_active"]) else "sgmv_cc_kernel"
     traffic = committed_traffic(kernel, args.workload)
 
     if rank != 0:
@@ -456,6 +474,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "frac_of_8tbs_delta": achieved / NOMINAL_HBM_GBS if achieved else None,
         "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s",
+                     "duration": "mean event time of the lora_delta call (its CUDA-core and "
+                                 "tensor-core launches together)",
                      "frac": achieved / peak if achieved else None, "traffic": traffic},
         "e2e": {"value": w.M / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
