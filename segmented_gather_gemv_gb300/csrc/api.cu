@@ -167,17 +167,24 @@ lora_status_t dispatch(const lora_batch_t *b, int32_t dtype, int mode, int32_t p
         p.min_len = 0;
         p.max_len = split ? b->tc_min_rows : 0x7fffffff;
         p.split_tc = split ? 1 : 0;
-        e = launch_cc(p, dtype, mode, cluster, sms, stream);
-        if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
-        if (e == cudaSuccess && split && b->M >= b->tc_min_rows) {
-            p.tc_ptr = b->tc_indptr;
-            p.tc_start = b->tc_segs;
-            p.tc_adapter = b->tc_segs + 2;
-            p.tc_rec_stride = 4;
-            p.tc_count_index = LORA_COUNT_TC_SEGS;
-            p.tc_rows_index = LORA_COUNT_TC_ROWS;
-            p.tc_only = 0;
-            e = launch_tc(p, mode, sms, stream);
+        // The two kernels write disjoint rows of y.  The tensor-core kernel
+        // goes first: when the batch has no long segment its CTAs leave right
+        // after prepare, instead of queueing for SMs behind the CUDA-core
+        // kernel's CTAs at the end of the call.
+        if (split && b->M >= b->tc_min_rows) {
+            DeltaArgs q = p;
+            q.tc_ptr = b->tc_indptr;
+            q.tc_start = b->tc_segs;
+            q.tc_adapter = b->tc_segs + 2;
+            q.tc_rec_stride = 4;
+            q.tc_count_index = LORA_COUNT_TC_SEGS;
+            q.tc_rows_index = LORA_COUNT_TC_ROWS;
+            q.tc_only = 0;
+            e = launch_tc(q, mode, sms, stream);
+            if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
+        }
+        if (e == cudaSuccess) {
+            e = launch_cc(p, dtype, mode, cluster, sms, stream);
             if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
         }
     }

@@ -386,16 +386,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fence_mbar_init();
         *abort = 0;
     }
-    if (warp == kMmaWarp) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(smem_u32(tmem_slot))
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-
     griddep_launch_dependents();
     griddep_wait();
 
@@ -413,6 +403,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     }
     __syncthreads();
+    // A CTA without rows (no tensor-core segments in this batch, or fewer
+    // rows than CTAs) leaves before it takes TMEM.
+    if (range[0] >= range[1]) return;
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(smem_u32(tmem_slot))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
     TileWalker walker{&p, range[0], range[1], range[2]};
     // Stage geometry of this CTA (same in every role).
     const int cap = min(kBM, (range[1] - range[0] + 7) & ~7);
