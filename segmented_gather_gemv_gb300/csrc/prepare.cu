@@ -41,6 +41,7 @@ struct PrepArgs {
     int32_t *whist;
     // shared-memory placement (byte offsets into dynamic shared memory, -1 = global)
     int32_t off_ids, off_adapters, off_groups, off_hist;
+    int32_t off_bits;  // first-appearance bitmap and its word prefix, or -1
 };
 
 // Block-wide exclusive scan of one value per thread.  `ws` is shared scratch
@@ -111,20 +112,44 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
     if (tid == 0) s_invalid = 0;
     __syncthreads();
     int bad = 0;
-    for (int base = 0; base < M; base += nthr) {
-        // Warp-aggregated: the lanes holding the same adapter elect one lane,
-        // which adds their count and offers their first row (runs of equal
-        // ids, as in prefill batches, would otherwise serialize).
-        const int i = base + tid;
-        int a = i < M ? ids[i] : -1;
-        if (a != -1 && (a < 0 || a >= n)) {
-            ++bad;
-            a = -1;
+    // Each warp walks its own contiguous rows.  A chunk of 32 equal ids (runs,
+    // as in prefill batches) only extends the warp's current run, kept in
+    // registers and added once when the run ends; mixed chunks elect one lane
+    // per adapter.  So warps do not queue on the same shared-memory counter.
+    const int per_warp = (M + nwarps - 1) / nwarps;
+    const int w0 = min(M, warp * per_warp), w1 = min(M, w0 + per_warp);
+    {
+        int run_a = -1, run_cnt = 0, run_first = 0;  // the same in every lane
+        for (int b = w0; b < w1; b += 32) {
+            const int i = b + lane;
+            int a = i < w1 ? ids[i] : -1;
+            if (i < w1 && a != -1 && (a < 0 || a >= n)) {
+                ++bad;
+                a = -1;
+            }
+            const int a0 = __shfl_sync(0xffffffffu, a, 0);
+            if (__all_sync(0xffffffffu, a == a0)) {
+                if (a0 != run_a) {
+                    if (lane == 0 && run_a >= 0) {
+                        atomicMin(&first_pos[run_a], run_first);
+                        atomicAdd(&acnt[run_a], run_cnt);
+                    }
+                    run_a = a0;
+                    run_first = b;
+                    run_cnt = 0;
+                }
+                run_cnt += 32;
+            } else {
+                const unsigned peers = __match_any_sync(0xffffffffu, a);
+                if (a >= 0 && lane == __ffs(peers) - 1) {
+                    atomicMin(&first_pos[a], i);
+                    atomicAdd(&acnt[a], __popc(peers));
+                }
+            }
         }
-        const unsigned peers = __match_any_sync(0xffffffffu, a);
-        if (a >= 0 && lane == __ffs(peers) - 1) {
-            atomicMin(&first_pos[a], i);
-            atomicAdd(&acnt[a], __popc(peers));
+        if (lane == 0 && run_a >= 0) {
+            atomicMin(&first_pos[run_a], run_first);
+            atomicAdd(&acnt[run_a], run_cnt);
         }
     }
 #pragma unroll
@@ -134,7 +159,37 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
 
     // Phase 2: group number by order of first appearance.
     int G = 0;
-    if (n <= nthr && n <= 512 && p.off_adapters >= 0) {
+    if (p.off_bits >= 0 && p.off_adapters >= 0) {
+        // The group of a present adapter a is the number of present adapters
+        // that first appear before it: set one bit per first appearance, then
+        // count the bits below first_pos[a] (word prefix sums + popcount).
+        uint32_t *bits = reinterpret_cast<uint32_t *>(smem_raw + p.off_bits);
+        const int nw = (M + 31) >> 5;
+        int32_t *wpre = reinterpret_cast<int32_t *>(bits + nw);
+        for (int w = tid; w < nw; w += nthr) bits[w] = 0u;
+        __syncthreads();
+        for (int a = tid; a < n; a += nthr)
+            if (acnt[a] > 0) atomicOr(&bits[first_pos[a] >> 5], 1u << (first_pos[a] & 31));
+        __syncthreads();
+        int run = 0;
+        for (int base = 0; base < nw; base += nthr) {
+            const int w = base + tid;
+            int tot;
+            const int ex = block_excl_scan(w < nw ? __popc(bits[w]) : 0, &tot, scan_ws);
+            if (w < nw) wpre[w] = run + ex;
+            run += tot;
+        }
+        G = run;
+        __syncthreads();
+        for (int a = tid; a < n; a += nthr)
+            if (acnt[a] > 0) {
+                const int fp = first_pos[a];
+                const int rank = wpre[fp >> 5] + __popc(bits[fp >> 5] & ((1u << (fp & 31)) - 1u));
+                agroup[a] = rank;
+                gadapter[rank] = a;
+            }
+        __syncthreads();
+    } else if (n <= nthr && n <= 512 && p.off_adapters >= 0) {
         // Small pool: the group of adapter a is the number of present
         // adapters that first appear before it (every thread reads the same
         // entries in step, so the shared-memory reads are broadcasts).
@@ -248,20 +303,34 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
     // Phase 5: stable row positions.
     for (int k = tid; k < nwarps * G; k += nthr) whist[k] = 0;
     __syncthreads();
-    const int per_warp = (M + nwarps - 1) / nwarps;
-    const int w0 = warp * per_warp;
-    const int w1 = min(M, w0 + per_warp);
     int32_t *wh = whist + warp * G;
-    for (int b = w0; b < w1; b += 32) {
-        const int i = b + lane;
-        int g = -1;
-        if (i < w1) {
-            const int a = ids[i];
-            if (a >= 0 && a < n) g = agroup[a];
+    // Rows of this warp per group (the same contiguous rows as phase 1); a
+    // run of 32 equal groups is counted in registers.
+    {
+        int run_g = -1, run_c = 0;
+        for (int b = w0; b < w1; b += 32) {
+            const int i = b + lane;
+            int g = -1;
+            if (i < w1) {
+                const int a = ids[i];
+                if (a >= 0 && a < n) g = agroup[a];
+            }
+            const int g0 = __shfl_sync(0xffffffffu, g, 0);
+            if (__all_sync(0xffffffffu, g == g0)) {
+                if (g0 != run_g) {
+                    if (lane == 0 && run_g >= 0) wh[run_g] += run_c;
+                    __syncwarp();
+                    run_g = g0;
+                    run_c = 0;
+                }
+                run_c += 32;
+            } else {
+                const unsigned peers = __match_any_sync(0xffffffffu, g);
+                if (g >= 0 && lane == __ffs(peers) - 1) wh[g] += __popc(peers);
+                __syncwarp();
+            }
         }
-        const unsigned peers = __match_any_sync(0xffffffffu, g);
-        if (g >= 0 && lane == __ffs(peers) - 1) wh[g] += __popc(peers);
-        __syncwarp();
+        if (lane == 0 && run_g >= 0) wh[run_g] += run_c;
     }
     __syncthreads();
     for (int g = tid; g < G; g += nthr) {
@@ -273,27 +342,53 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
         }
     }
     __syncthreads();
-    for (int b = w0; b < w1; b += 32) {
-        const int i = b + lane;
-        int g = -1;
-        if (i < w1) {
-            const int a = ids[i];
-            if (a >= 0 && a < n) g = agroup[a];
+    // Positions: the warp's next free slot of each group, in registers for
+    // the current run.
+    auto place_row = [&](int i, int g, int pos) {
+        p.sorted[pos] = i;
+        // first rows of every segment, inline in its descriptor
+        const int off = pos - grow[g];
+        const int s = gseg[g] + (p.chunk > 0 ? off / p.chunk : 0);
+        const int k = p.chunk > 0 ? off - (off / p.chunk) * p.chunk : off;
+        if (k < kInlineRows) p.desc[s].rows[k] = i;
+    };
+    {
+        int run_g = -1, run_next = 0;
+        for (int b = w0; b < w1; b += 32) {
+            const int i = b + lane;
+            int g = -1;
+            if (i < w1) {
+                const int a = ids[i];
+                if (a >= 0 && a < n) g = agroup[a];
+            }
+            const int g0 = __shfl_sync(0xffffffffu, g, 0);
+            const bool uniform = __all_sync(0xffffffffu, g == g0);
+            if (uniform && g0 >= 0) {
+                if (g0 != run_g) {
+                    if (lane == 0 && run_g >= 0) wh[run_g] = run_next;
+                    __syncwarp();
+                    run_g = g0;
+                    run_next = wh[g0];
+                    __syncwarp();
+                }
+                place_row(i, g0, run_next + lane);
+                run_next += 32;
+            } else if (!uniform) {
+                if (run_g >= 0) {
+                    if (lane == 0) wh[run_g] = run_next;
+                    run_g = -1;
+                }
+                __syncwarp();
+                const unsigned peers = __match_any_sync(0xffffffffu, g);
+                const int base_pos = g >= 0 ? wh[g] : 0;
+                __syncwarp();
+                if (g >= 0) {
+                    place_row(i, g, base_pos + __popc(peers & ((1u << lane) - 1u)));
+                    if (lane == __ffs(peers) - 1) wh[g] = base_pos + __popc(peers);
+                }
+                __syncwarp();
+            }
         }
-        const unsigned peers = __match_any_sync(0xffffffffu, g);
-        const int base_pos = g >= 0 ? wh[g] : 0;
-        __syncwarp();
-        if (g >= 0) {
-            const int pos = base_pos + __popc(peers & ((1u << lane) - 1u));
-            p.sorted[pos] = i;
-            if (lane == __ffs(peers) - 1) wh[g] = base_pos + __popc(peers);
-            // first rows of every segment, inline in its descriptor
-            const int off = pos - grow[g];
-            const int s = gseg[g] + (p.chunk > 0 ? off / p.chunk : 0);
-            const int k = p.chunk > 0 ? off - (off / p.chunk) * p.chunk : off;
-            if (k < kInlineRows) p.desc[s].rows[k] = i;
-        }
-        __syncwarp();
     }
 
     // Phase 6: counters.
@@ -355,6 +450,7 @@ cudaError_t launch_prepare(const int32_t *ids, int32_t M, int32_t n, int32_t chu
     p.off_groups = place(size_t(3 * gcap + 2) * 4);
     p.off_hist = place(size_t(threads / 32) * gcap * 4);
     p.off_adapters = place(size_t(3) * n * 4);
+    p.off_bits = M <= 65536 ? place(size_t(2) * ((M + 31) / 32) * 4) : -1;
     p.off_ids = place(size_t(M) * 4);
 
     static DeviceOnce configured;
