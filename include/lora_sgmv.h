@@ -83,7 +83,7 @@ typedef int lora_status_t;
 #define LORA_BF16 1
 
 /* Path selection for lora_delta / lora_shrink / lora_expand. */
-#define LORA_PATH_AUTO 0      /* segments with >= tc_min_rows rows use tensor cores (bf16) */
+#define LORA_PATH_AUTO 0      /* groups with >= tc_min_rows rows use tensor cores (bf16) */
 #define LORA_PATH_CUDA_CORE 1 /* every segment on CUDA-core dot products */
 #define LORA_PATH_TENSOR 2    /* every segment on tcgen05 tensor cores (bf16 only) */
 
@@ -97,12 +97,15 @@ typedef int lora_status_t;
 #define LORA_COUNT_SEGS 0       /* number of segments S */
 #define LORA_COUNT_ACTIVE 1     /* rows with a valid adapter */
 #define LORA_COUNT_INVALID 2    /* rows whose id is outside [-1, n_adapters) */
-#define LORA_COUNT_SMALL_SEGS 3 /* segments with fewer than tc_min_rows rows */
-#define LORA_COUNT_TC_SEGS 4    /* segments with at least tc_min_rows rows */
+#define LORA_COUNT_SMALL_SEGS 3 /* segments of groups with fewer than tc_min_rows rows */
+#define LORA_COUNT_TC_SEGS 4    /* segments of groups with at least tc_min_rows rows */
 #define LORA_COUNT_TC_ROWS 5    /* rows inside those segments */
 #define LORA_COUNT_DEVERR 6     /* bit set of LORA_DEVERR_* raised by later calls */
 #define LORA_COUNT_GROUPS 7     /* distinct adapters in the batch */
 #define LORA_NUM_COUNTS 8
+
+/* Bit of a descriptor's segment-index field: the segment is in tc_segs. */
+#define LORA_DESC_TC_FLAG 0x40000000
 
 #define LORA_DEVERR_RANK 1 /* an adapter's rank was outside [0, r_max] */
 #define LORA_DEVERR_WAIT 2 /* a bounded device wait gave up (result incomplete) */
@@ -119,15 +122,17 @@ typedef int lora_status_t;
  *   seg_lens[max_segs]      rows in segment s (> 0)
  *   weight_indices[max_segs] adapter slot of segment s
  *   seg_records[max_segs][32] per segment s a 128-byte descriptor
- *                             {start, len, adapter, s, rows[28]}: rows
- *                             holds the segment's first min(len, 28)
- *                             token rows; entries s >= num_segs have
- *                             len 0
+ *                             {start, len, adapter, s | flag, rows[28]}:
+ *                             flag is LORA_DESC_TC_FLAG when the segment
+ *                             is in tc_segs; rows holds the segment's
+ *                             first min(len, 28) token rows; entries
+ *                             s >= num_segs have len 0
  *   small_segs[max_segs][4]   records {start, len, adapter, s} of the
- *                             segments with < tc_min_rows rows, in
- *                             segment order
- *   tc_segs[max_segs][4]      records of the segments with >= tc_min_rows
- *                             rows, in segment order
+ *                             segments whose adapter group has fewer than
+ *                             tc_min_rows rows, in segment order
+ *   tc_segs[max_segs][4]      records of the segments whose adapter group
+ *                             has at least tc_min_rows rows (all chunks of
+ *                             such a group), in segment order
  *   tc_indptr[max_segs+1]   prefix sum of rows over tc_segs
  *   counts[LORA_NUM_COUNTS] see LORA_COUNT_*
  * Host fields describe the batch the metadata was built for.
@@ -178,10 +183,12 @@ size_t lora_workspace_size(int32_t M, int32_t n_adapters, int32_t chunk_size);
  *              ("III.Punica: Multi-Tenant LoRA Serving", section 代码:
  *              the regrouped token stream is cut into fixed-size chunks,
  *              each a logical segment with its own adapter).
- * tc_min_rows  segments with at least this many rows go to the tensor-core
- *              kernel under LORA_PATH_AUTO ("vLLM-Ascend LoRA" article,
- *              section 4.1: blocks below a row threshold use vector dot
- *              products); <= 0 selects the library default.
+ * tc_min_rows  the segments of adapter groups with at least this many rows
+ *              go to the tensor-core kernel under LORA_PATH_AUTO
+ *              ("vLLM-Ascend LoRA" article, section 4.1: blocks below a row
+ *              threshold use vector dot products; with chunking, every chunk
+ *              of a long group counts as part of its group); <= 0 selects
+ *              the library default.
  * workspace    device buffer of >= lora_workspace_size(M, n_adapters,
  *              chunk_size) bytes, 256-byte aligned; owned by the caller and
  *              referenced by *batch until the batch is no longer used.

@@ -250,11 +250,11 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
     __syncthreads();
     const int S = segs_run, ACT = rows_run;
 
-    // Phase 4: segments, records and the tensor-core split.
+    // Phase 4: segments, records and the tensor-core split (by group rows).
     int n_small = 0, n_tc = 0, tc_rows = 0;
     for (int base = 0; base < S; base += nthr) {
         const int s = base + tid;
-        int seg_start = 0, seg_len = 0, adapter = 0;
+        int seg_start = 0, seg_len = 0, adapter = 0, grp_len = 0;
         if (s < S) {
             int lo = 0, hi = G - 1;
             while (lo < hi) {
@@ -266,6 +266,7 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
             const int start = grow[g], len = grow[g + 1] - start;
             seg_start = start;
             seg_len = len;
+            grp_len = len;
             if (p.chunk > 0) {
                 seg_start = start + c * p.chunk;
                 seg_len = min(p.chunk, len - c * p.chunk);
@@ -274,9 +275,14 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
             p.indptr[s] = seg_start;
             p.lens[s] = seg_len;
             p.widx[s] = adapter;
-            *reinterpret_cast<int4 *>(&p.desc[s]) = make_int4(seg_start, seg_len, adapter, s);
         }
-        const int is_tc = (s < S && seg_len >= p.tc_min) ? 1 : 0;
+        // The split follows the adapter group's rows: the chunks of a long
+        // group stay one dense contraction (and the tensor-core kernel joins
+        // consecutive chunks of one group into one tile).
+        const int is_tc = (s < S && grp_len >= p.tc_min) ? 1 : 0;
+        if (s < S)
+            *reinterpret_cast<int4 *>(&p.desc[s]) =
+                make_int4(seg_start, seg_len, adapter, s | (is_tc ? LORA_DESC_TC_FLAG : 0));
         const int is_small = (s < S && !is_tc) ? 1 : 0;
         int t1, t2, t3;
         const int es = block_excl_scan(is_small, &t1, scan_ws);

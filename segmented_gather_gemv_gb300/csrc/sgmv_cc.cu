@@ -134,9 +134,9 @@ __global__ void __launch_bounds__(kCcThreads, 1)
         const int start = desc_s[0], len = desc_s[1], a = desc_s[2];
         if (len == 0) break;  // descriptors are compacted: the list ends here
         const int r = p.ranks ? p.ranks[a] : p.r_max;
-        // Long segments belong to the tensor-core kernel when it can take
-        // their rank.
-        if (len < p.min_len || (len >= p.max_len && (!p.split_tc || tc_rank_ok(r)))) continue;
+        // Segments of long adapter groups (flagged by prepare) belong to the
+        // tensor-core kernel when it can take their rank.
+        if (len < p.min_len || (p.split_tc && (desc_s[3] & LORA_DESC_TC_FLAG) && tc_rank_ok(r))) continue;
         if (r == 0 && MODE != kShrink) continue;  // rank 0: nothing to add
         if (r < 0 || r > p.r_max) {
             if (q == 0 && tid == 0) raise_deverr(p.counts, LORA_DEVERR_RANK);

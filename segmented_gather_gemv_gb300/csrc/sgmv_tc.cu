@@ -52,13 +52,12 @@
 // y is stored with st.global, four 128-byte row pieces per instruction: TMA
 // stores mixed with such stores in one CTA stalled the CTA's loads.
 //
-// Warp roles (416 threads): warps 0-3 loaders (lane 0 of warps 0 and 1 issue
+// Warp roles (672 threads): warps 0-3 loaders (lane 0 of warps 0 and 1 issue
 // the boxes of atoms 0 and 1; warps 2-3 the cp.async copies), warp 4 MMA
-// issuer (one thread) and TMEM owner, warps 5..12 epilogue.  Epilogue warp w
-// owns TMEM lanes 32 (w % 4) .. +31 (tile rows) and one half of the columns
-// of every n-tile; four of them also build H.  Without tensor maps (or for
-// gathered tiles when they are missing) every loader thread copies by
-// cp.async.
+// issuer (one thread) and TMEM owner, warps 5..20 epilogue.  Epilogue warp w
+// owns TMEM lanes 32 (w % 4) .. +31 (tile rows) and one quarter of the
+// columns of every n-tile; four of them also build H.  Without tensor maps
+// every loader thread copies by cp.async.
 #include <cuda.h>
 #include <cstring>
 
@@ -69,8 +68,10 @@ namespace lora {
 constexpr int kLoaderWarps = 4;                      // warps 0-3
 constexpr int kLoaderThreads = kLoaderWarps * 32;
 constexpr int kMmaWarp = 4;
-constexpr int kEpiWarp0 = 5;                         // warps 5..12
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarp0 = 5;                         // warps 5..20
+constexpr int kEpiWarps = 16;                        // 4 per TMEM lane quadrant
+constexpr int kEpiCols = 128 * 4 / kEpiWarps;        // columns of an n-tile per epilogue warp
+constexpr int kEpiChunks = kEpiCols / 8;             // 16-byte chunks of a row per epilogue warp
 constexpr int kTcThreads = (kEpiWarp0 + kEpiWarps) * 32;
 constexpr int kBM = 128;        // tile rows (MMA M)
 constexpr int kBK = 128;        // shrink K block: two 64-element (128-byte) swizzle atoms
@@ -376,7 +377,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < kMaxNS; ++s) {
             mbar_init(&full[s], kLoaderThreads + 2);  // + the two TMA issuers' expect_tx
-            mbar_init(&empty[s], kEpiWarps);  // 8 epilogue warps, or the MMA thread (7 arrivals + commit)
+            mbar_init(&empty[s], kEpiWarps);  // the epilogue warps, or the MMA thread (kEpiWarps - 1 arrivals + commit)
         }
         mbar_init(d1f, 1);
         mbar_init(hr, 4);
@@ -779,7 +780,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ------------------------------------------------------------ epilogue
         const int ew = warp - kEpiWarp0;     // 0..7
         const int q4 = warp & 3;             // TMEM lane quadrant
-        const int chalf = ew >> 2;           // which 64 columns of an n-tile
+        const int chalf = ew >> 2;           // which kEpiCols columns of an n-tile
         const int row = q4 * 32 + lane;      // tile row owned by this thread
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         unsigned char *H = smem + kOffH;
@@ -847,10 +848,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (!wait_warp(&tf[sd], (ts / kST) & 1, ok, abort)) goto role_done;
                 if (!wait_warp(&full[s], (job / NS) & 1, ok, abort)) goto role_done;
                 tc_fence_after();
-                uint32_t v[4][16];
-                const uint32_t ta = tmem + 128 + 128 * sd + lane_off + 64 * chalf;
+                uint32_t v[kEpiCols / 16][16];
+                const uint32_t ta = tmem + 128 + 128 * sd + lane_off + kEpiCols * chalf;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) tmem_ld16(ta + 16 * q, v[q]);
+                for (int q = 0; q < kEpiCols / 16; ++q) tmem_ld16(ta + 16 * q, v[q]);
                 tmem_wait_ld();
                 // the TMEM buffer is free as soon as it is read
                 tc_fence_before();
@@ -859,8 +860,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 unsigned char *ys = smem + s * stage_bytes;
                 if (live) {
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        uint4 *pq4 = reinterpret_cast<uint4 *>(ys + schunk(xatom, row, 8 * chalf + q));
+                    for (int q = 0; q < kEpiChunks; ++q) {
+                        uint4 *pq4 = reinterpret_cast<uint4 *>(ys + schunk(xatom, row, kEpiChunks * chalf + q));
                         uint4 yv = *pq4;
                         uint32_t *yw32 = reinterpret_cast<uint32_t *>(&yv);
 #pragma unroll
@@ -876,19 +877,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
                 __syncwarp();
-                // store the warp's live rows: 4 rows x 128 bytes per instruction
-                // (st.global: TMA stores mixed with these in one CTA stalled its loads)
+                // store the warp's live rows: 32 / kEpiChunks row pieces of
+                // kEpiCols columns per instruction (st.global: TMA stores mixed
+                // with these in one CTA stalled its loads)
                 {
-                    const int cq = lane & 7, col = (8 * chalf + cq) * 8;
+                    const int cq = lane % kEpiChunks, col = (kEpiChunks * chalf + cq) * 8;
                     __nv_bfloat16 *ydst = yw + S.y_col + c0 + col;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int rl = 4 * k + (lane >> 3);
+                    for (int k = 0; k < kEpiChunks; ++k) {
+                        const int rl = (32 / kEpiChunks) * k + lane / kEpiChunks;
                         const int tok = __shfl_sync(0xffffffffu, my_tok, rl);
                         const bool lv = __shfl_sync(0xffffffffu, live, rl);
                         if (lv && col < nc)
                             *reinterpret_cast<uint4 *>(ydst + (int64_t)tok * p.ldy) =
-                                *reinterpret_cast<const uint4 *>(ys + schunk(xatom, q4 * 32 + rl, 8 * chalf + cq));
+                                *reinterpret_cast<const uint4 *>(ys + schunk(xatom, q4 * 32 + rl, kEpiChunks * chalf + cq));
                     }
                 }
                 __syncwarp();

@@ -37,22 +37,29 @@ def _check_prepare(B, ids_np, n, chunk, tc_min=0):
     assert got["num_invalid"] == ref["num_invalid"]
     for k in ("sorted_token_ids", "seg_indptr", "seg_lens", "weight_indices"):
         assert np.array_equal(got[k].numpy(), ref[k]), k
-    # path split: every segment in exactly one list, by its length
+    # path split: every segment in exactly one list, by its adapter group's rows
     thr = tc_min if tc_min > 0 else batch.raw.tc_min_rows
     lens = ref["seg_lens"]
+    ids_a = np.asarray(ids_np, np.int64)
+    valid = (ids_a >= 0) & (ids_a < n)
+    group_rows = np.bincount(ids_a[valid], minlength=n)
+    to_tc = group_rows[ref["weight_indices"]] >= thr
     recs = np.stack([ref["seg_indptr"][:-1], lens, ref["weight_indices"],
                      np.arange(len(lens))], axis=1).astype(np.int32).reshape(-1, 4)
     desc = got["seg_records"].numpy()
     S = len(lens)
-    assert np.array_equal(desc[:S, :4], recs)
+    flag = 0x40000000
+    assert np.array_equal(desc[:S, :3], recs[:, :3])
+    assert np.array_equal(desc[:S, 3] & ~flag, recs[:, 3])
+    assert np.array_equal((desc[:S, 3] & flag) != 0, to_tc)
     assert np.all(desc[S:, 1] == 0), "descriptors past the last segment must have len 0"
     for s_ in range(S):
         k = min(int(lens[s_]), 28)
         st = int(ref["seg_indptr"][s_])
         assert np.array_equal(desc[s_, 4:4 + k], ref["sorted_token_ids"][st:st + k])
-    assert np.array_equal(got["small_segs"].numpy().reshape(-1, 4), recs[lens < thr])
-    assert np.array_equal(got["tc_segs"].numpy().reshape(-1, 4), recs[lens >= thr])
-    big = lens[lens >= thr]
+    assert np.array_equal(got["small_segs"].numpy().reshape(-1, 4), recs[~to_tc])
+    assert np.array_equal(got["tc_segs"].numpy().reshape(-1, 4), recs[to_tc])
+    big = lens[to_tc]
     assert np.array_equal(got["tc_indptr"].numpy(), np.concatenate([[0], np.cumsum(big)]).astype(np.int32))
     assert got["device_error"] == 0
     return batch
