@@ -395,7 +395,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int nseg = min(p.counts[p.tc_count_index], p.max_list);
         const int Mrows = nseg > 0 ? p.counts[p.tc_rows_index] : 0;
         const int G = gridDim.x, b = blockIdx.x;
-        const int r0 = (int)((int64_t)Mrows * b / G), r1 = (int)((int64_t)Mrows * (b + 1) / G);
+        // When two pieces of the largest rank cannot share a tile (their rank
+        // columns exceed K), a share end moves to a segment boundary within
+        // half a share, so that no CTA pays a second pass over its K blocks
+        // and n-tiles.  Both neighbours compute the same end.
+        const bool snap = 2 * min(p.r_max, kTcMaxRank) > kTcMaxRank && nseg > 1;
+        const int half = (int)(Mrows / (2 * (int64_t)G));
+        auto share_end = [&](int e) {
+            if (!snap || e <= 0 || e >= Mrows) return e;
+            const int i = warp_seg_of(p.tc_ptr, nseg, e, lane);
+            const int lo = p.tc_ptr[i], hi = p.tc_ptr[i + 1];
+            if (e - lo <= half) return lo;
+            if (hi - e <= half) return hi;
+            return e;
+        };
+        const int r0 = share_end((int)((int64_t)Mrows * b / G));
+        const int r1 = max(r0, share_end((int)((int64_t)Mrows * (b + 1) / G)));
         const int i0 = r0 < r1 ? warp_seg_of(p.tc_ptr, nseg, r0, lane) : 0;
         if (lane == 0) {
             range[0] = r0;
