@@ -395,18 +395,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int nseg = min(p.counts[p.tc_count_index], p.max_list);
         const int Mrows = nseg > 0 ? p.counts[p.tc_rows_index] : 0;
         const int G = gridDim.x, b = blockIdx.x;
-        // When two pieces of the largest rank cannot share a tile (their rank
-        // columns exceed K), a share end moves to a segment boundary within
-        // half a share, so that no CTA pays a second pass over its K blocks
-        // and n-tiles.  Both neighbours compute the same end.
-        const bool snap = 2 * min(p.r_max, kTcMaxRank) > kTcMaxRank && nseg > 1;
+        // A share end moves to a boundary between two adapters when one lies
+        // within half a share: a tile of one adapter needs no row split by a
+        // piece boundary (its rows move by TMA boxes alone) and no second
+        // pass when two ranks do not fit one tile.  Chunks of one adapter do
+        // not count as boundaries.  Both neighbours compute the same end.
         const int half = (int)(Mrows / (2 * (int64_t)G));
+        auto adapter_of = [&](int i) { return p.tc_adapter[(int64_t)i * p.tc_rec_stride]; };
         auto share_end = [&](int e) {
-            if (!snap || e <= 0 || e >= Mrows) return e;
+            if (nseg < 2 || e <= 0 || e >= Mrows) return e;
             const int i = warp_seg_of(p.tc_ptr, nseg, e, lane);
             const int lo = p.tc_ptr[i], hi = p.tc_ptr[i + 1];
-            if (e - lo <= half) return lo;
-            if (hi - e <= half) return hi;
+            const int a = adapter_of(i);
+            if (e - lo <= half && i > 0 && adapter_of(i - 1) != a) return lo;
+            if (hi - e <= half && i + 1 < nseg && adapter_of(i + 1) != a) return hi;
             return e;
         };
         const int r0 = share_end((int)((int64_t)Mrows * b / G));
