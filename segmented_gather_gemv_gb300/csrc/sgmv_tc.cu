@@ -91,8 +91,9 @@ constexpr int kTcMaxRank = 32;  // ranks above this use the CUDA-core kernel
 struct TcMaps {
     CUtensorMap x64, x32, x8;
     CUtensorMap y64[LORA_MAX_SLICES], y32[LORA_MAX_SLICES], y8[LORA_MAX_SLICES];
-    CUtensorMap a8, b[LORA_MAX_SLICES];
+    CUtensorMap a8, a16, a32, b[LORA_MAX_SLICES];
     int32_t use, use_ab, r_pad;  // r_pad: first rank index past every adapter's rank, a multiple of 8
+    int32_t a_box_max;           // largest rank box encoded: 8, 16 or 32
 };
 
 
@@ -376,7 +377,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (tid == 0) {
         for (int s = 0; s < kMaxNS; ++s) {
-            mbar_init(&full[s], kLoaderThreads + 2);  // + the two TMA issuers' expect_tx
+            // TMA path: the two issuers' expect_tx and the 64 helper threads;
+            // cp.async path: every loader thread and the two issuers
+            mbar_init(&full[s], m.use_ab ? 2 + 64 : kLoaderThreads + 2);
             mbar_init(&empty[s], kEpiWarps);  // the epilogue warps, or the MMA thread (kEpiWarps - 1 arrivals + commit)
         }
         mbar_init(d1f, 1);
@@ -543,40 +546,120 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if ((mask8 >> g) & 1) covered += min(8, t.n - 8 * g);
                 const int nu = t.n - covered;  // rows moved by cp.async
                 if (warp < 2 && lane == 0) {
-                    const uint32_t stand_in = kLoaderThreads - 64;
+                    // This atom's copies of the tile, resolved once: up to kCmds
+                    // boxes (row boxes first, then the stacked A block in rank
+                    // boxes of 32/16/8) with their shared-memory offset, map
+                    // code and coordinates; the job loop only adds the column.
+                    constexpr int kCmds = 6;
+                    uint32_t c_off[kCmds];
+                    int c_code[kCmds], c_r[kCmds], c_a[kCmds];
+                    int nrow = 0, ncmd = 0;
+                    bool fast = nbox <= kCmds;
+#pragma unroll
+                    for (int q = 0; q < kCmds; ++q) {
+                        c_off[q] = 0;
+                        c_code[q] = 0;
+                        c_r[q] = 0;
+                        c_a[q] = 0;
+                        if (q < nbox) {
+                            const uint2 bx = lbox[q];
+                            c_off[q] = (uint32_t)(hq * xatom + (int)(bx.x & 255) * 128);
+                            c_code[q] = 2 - (int)(bx.x >> 8);  // 0: 64 rows, 1: 32, 2: 8
+                            c_r[q] = (int)bx.y;
+                        }
+                    }
+                    nrow = ncmd = fast ? nbox : 0;
+                    const uint32_t abase_off = (uint32_t)(xbytes + hq * aatom);
+                    for (int u = 0; fast && u < t.np; ++u) {
+                        const int rk = sel(t.rk, u), ko = sel(t.kofs, u), au = sel(t.a, u);
+                        for (int j = 0; fast && j < rk;) {
+                            const int w = (rk - j >= 32 && m.a_box_max >= 32) ? 32 : (rk - j >= 16 && m.a_box_max >= 16) ? 16 : 8;
+                            if (ncmd == kCmds) {
+                                fast = false;
+                                break;
+                            }
+#pragma unroll
+                            for (int q = 0; q < kCmds; ++q)
+                                if (q == ncmd) {
+                                    c_off[q] = abase_off + (uint32_t)(ko + j) * 128;
+                                    c_code[q] = w == 32 ? 5 : w == 16 ? 4 : 3;
+                                    c_r[q] = j;
+                                    c_a[q] = au;
+                                }
+                            ++ncmd;
+                            j += w;
+                        }
+                    }
+                    for (int j = t.K; fast && j < K16; j += 8) {
+                        if (ncmd == kCmds) {
+                            fast = false;
+                            break;
+                        }
+#pragma unroll
+                        for (int q = 0; q < kCmds; ++q)
+                            if (q == ncmd) {
+                                c_off[q] = abase_off + (uint32_t)j * 128;
+                                c_code[q] = 3;
+                                c_r[q] = m.r_pad;
+                                c_a[q] = 0;
+                            }
+                        ++ncmd;
+                    }
+                    const uint32_t x_tx = box_bytes + (uint32_t)(K16 / 8) * 1024;
                     for (int jb = 0; jb < njobs; ++jb) {
                         if (!wait1(&empty[s], ph ^ 1, ok, abort)) goto role_done;
                         unsigned char *st = smem + s * stage_bytes;
                         if (jb < nkb) {
                             const int kb = jb + kb_rot < nkb ? jb + kb_rot : jb + kb_rot - nkb;
                             const int col = kb * kBK + 64 * hq;
-                            mbar_arrive_expect_tx(&full[s], box_bytes + (uint32_t)(K16 / 8) * 1024);
-                            if (warp == 0) mbar_arrive_n(&full[s], stand_in);
-                            for (int e = 0; e < nbox; ++e) {
-                                const uint2 bx = lbox[e];
-                                const int code = bx.x >> 8, i = bx.x & 255;
-                                tma_load_2d(st + hq * xatom + i * 128, code == 2 ? &m.x64 : code == 1 ? &m.x32 : &m.x8, col,
-                                            (int)bx.y, &full[s]);
+                            mbar_arrive_expect_tx(&full[s], x_tx);
+                            if (fast) {
+#pragma unroll
+                                for (int q = 0; q < kCmds; ++q) {
+                                    if (q >= ncmd) break;
+                                    const int cd = c_code[q];
+                                    if (cd < 3)
+                                        tma_load_2d(st + c_off[q], cd == 0 ? &m.x64 : cd == 1 ? &m.x32 : &m.x8, col, c_r[q], &full[s]);
+                                    else
+                                        tma_load_3d(st + c_off[q], cd == 5 ? &m.a32 : cd == 4 ? &m.a16 : &m.a8, col, c_r[q], c_a[q],
+                                                    &full[s]);
+                                }
+                            } else {
+                                for (int e = 0; e < nbox; ++e) {
+                                    const uint2 bx = lbox[e];
+                                    const int code = bx.x >> 8, i = bx.x & 255;
+                                    tma_load_2d(st + hq * xatom + i * 128, code == 2 ? &m.x64 : code == 1 ? &m.x32 : &m.x8, col,
+                                                (int)bx.y, &full[s]);
+                                }
+                                // the stacked A block of this atom: 8 rank rows per box
+                                unsigned char *abuf = st + xbytes + hq * aatom;
+                                for (int u = 0; u < t.np; ++u)
+                                    for (int j = 0; j < sel(t.rk, u); j += 8)
+                                        tma_load_3d(abuf + (sel(t.kofs, u) + j) * 128, &m.a8, col, j, sel(t.a, u), &full[s]);
+                                for (int j = t.K; j < K16; j += 8) tma_load_3d(abuf + j * 128, &m.a8, col, m.r_pad, 0, &full[s]);
                             }
-                            // the stacked A block of this atom: 8 rank rows per box
-                            unsigned char *abuf = st + xbytes + hq * aatom;
-                            for (int u = 0; u < t.np; ++u)
-                                for (int j = 0; j < sel(t.rk, u); j += 8)
-                                    tma_load_3d(abuf + (sel(t.kofs, u) + j) * 128, &m.a8, col, j, sel(t.a, u), &full[s]);
-                            for (int j = t.K; j < K16; j += 8) tma_load_3d(abuf + j * 128, &m.a8, col, m.r_pad, 0, &full[s]);
                         } else {
                             const int nti = jb - nkb, nt = nti + nt_rot < n_nt ? nti + nt_rot : nti + nt_rot - n_nt;
                             int sl, c0, nc;
                             ntile_cols(p, nt, sl, c0, nc);
                             const int col = c0 + 64 * hq;
                             mbar_arrive_expect_tx(&full[s], box_bytes);
-                            if (warp == 0) mbar_arrive_n(&full[s], stand_in);
-                            for (int e = 0; e < nbox; ++e) {
-                                const uint2 bx = lbox[e];
-                                const int code = bx.x >> 8, i = bx.x & 255;
-                                tma_load_2d(st + hq * xatom + i * 128,
-                                            code == 2 ? &m.y64[sl] : code == 1 ? &m.y32[sl] : &m.y8[sl], col, (int)bx.y,
-                                            &full[s]);
+                            if (fast) {
+#pragma unroll
+                                for (int q = 0; q < kCmds; ++q) {
+                                    if (q >= nrow) break;
+                                    const int cd = c_code[q];
+                                    tma_load_2d(st + c_off[q], cd == 0 ? &m.y64[sl] : cd == 1 ? &m.y32[sl] : &m.y8[sl], col, c_r[q],
+                                                &full[s]);
+                                }
+                            } else {
+                                for (int e = 0; e < nbox; ++e) {
+                                    const uint2 bx = lbox[e];
+                                    const int code = bx.x >> 8, i = bx.x & 255;
+                                    tma_load_2d(st + hq * xatom + i * 128,
+                                                code == 2 ? &m.y64[sl] : code == 1 ? &m.y32[sl] : &m.y8[sl], col, (int)bx.y,
+                                                &full[s]);
+                                }
                             }
                         }
                         if (++s == NS) {
@@ -1006,6 +1089,17 @@ cudaError_t launch_tc(const DeltaArgs &p, int mode, int sms, cudaStream_t stream
         use_ab = fn(&maps.a8, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p.A), dims, strides, box, elem,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        // wider rank boxes, one TMA copy per 16 or 32 rank rows of a piece
+        maps.a_box_max = 8;
+        CUtensorMap *wide[2] = {&maps.a16, &maps.a32};
+        for (int w = 0; use_ab && w < 2 && p.r_max >= 16 << w; ++w) {
+            const cuuint32_t boxw[3] = {64, (cuuint32_t)(16 << w), 1};
+            if (fn(wide[w], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p.A), dims, strides, boxw, elem,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                break;
+            maps.a_box_max = 16 << w;
+        }
     }
     for (int t = 0; use_ab && t < p.n_slices; ++t) {
         const SliceDesc &S = p.slices[t];
