@@ -52,12 +52,14 @@
 // y is stored with st.global, four 128-byte row pieces per instruction: TMA
 // stores mixed with such stores in one CTA stalled the CTA's loads.
 //
-// Warp roles (672 threads): warps 0-3 loaders (lane 0 of warps 0 and 1 issue
-// the boxes of atoms 0 and 1; warps 2-3 the cp.async copies), warp 4 MMA
-// issuer (one thread) and TMEM owner, warps 5..20 epilogue.  Epilogue warp w
-// owns TMEM lanes 32 (w % 4) .. +31 (tile rows) and one quarter of the
-// columns of every n-tile; four of them also build H.  Without tensor maps
-// every loader thread copies by cp.async.
+// Warp roles (672 threads): warps 0, 1, 2 and 4 loaders (lane 0 of warps 0
+// and 1 issue the boxes of atoms 0 and 1; warps 2 and 4 the cp.async
+// copies), warp 3 MMA issuer (one thread) and TMEM owner, warps 5..20
+// epilogue.  The MMA thread shares a scheduler with neither TMA issuer: next
+// to one, its MMAs slowed that issuer's boxes.  Epilogue warp w owns TMEM
+// lanes 32 (w % 4) .. +31 (tile rows) and one quarter of the columns of every
+// n-tile; four of them also build H.  Without tensor maps every loader thread
+// copies by cp.async.
 #include <cuda.h>
 #include <cstring>
 
@@ -65,9 +67,10 @@
 
 namespace lora {
 
-constexpr int kLoaderWarps = 4;                      // warps 0-3
+constexpr int kLoaderWarps = 4;                      // warps 0, 1, 2 and 4
 constexpr int kLoaderThreads = kLoaderWarps * 32;
-constexpr int kMmaWarp = 4;
+constexpr int kMmaWarp = 3;
+constexpr int kLoaderWarp3 = 4;                      // the fourth loader warp
 constexpr int kEpiWarp0 = 5;                         // warps 5..20
 constexpr int kEpiWarps = 16;                        // 4 per TMEM lane quadrant
 constexpr int kEpiCols = 128 * 4 / kEpiWarps;        // columns of an n-tile per epilogue warp
@@ -118,8 +121,12 @@ constexpr int kOffLdr = kOffMisc + 64;               // loader tables: row token
 // [2][16] ints, TMA boxes [2][16] uint2, then the helpers' row lists [2][128] int2
 constexpr int kLdrGtok = 4 * 32 * 4, kLdrBox = kLdrGtok + 2 * 16 * 4, kLdrRows = kLdrBox + 2 * 16 * 8;
 constexpr int kLdrBytes = kLdrRows + 2 * kBM * 8;
+// 16 x 16 bf16 identity, the B operand that adds a y stage into D2
+constexpr int kOffIdent = (kOffLdr + kLdrBytes + 127) & ~127;
+constexpr int kIdentBytes = 16 * 16 * 2;
 constexpr int kOverrun = (kBM - 8) * 128;            // MMA reads past the last stage
-constexpr int kTcSmemUsed = kOffLdr + kLdrBytes > kRingBytes + kOverrun ? kOffLdr + kLdrBytes : kRingBytes + kOverrun;
+constexpr int kTcSmemUsed =
+    kOffIdent + kIdentBytes > kRingBytes + kOverrun ? kOffIdent + kIdentBytes : kRingBytes + kOverrun;
 constexpr int kTcSmem = kTcSmemUsed + 1024;          // + alignment slack
 
 // ---------------------------------------------------------------------------
@@ -393,6 +400,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     griddep_launch_dependents();
     griddep_wait();
 
+    if (tid < 256) {
+        // identity I[n][k] = (n == k), K-major without swizzle: 8-column
+        // halves 256 bytes apart, 16 bytes per row
+        const int n = tid >> 4, k = tid & 15;
+        *reinterpret_cast<uint16_t *>(smem + kOffIdent + (k >> 3) * 256 + n * 16 + (k & 7) * 2) =
+            n == k ? (uint16_t)0x3F80 : (uint16_t)0;
+        fence_proxy_async_smem();
+    }
     if (warp == kMmaWarp) {
         // This CTA's row range: an equal share of the row space.
         const int nseg = min(p.counts[p.tc_count_index], p.max_list);
@@ -453,18 +468,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const __nv_bfloat16 *yg = static_cast<const __nv_bfloat16 *>(p.y);
     bool ok = true;
 
-    if (warp < kLoaderWarps) {
+    if (warp < kMmaWarp || warp == kLoaderWarp3) {
+        // loader warps 0, 1, 2 and 4 (warp 3 issues the MMAs, so that the
+        // MMA thread shares a scheduler with neither TMA issuer); lw numbers
+        // them 0-3
+        const int lw = warp == kLoaderWarp3 ? 3 : warp;
         // ------------------------------------------------------------ loaders
         // Thread lt copies chunk (lt & 15) of tile rows (lt >> 4) + 8q (row
         // group q) by cp.async where no TMA box covers them; lane 0 of warps
         // 0 and 1 issues the TMA boxes of atoms 0 and 1.  Per tile, each warp
         // writes its tables (row tokens; box list) to shared memory once, so
         // the per-stage loop only reads them.
-        const int lt = tid, c = lt & 15, i0 = lt >> 4;
-        const int hq = warp;  // the atom of an issuing warp (0 or 1)
-        int32_t *lrow = reinterpret_cast<int32_t *>(smem + kOffLdr) + 32 * warp;      // [slot]: token row
-        int32_t *lgt = reinterpret_cast<int32_t *>(smem + kOffLdr + kLdrGtok) + 16 * (warp & 1);  // [g]: token of row 8g
-        uint2 *lbox = reinterpret_cast<uint2 *>(smem + kOffLdr + kLdrBox) + 16 * (warp & 1);     // {row | height code << 8, token}
+        const int lt = lw * 32 + lane, c = lt & 15, i0 = lt >> 4;
+        const int hq = lw;  // the atom of an issuing warp (0 or 1)
+        int32_t *lrow = reinterpret_cast<int32_t *>(smem + kOffLdr) + 32 * lw;      // [slot]: token row
+        int32_t *lgt = reinterpret_cast<int32_t *>(smem + kOffLdr + kLdrGtok) + 16 * (lw & 1);  // [g]: token of row 8g
+        uint2 *lbox = reinterpret_cast<uint2 *>(smem + kOffLdr + kLdrBox) + 16 * (lw & 1);     // {row | height code << 8, token}
         const __nv_bfloat16 *xg = static_cast<const __nv_bfloat16 *>(p.x);
         const __nv_bfloat16 *Ag = static_cast<const __nv_bfloat16 *>(p.A);
         int s = 0;
@@ -476,10 +495,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tile_box_masks(p, m, t, lane, mask8, mask32, mask64);
             // this lane's slot: tile row (2 warp + (lane & 1)) + 8 (lane >> 1)
             {
-                const int i = 2 * warp + (lane & 1) + 8 * (lane >> 1);
+                const int i = 2 * lw + (lane & 1) + 8 * (lane >> 1);
                 __syncwarp();  // the previous tile's readers are done
                 lrow[lane] = i < t.n ? tile_token(p, t, i) : 0;
-                if (warp < 2 && lane < 16) lgt[lane] = 8 * lane < t.n ? tile_token(p, t, 8 * lane) : 0;
+                if (lw < 2 && lane < 16) lgt[lane] = 8 * lane < t.n ? tile_token(p, t, 8 * lane) : 0;
                 __syncwarp();
             }
             // cp.async rows of this thread: bit q = row i0 + 8q
@@ -487,7 +506,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int q = 0; q < kBM / 8; ++q) mine |= (i0 + 8 * q < t.n && !((mask8 >> q) & 1)) ? 1u << q : 0u;
             int nbox = 0;
-            if (warp < 2 && lane == 0) {
+            if (lw < 2 && lane == 0) {
                 for (int h = 0; h < 2; ++h) {
                     if ((mask64 >> h) & 1) {
                         lbox[nbox++] = make_uint2(64 * h | 2u << 8, lgt[8 * h]);
@@ -545,7 +564,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int g = 0; g < 16; ++g)
                     if ((mask8 >> g) & 1) covered += min(8, t.n - 8 * g);
                 const int nu = t.n - covered;  // rows moved by cp.async
-                if (warp < 2 && lane == 0) {
+                if (lw < 2 && lane == 0) {
                     // This atom's copies of the tile, resolved once: up to kCmds
                     // boxes (row boxes first, then the stacked A block in rank
                     // boxes of 32/16/8) with their shared-memory offset, map
@@ -667,9 +686,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             ph ^= 1;
                         }
                     }
-                } else if (warp >= 2) {
+                } else if (lw >= 2) {
                     // the uncovered rows: tile row and token row, in this warp's list
-                    int2 *ul = reinterpret_cast<int2 *>(smem + kOffLdr + kLdrRows) + kBM * (warp - 2);
+                    int2 *ul = reinterpret_cast<int2 *>(smem + kOffLdr + kLdrRows) + kBM * (lw - 2);
                     {
                         int cnt = 0;
                         __syncwarp();
@@ -710,11 +729,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             ntile_cols(p, nt, sl, c0, nc);
                             const SliceDesc &S = p.slices[sl];
                             const __nv_bfloat16 *yc = yg + S.y_col + c0;
-                            if (hc * 8 < nc)
-                                for (int e = hr0; e < nu; e += 4) {
-                                    const int2 ri = ul[e];
-                                    cp_async16(st + schunk(xatom, ri.x, hc), yc + (int64_t)ri.y * p.ldy + hc * 8, 16);
-                                }
+                            // chunks past the n-tile's last column are zero-filled: the
+                            // MMA adds the whole stage (times the identity) into D2
+                            for (int e = hr0; e < nu; e += 4) {
+                                const int2 ri = ul[e];
+                                const __nv_bfloat16 *yr = yc + (int64_t)ri.y * p.ldy;
+                                cp_async16(st + schunk(xatom, ri.x, hc), hc * 8 < nc ? yr + hc * 8 : yr, hc * 8 < nc ? 16 : 0);
+                            }
                             // the stacked B block: rows c0 .. c0+nc-1 of the slice (columns of no piece zero-filled)
                             const __nv_bfloat16 *Bb =
                                 static_cast<const __nv_bfloat16 *>(S.B) + (int64_t)hb_a * S.stride_adapter + hb_j;
@@ -743,7 +764,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 unsigned char *st = smem + s * stage_bytes;
                 const int k = kb * kBK + c * 8;
                 const bool kin = k < p.d_in;
-                if (warp < 2 && lane == 0) {
+                if (lw < 2 && lane == 0) {
                     // the expected bytes are announced before the boxes are issued
                     mbar_arrive_expect_tx(&full[s], box_bytes);
                     unsigned char *dst = st + hq * xatom;
@@ -785,7 +806,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const SliceDesc &S = p.slices[sl];
                 if (!wait_warp(&empty[s], ph ^ 1, ok, abort)) goto role_done;
                 unsigned char *st = smem + s * stage_bytes;
-                if (warp < 2 && lane == 0) {
+                if (lw < 2 && lane == 0) {
                     mbar_arrive_expect_tx(&full[s], box_bytes);
                     unsigned char *dst = st + hq * xatom;
                     const int col = c0 + 64 * hq;
@@ -804,11 +825,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         cp_async16(st + schunk(xatom, i0 + 8 * q, c), yc + (int64_t)lrow[2 * q + slot_hi] * p.ldy + c * 8, 16);
                     }
                 } else {
+                    // chunks past the n-tile's last column are zero-filled
                     const int nch = nc >> 3;
-                    for (int e = lt; e < t.n * nch; e += kLoaderThreads) {
-                        const int i = e / nch, cc = e % nch;
+                    for (int e = lt; e < t.n * 16; e += kLoaderThreads) {
+                        const int i = e >> 4, cc = e & 15;
                         if ((mask8 >> (i >> 3)) & 1) continue;
-                        cp_async16(st + schunk(xatom, i, cc), yc + (int64_t)tile_token(p, t, i) * p.ldy + cc * 8, 16);
+                        const __nv_bfloat16 *yr = yc + (int64_t)tile_token(p, t, i) * p.ldy;
+                        cp_async16(st + schunk(xatom, i, cc), cc < nch ? yr + cc * 8 : yr, cc < nch ? 16 : 0);
                     }
                 }
                 // the stacked B block: rows c0 .. c0+nc-1 of the slice, 8 rank
@@ -830,8 +853,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             uint32_t job = 0, ts = 0, tiles = 0;
-            const uint32_t id2 = idesc_bf16(kBM, kBN);
+            const uint32_t id2 = idesc_bf16(kBM, kBN), idi = idesc_bf16(kBM, 16);
             const uint32_t ring = smem_u32(smem), h_base = smem_u32(smem + kOffH);
+            const uint64_t ident = smem_desc(smem_u32(smem + kOffIdent), 256, 128, kLayoutNone);
             Tile t;
             while (walker.next(t)) {
                 if (t.K == 0) continue;
@@ -843,6 +867,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int s = job % NS;
                     if (!wait1(&full[s], (job / NS) & 1, ok, abort)) goto role_done;
                     tc_fence_after();
+                    fence_proxy_async_smem();  // rows the helpers wrote by cp.async
                     const uint32_t xa = ring + s * stage_bytes, aa = xa + xbytes;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
@@ -865,11 +890,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (!wait1(&full[s], (job / NS) & 1, ok, abort)) goto role_done;
                     if (!wait1(&te[sd], ((ts / kST) & 1) ^ 1, ok, abort)) goto role_done;
                     tc_fence_after();
-                    const uint32_t bb = ring + s * stage_bytes + xbytes;
+                    fence_proxy_async_smem();  // rows the helpers wrote by cp.async
+                    const uint32_t ya = ring + s * stage_bytes, bb = ya + xbytes;
                     const uint32_t d2 = tmem + 128 + 128 * sd;
+                    // D2 = y: columns 16 kk .. +15 take the y stage's K block kk
+                    // times the identity (exact: one product per column is y, the
+                    // others are zero), so the epilogue needs no y of its own
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        umma(d2 + 16 * kk, smem_desc(ya + (kk >> 2) * xatom + (kk & 3) * 32, 16, 1024, kLayoutSw128),
+                             ident, idi, 0);
+                    // D2 += H . B^T
                     for (int kc = 0; kc < n16; ++kc)
                         umma(d2, smem_desc(h_base + kc * 2 * kHChunk, kHChunk, 128, kLayoutNone),
-                             smem_desc(bb + kc * 2 * kBChunk, kBChunk, 128, kLayoutNone), id2, kc != 0);
+                             smem_desc(bb + kc * 2 * kBChunk, kBChunk, 128, kLayoutNone), id2, 1);
                     umma_commit(&tf[sd]);
                 }
                 umma_commit(he);
@@ -938,15 +972,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(hr);
             }
-            // ---- expand n-tiles: y += D2 (this warp: 32 rows x 64 columns)
+            // ---- expand n-tiles: y = D2 (this warp: 32 rows x kEpiCols columns)
+            // Per tile, once: the rows this lane stores (8 k + lane / kEpiChunks
+            // of the warp's quadrant) as offsets into y (-1: no row or rank 0),
+            // the stage offsets it reads them from (rows 8 apart: + 1024 k)
+            // and the offsets of its own row's chunks.
+            static_assert(kEpiChunks == 4, "store map: 4 chunks per row piece, 8 rows per instruction");
+            int64_t srow[kEpiChunks];
+#pragma unroll
+            for (int k = 0; k < kEpiChunks; ++k) {
+                const int rl = 8 * k + lane / kEpiChunks;
+                const int tok = __shfl_sync(0xffffffffu, my_tok, rl);
+                const bool lv = __shfl_sync(0xffffffffu, live, rl);
+                srow[k] = lv ? (int64_t)tok * p.ldy : -1;
+            }
+            const int ccol = kEpiChunks * chalf + lane % kEpiChunks;  // this lane's 16-byte chunk of a row
+            const int ld_off = schunk(xatom, q4 * 32 + lane / kEpiChunks, ccol);
+            int st_off[kEpiChunks];
+#pragma unroll
+            for (int q = 0; q < kEpiChunks; ++q) st_off[q] = schunk(xatom, row, kEpiChunks * chalf + q);
             for (int nti = 0; nti < n_nt; ++nti, ++job, ++ts) {
                 const int nt = nti + nt_rot < n_nt ? nti + nt_rot : nti + nt_rot - n_nt;
                 const int s = job % NS, sd = ts % kST;
                 int sl, c0, nc;
                 ntile_cols(p, nt, sl, c0, nc);
                 const SliceDesc &S = p.slices[sl];
+                // D2 holds y + delta (the MMA read this job's y stage before it
+                // committed tf)
                 if (!wait_warp(&tf[sd], (ts / kST) & 1, ok, abort)) goto role_done;
-                if (!wait_warp(&full[s], (job / NS) & 1, ok, abort)) goto role_done;
                 tc_fence_after();
                 uint32_t v[kEpiCols / 16][16];
                 const uint32_t ta = tmem + 128 + 128 * sd + lane_off + kEpiCols * chalf;
@@ -957,41 +1010,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&te[sd]);
+                // round once to bf16, into the stage in place of y (rows of the
+                // tile only: the stage holds cap rows per atom)
                 unsigned char *ys = smem + s * stage_bytes;
-                if (live) {
 #pragma unroll
-                    for (int q = 0; q < kEpiChunks; ++q) {
-                        uint4 *pq4 = reinterpret_cast<uint4 *>(ys + schunk(xatom, row, kEpiChunks * chalf + q));
-                        uint4 yv = *pq4;
-                        uint32_t *yw32 = reinterpret_cast<uint32_t *>(&yv);
+                for (int q = 0; q < kEpiChunks; ++q) {
+                    if (!live) break;
+                    uint32_t o[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const uint32_t a0 = v[q >> 1][(q & 1) * 8 + 2 * e];
-                            const uint32_t a1 = v[q >> 1][(q & 1) * 8 + 2 * e + 1];
-                            const float y0 = __uint_as_float(yw32[e] << 16) + __uint_as_float(a0);
-                            const float y1 = __uint_as_float(yw32[e] & 0xFFFF0000u) + __uint_as_float(a1);
-                            const __nv_bfloat162 o = __floats2bfloat162_rn(y0, y1);
-                            yw32[e] = *reinterpret_cast<const uint32_t *>(&o);
-                        }
-                        *pq4 = yv;
+                    for (int e = 0; e < 4; ++e) {
+                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[q >> 1][(q & 1) * 8 + 2 * e]),
+                                                                        __uint_as_float(v[q >> 1][(q & 1) * 8 + 2 * e + 1]));
+                        o[e] = *reinterpret_cast<const uint32_t *>(&h2);
                     }
+                    *reinterpret_cast<uint4 *>(ys + st_off[q]) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
                 __syncwarp();
-                // store the warp's live rows: 32 / kEpiChunks row pieces of
-                // kEpiCols columns per instruction (st.global: TMA stores mixed
-                // with these in one CTA stalled its loads)
-                {
-                    const int cq = lane % kEpiChunks, col = (kEpiChunks * chalf + cq) * 8;
-                    __nv_bfloat16 *ydst = yw + S.y_col + c0 + col;
+                // store the warp's live rows: 8 row pieces of kEpiCols columns
+                // per instruction (st.global: TMA stores mixed with these in
+                // one CTA stalled its loads)
+                if (ccol * 8 < nc) {
+                    __nv_bfloat16 *ydst = yw + S.y_col + c0 + ccol * 8;
 #pragma unroll
-                    for (int k = 0; k < kEpiChunks; ++k) {
-                        const int rl = (32 / kEpiChunks) * k + lane / kEpiChunks;
-                        const int tok = __shfl_sync(0xffffffffu, my_tok, rl);
-                        const bool lv = __shfl_sync(0xffffffffu, live, rl);
-                        if (lv && col < nc)
-                            *reinterpret_cast<uint4 *>(ydst + (int64_t)tok * p.ldy) =
-                                *reinterpret_cast<const uint4 *>(ys + schunk(xatom, q4 * 32 + rl, kEpiChunks * chalf + cq));
-                    }
+                    for (int k = 0; k < kEpiChunks; ++k)
+                        if (srow[k] >= 0)
+                            *reinterpret_cast<uint4 *>(ydst + srow[k]) = *reinterpret_cast<const uint4 *>(ys + ld_off + 1024 * k);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
@@ -1000,7 +1043,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     }
 role_done:
-    if (warp < kLoaderWarps) asm volatile("cp.async.wait_all;\n" ::: "memory");
+    if (warp < kMmaWarp || warp == kLoaderWarp3) asm volatile("cp.async.wait_all;\n" ::: "memory");
     if (warp == kMmaWarp && lane == 0) {
         // every MMA this CTA issued has completed before TMEM is released
         umma_commit(fin);
