@@ -199,6 +199,13 @@ size_t lora_workspace_size(int32_t M, int32_t n_adapters, int32_t chunk_size);
  * order (the Punica page's example: ids 2 2 2 5 5 1 1 give
  * seg_indptr = [0, 3, 5, 7]).  Rows with id -1 or an out-of-range id are
  * in no segment.
+ *
+ * Ordering: the kernel is launched with programmatic dependent launch and
+ * reads ids while the previous kernel in the stream may still be running
+ * (the workspace is written only after that kernel has completed).  ids
+ * must therefore be final before that previous kernel starts, which holds
+ * whenever ids come from a copy or from any kernel enqueued before it, and
+ * when that previous kernel is one of this library's (they never write ids).
  */
 lora_status_t lora_prepare_batch(const int32_t *ids, int32_t M, int32_t n_adapters,
                                  int32_t chunk_size, int32_t tc_min_rows,
@@ -271,7 +278,12 @@ lora_status_t lora_expand(const lora_batch_t *batch, int32_t dtype,
  * Fused delta: shrink, scale and expand in one pass; the M x r
  * intermediate stays in registers, shared memory or tensor memory and is
  * never written to global memory ("vLLM-Ascend LoRA" article, section 4.3).
- * Arguments as for lora_shrink and lora_expand.
+ * Arguments as for lora_shrink and lora_expand.  Each y element is read,
+ * y + delta is formed in fp32 and rounded to y's type once.
+ * Non-finite y: on the tensor-core path y enters the fp32 accumulator through
+ * an MMA with a 16 x 16 identity, so a NaN or infinity in y[i, n] turns the
+ * other outputs of row i in the same aligned 16-column group of the 128-column
+ * tile into NaN (0 * inf); finite y is added exactly.
  */
 lora_status_t lora_delta(const lora_batch_t *batch, int32_t dtype,
                          const void *x, int64_t ldx, int32_t d_in,

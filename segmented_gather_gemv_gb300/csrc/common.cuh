@@ -162,6 +162,9 @@ __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
 // Programmatic dependent launch: let the next grid in the stream start its
 // prologue early / wait until the previous grid has completed and its
 // memory is visible.  Both are no-ops when the launch did not opt in.
+// Every kernel of this library waits before it triggers, so a grid that
+// starts early finds every grid before its predecessor complete: the
+// predecessor itself is the only one still running.
 __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }

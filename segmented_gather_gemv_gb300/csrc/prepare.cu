@@ -80,10 +80,18 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
     __shared__ int scan_ws[33];
     __shared__ int s_invalid;
 
-    // Let the next kernel in the stream start its prologue; it waits for
-    // this grid's completion before it reads what this grid writes.
-    griddep_launch_dependents();
-    griddep_wait();
+    // Phases 1-3 read only the ids and write only shared memory; when every
+    // table of theirs is in shared memory they run before the wait on the
+    // previous grid, overlapping it (the previous grid of this library
+    // writes y, never ids, and everything before it has completed: see
+    // griddep_launch_dependents).  The next kernel may start once this grid
+    // has waited; it waits for this grid's completion before it reads what
+    // this grid writes.
+    const bool early = p.off_adapters >= 0 && p.off_groups >= 0;
+    if (!early) {
+        griddep_wait();
+        griddep_launch_dependents();
+    }
 
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
@@ -249,6 +257,11 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
     }
     __syncthreads();
     const int S = segs_run, ACT = rows_run;
+
+    if (early) {
+        griddep_wait();
+        griddep_launch_dependents();
+    }
 
     // Phase 4: segments, records and the tensor-core split (by group rows).
     int n_small = 0, n_tc = 0, tc_rows = 0;

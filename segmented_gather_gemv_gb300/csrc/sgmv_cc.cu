@@ -116,8 +116,8 @@ __global__ void __launch_bounds__(kCcThreads, 1)
     const uint32_t cid = cluster_id_x(), ncl = nclusters_x();
     const int RT = g.RT, HP = g.HP, SB = g.stage_bytes;
 
-    griddep_launch_dependents();
     griddep_wait();
+    griddep_launch_dependents();
 
     const int kv_total = p.d_in / V;
     const int kv0 = (int)((int64_t)kv_total * q / CL), kv1 = (int)((int64_t)kv_total * (q + 1) / CL);

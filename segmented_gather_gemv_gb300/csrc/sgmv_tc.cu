@@ -397,8 +397,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fence_mbar_init();
         *abort = 0;
     }
-    griddep_launch_dependents();
     griddep_wait();
+    griddep_launch_dependents();
 
     if (tid < 256) {
         // identity I[n][k] = (n == k), K-major without swizzle: 8-column
