@@ -41,7 +41,8 @@ struct PrepArgs {
     int32_t *whist;
     // shared-memory placement (byte offsets into dynamic shared memory, -1 = global)
     int32_t off_ids, off_adapters, off_groups, off_hist;
-    int32_t off_bits;  // first-appearance bitmap and its word prefix, or -1
+    int32_t off_bits;   // first-appearance bitmap and its word prefix, or -1
+    int32_t off_stage;  // shared-memory copies of every phase 4-5 output, or -1
 };
 
 // Block-wide exclusive scan of one value per thread.  `ws` is shared scratch
@@ -258,7 +259,28 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
     __syncthreads();
     const int S = segs_run, ACT = rows_run;
 
-    if (early) {
+    // Phases 4-5 write their outputs to shared memory too when they fit
+    // (staging), so that only the copy to global memory waits on the
+    // previous grid.
+    const bool stage = early && p.off_stage >= 0 && p.off_hist >= 0;
+    SegDesc *o_desc = p.desc;
+    int4 *o_small = p.small, *o_tc = p.tc;
+    int32_t *o_indptr = p.indptr, *o_lens = p.lens, *o_widx = p.widx, *o_tcptr = p.tcptr, *o_sorted = p.sorted;
+    if (stage) {
+        unsigned char *b = smem_raw + p.off_stage;
+        o_desc = reinterpret_cast<SegDesc *>(b);
+        b += size_t(p.max_segs) * sizeof(SegDesc);
+        o_small = reinterpret_cast<int4 *>(b);
+        b += size_t(p.max_segs) * 16;
+        o_tc = reinterpret_cast<int4 *>(b);
+        b += size_t(p.max_segs) * 16;
+        o_indptr = reinterpret_cast<int32_t *>(b);
+        o_lens = o_indptr + p.max_segs + 1;
+        o_widx = o_lens + p.max_segs;
+        o_tcptr = o_widx + p.max_segs;
+        o_sorted = o_tcptr + p.max_segs + 1;
+    }
+    if (early && !stage) {
         griddep_wait();
         griddep_launch_dependents();
     }
@@ -285,16 +307,16 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
                 seg_len = min(p.chunk, len - c * p.chunk);
             }
             adapter = gadapter[g];
-            p.indptr[s] = seg_start;
-            p.lens[s] = seg_len;
-            p.widx[s] = adapter;
+            o_indptr[s] = seg_start;
+            o_lens[s] = seg_len;
+            o_widx[s] = adapter;
         }
         // The split follows the adapter group's rows: the chunks of a long
         // group stay one dense contraction (and the tensor-core kernel joins
         // consecutive chunks of one group into one tile).
         const int is_tc = (s < S && grp_len >= p.tc_min) ? 1 : 0;
         if (s < S)
-            *reinterpret_cast<int4 *>(&p.desc[s]) =
+            *reinterpret_cast<int4 *>(&o_desc[s]) =
                 make_int4(seg_start, seg_len, adapter, s | (is_tc ? LORA_DESC_TC_FLAG : 0));
         const int is_small = (s < S && !is_tc) ? 1 : 0;
         int t1, t2, t3;
@@ -302,22 +324,22 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
         const int et = block_excl_scan(is_tc, &t2, scan_ws);
         const int er = block_excl_scan(is_tc ? seg_len : 0, &t3, scan_ws);
         const int4 rec = make_int4(seg_start, seg_len, adapter, s);
-        if (is_small) p.small[n_small + es] = rec;
+        if (is_small) o_small[n_small + es] = rec;
         if (is_tc) {
-            p.tc[n_tc + et] = rec;
-            p.tcptr[n_tc + et] = tc_rows + er;
+            o_tc[n_tc + et] = rec;
+            o_tcptr[n_tc + et] = tc_rows + er;
         }
         n_small += t1;
         n_tc += t2;
         tc_rows += t3;
     }
     if (tid == 0) {
-        p.indptr[S] = ACT;
-        p.tcptr[n_tc] = tc_rows;
+        o_indptr[S] = ACT;
+        o_tcptr[n_tc] = tc_rows;
     }
     // Descriptors past the last segment end the list (len 0).
     for (int s = S + tid; s < p.max_segs; s += nthr)
-        *reinterpret_cast<int4 *>(&p.desc[s]) = make_int4(0, 0, 0, s);
+        *reinterpret_cast<int4 *>(&o_desc[s]) = make_int4(0, 0, 0, s);
 
     // Phase 5: stable row positions.
     for (int k = tid; k < nwarps * G; k += nthr) whist[k] = 0;
@@ -364,12 +386,12 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
     // Positions: the warp's next free slot of each group, in registers for
     // the current run.
     auto place_row = [&](int i, int g, int pos) {
-        p.sorted[pos] = i;
+        o_sorted[pos] = i;
         // first rows of every segment, inline in its descriptor
         const int off = pos - grow[g];
         const int s = gseg[g] + (p.chunk > 0 ? off / p.chunk : 0);
         const int k = p.chunk > 0 ? off - (off / p.chunk) * p.chunk : off;
-        if (k < kInlineRows) p.desc[s].rows[k] = i;
+        if (k < kInlineRows) o_desc[s].rows[k] = i;
     };
     {
         int run_g = -1, run_next = 0;
@@ -408,6 +430,26 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
                 __syncwarp();
             }
         }
+    }
+
+    if (stage) {
+        // copy the staged outputs (descriptors as 16-byte pieces)
+        __syncthreads();
+        griddep_wait();
+        griddep_launch_dependents();
+        const int4 *dsrc = reinterpret_cast<const int4 *>(o_desc);
+        int4 *ddst = reinterpret_cast<int4 *>(p.desc);
+        const int nd = p.max_segs * int(sizeof(SegDesc) / 16);
+        for (int k = tid; k < nd; k += nthr) ddst[k] = dsrc[k];
+        for (int k = tid; k < n_small; k += nthr) p.small[k] = o_small[k];
+        for (int k = tid; k < n_tc; k += nthr) p.tc[k] = o_tc[k];
+        for (int k = tid; k <= S; k += nthr) p.indptr[k] = o_indptr[k];
+        for (int k = tid; k < S; k += nthr) {
+            p.lens[k] = o_lens[k];
+            p.widx[k] = o_widx[k];
+        }
+        for (int k = tid; k <= n_tc; k += nthr) p.tcptr[k] = o_tcptr[k];
+        for (int k = tid; k < ACT; k += nthr) p.sorted[k] = o_sorted[k];
     }
 
     // Phase 6: counters.
@@ -471,6 +513,7 @@ cudaError_t launch_prepare(const int32_t *ids, int32_t M, int32_t n, int32_t chu
     p.off_adapters = place(size_t(3) * n * 4);
     p.off_bits = M <= 65536 ? place(size_t(2) * ((M + 31) / 32) * 4) : -1;
     p.off_ids = place(size_t(M) * 4);
+    p.off_stage = place(size_t(L.max_segs) * (sizeof(SegDesc) + 32 + 16) + 8 + size_t(M) * 4);
 
     static DeviceOnce configured;
     cudaError_t e = configured.run([] {
