@@ -439,7 +439,12 @@ static cudaError_t launch_cc_t(const DeltaArgs &p, int cluster, int sms, cudaStr
     const CcGeom g = cc_geometry(p.r_max, cluster);
     static DeviceOnce once;
     cudaError_t e = once.run([&] {
-        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        // the block's 227 KB less the kernel's static shared memory
+        cudaFuncAttributes fa;
+        cudaError_t r = cudaFuncGetAttributes(&fa, kern);
+        if (r != cudaSuccess) return r;
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    227 * 1024 - (int)fa.sharedSizeBytes);
     });
     if (e != cudaSuccess) return e;
 
