@@ -13,9 +13,12 @@ barrier and a device synchronize.  Every step uses one of S rotating input
 sets (x, y, pools, ids, workspace) whose total exceeds L2, so no step finds
 its inputs in L2.  The kernels of a step are chained by programmatic
 dependent launch.  Kernel durations (for the roofline) come from one more
-replay of the same steps in which event nodes bracket every kernel; event
+replay of the same steps in which event nodes bracket every call; event
 nodes cut the programmatic overlap, so that replay is kept out of the timed
-region.
+region.  When one kernel takes every active row (the tensor-core kernel on
+prefill, the CUDA-core kernel on decode) a further replay forces the path to
+it, so the roofline divides by that kernel's own launch time; otherwise by
+the time of the whole lora_delta call.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
 a bounded sample of the same workload instead.
@@ -340,10 +343,20 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     except TypeError:
         use_graph = False
 
-    def capture(nsteps, offset, timed):
+    # The dominant kernel alone: when one kernel takes every active row, the
+    # path forced to it launches exactly that kernel with the same work.
+    dom_path = None
+    if args.path == 0 and counts["num_active"] > 0:
+        if counts["tc_rows"] == counts["num_active"]:
+            dom_path = 2
+        elif counts["tc_rows"] == 0:
+            dom_path = 1
+
+    def capture(nsteps, offset, timed, path=None):
         """Graph of `nsteps` steps.  With `timed`, event nodes bracket every
         kernel (they also cut the programmatic overlap between kernels, so
         the step-time graph has none)."""
+        path = args.path if path is None else path
         evs = [(torch.cuda.Event(enable_timing=True, external=True),
                 torch.cuda.Event(enable_timing=True, external=True),
                 torch.cuda.Event(enable_timing=True, external=True)) for _ in range(nsteps if timed else 0)]
@@ -358,7 +371,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                 if timed:
                     evs[i][1].record(stream)
                 B.lora_delta(batch, s["x"], s["A"], s["B"], s["y"], scale=w.scale,
-                             adapter_scale=ascale, ranks=ranks, path=args.path, stream=stream)
+                             adapter_scale=ascale, ranks=ranks, path=path, stream=stream)
                 if timed:
                     evs[i][2].record(stream)
         return g, evs
@@ -368,9 +381,12 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         g_main, _ = capture(G, 0, False)
         g_rem, _ = capture(rem, 0, False) if rem else (None, [])
         g_kern, ev_main = capture(G, 0, True)
+        g_dom, ev_dom = capture(G, 0, True, dom_path) if dom_path is not None else (None, [])
         with torch.cuda.stream(stream):
             g_main.replay()
             g_kern.replay()
+            if g_dom is not None:
+                g_dom.replay()
         stream.synchronize()
 
     if world > 1:
@@ -405,14 +421,18 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     # Kernel durations: the same steps replayed once more with event nodes
     # around every kernel, right after the timed region.
-    prep_us, delta_us = [], []
+    prep_us, delta_us, dom_us = [], [], []
     if use_graph:
         with torch.cuda.stream(stream):
             g_kern.replay()
+            if g_dom is not None:
+                g_dom.replay()
         stream.synchronize()
         for e0, e1, e2 in ev_main:
             prep_us.append(1e3 * e0.elapsed_time(e1))
             delta_us.append(1e3 * e1.elapsed_time(e2))
+        for e0, e1, e2 in ev_dom:
+            dom_us.append(1e3 * e1.elapsed_time(e2))
     ms_per_step = elapsed_ms / K
     value = whole_job_tokens_per_s(world, K, w.M, elapsed_ms)
 
@@ -443,7 +463,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     peak, peak_kind = load_peaks()
     d_us = statistics.mean(delta_us) if delta_us else None
-    achieved = ab["total"] / (d_us * 1e-6) / 1e9 if d_us else None
+    k_us = statistics.mean(dom_us) if dom_us else d_us
+    achieved = ab["total"] / (k_us * 1e-6) / 1e9 if k_us else None
     # dominant kernel: the tensor-core one when most active rows are in its segments
     kernel = "sgmv_tc_kernel" if 2 * counts["tc_rows"] > max(1, counts["num_active"]) else "sgmv_cc_kernel"
     traffic = committed_traffic(kernel, args.workload)
@@ -467,15 +488,19 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         },
         "kernels_us": {"prepare_mean": statistics.mean(prep_us) if prep_us else None,
                        "delta_mean": d_us,
-                       "delta_median": statistics.median(delta_us) if delta_us else None},
+                       "delta_median": statistics.median(delta_us) if delta_us else None,
+                       "kernel_mean": k_us},
         "algorithmic_bytes_per_step": ab["total"],
         "algorithmic_bytes_padded_rank": ab["total_padded_rank"],
-        "hbm_gbs_delta": achieved,
-        "frac_of_8tbs_delta": achieved / NOMINAL_HBM_GBS if achieved else None,
+        "hbm_gbs_delta": ab["total"] / (d_us * 1e-6) / 1e9 if d_us else None,
+        "frac_of_8tbs_delta": ab["total"] / (d_us * 1e-6) / 1e9 / NOMINAL_HBM_GBS if d_us else None,
         "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s",
-                     "duration": "mean event time of the lora_delta call (its CUDA-core and "
-                                 "tensor-core launches together)",
+                     "duration": ("mean event time of %s alone: a replay of the same steps with "
+                                  "the path forced to it, which then does the same work (it "
+                                  "takes every active row)" % kernel) if dom_us else
+                                 "mean event time of the lora_delta call (its CUDA-core and "
+                                 "tensor-core launches together: both have rows)",
                      "frac": achieved / peak if achieved else None, "traffic": traffic},
         "e2e": {"value": w.M / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
