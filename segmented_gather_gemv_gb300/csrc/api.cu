@@ -184,6 +184,7 @@ lora_status_t dispatch(const lora_batch_t *b, int32_t dtype, int mode, int32_t p
             if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
         }
         if (e == cudaSuccess) {
+            p.after_tc = split && b->M >= b->tc_min_rows ? 1 : 0;
             e = launch_cc(p, dtype, mode, cluster, sms, stream);
             if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
         }

@@ -329,6 +329,7 @@ struct DeltaArgs {
     int32_t max_list;        // host-side capacity of desc / recs
     int32_t min_len, max_len;  // the CUDA-core kernel takes segments with min_len <= len < max_len
     int32_t split_tc;          // 1: segments >= max_len with a tensor-core rank go to the tensor-core kernel
+    int32_t after_tc;          // 1: launched right after the tensor-core kernel, which waited on prepare
     int32_t M_rows;            // rows of x and y
     int32_t n_adapters;
     // tensor-core row space: segment i covers rows [tc_ptr[i], tc_ptr[i+1]),

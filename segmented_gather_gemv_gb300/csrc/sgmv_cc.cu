@@ -116,7 +116,12 @@ __global__ void __launch_bounds__(kCcThreads, 1)
     const uint32_t cid = cluster_id_x(), ncl = nclusters_x();
     const int RT = g.RT, HP = g.HP, SB = g.stage_bytes;
 
-    griddep_wait();
+    // Launched right after the tensor-core kernel, which triggers only after
+    // its own wait: the batch metadata is final and the two kernels write
+    // disjoint rows, so this grid works at once and waits for its
+    // predecessor only before it exits (its completion then implies the
+    // predecessor's).  Otherwise it waits first.
+    if (!p.after_tc) griddep_wait();
     griddep_launch_dependents();
 
     const int kv_total = p.d_in / V;
@@ -386,6 +391,7 @@ __global__ void __launch_bounds__(kCcThreads, 1)
             }
         }
     }
+    if (p.after_tc) griddep_wait();
 }
 
 // ---------------------------------------------------------------------------
