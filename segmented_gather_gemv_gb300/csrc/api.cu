@@ -11,7 +11,7 @@
 
 namespace lora {
 cudaError_t launch_prepare(const int32_t *ids, int32_t M, int32_t n, int32_t chunk, int32_t tc_min,
-                           char *ws, const WsLayout &L, lora_batch_t *b, cudaStream_t stream);
+                           int32_t share_grid, char *ws, const WsLayout &L, lora_batch_t *b, cudaStream_t stream);
 cudaError_t launch_cc(const DeltaArgs &p, int dtype, int mode, int cluster, int sms, cudaStream_t stream);
 int cc_cluster_size(int d_in, int d_out);
 cudaError_t launch_tc(const DeltaArgs &p, int mode, int sms, cudaStream_t stream);
@@ -180,6 +180,8 @@ lora_status_t dispatch(const lora_batch_t *b, int32_t dtype, int mode, int32_t p
             q.tc_count_index = LORA_COUNT_TC_SEGS;
             q.tc_rows_index = LORA_COUNT_TC_ROWS;
             q.tc_only = 0;
+            q.tc_share = share_table(b->counts);
+            q.tc_share_grid = sms <= kMaxShareGrid ? sms : -1;
             e = launch_tc(q, mode, sms, stream);
             if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
         }
@@ -218,7 +220,9 @@ lora_status_t lora_prepare_batch(const int32_t *ids, int32_t M, int32_t n_adapte
         return fail(LORA_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, L.total);
     const int32_t tc_min = tc_min_rows > 0 ? tc_min_rows : kDefaultTcMinRows;
     lora_batch_t b{};
-    cudaError_t e = launch_prepare(ids, M, n_adapters, chunk_size, tc_min, static_cast<char *>(workspace), L, &b,
+    const int grid = sm_count();
+    cudaError_t e = launch_prepare(ids, M, n_adapters, chunk_size, tc_min, grid <= kMaxShareGrid ? grid : 0,
+                                   static_cast<char *>(workspace), L, &b,
                                    static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "prepare launch failed: %s", cudaGetErrorString(e));
     launch_counter().fetch_add(1, std::memory_order_relaxed);

@@ -15,8 +15,12 @@ namespace lora {
 // Workspace layout of a prepared batch.  Every array starts on a 256-byte
 // boundary so that the device arrays are aligned for vector access.
 // ---------------------------------------------------------------------------
+// Largest tensor-core grid whose CTA shares prepare computes in advance.
+constexpr int kMaxShareGrid = 1024;
+
 struct WsLayout {
     size_t sorted, indptr, lens, widx, rec, small, tc, tcptr, counts;
+    size_t shares;                                   // right after counts: [kMaxShareGrid + 1] int2
     size_t first_pos, adapter_cnt, adapter_group;   // per adapter [n]
     size_t group_adapter, group_row, group_seg;      // per group [g_max]
     size_t warp_hist;                                // [32][g_max]
@@ -31,6 +35,12 @@ static inline int64_t max_segments(int64_t M, int64_t n, int64_t chunk) {
     if (chunk <= 0) return g;
     int64_t s = M / chunk + g;              // sum ceil(L_g / C) <= M / C + G
     return s < M ? s : M;                   // and never more than the rows
+}
+
+// The share table of a batch, from its counts pointer (ws_layout puts it
+// right after the counts).
+static inline const int2 *share_table(const int32_t *counts) {
+    return reinterpret_cast<const int2 *>(reinterpret_cast<const char *>(counts) + align256(LORA_NUM_COUNTS * 4));
 }
 
 static inline WsLayout ws_layout(int32_t M, int32_t n, int32_t chunk) {
@@ -52,6 +62,7 @@ static inline WsLayout ws_layout(int32_t M, int32_t n, int32_t chunk) {
     L.tc = take((size_t)ms * 4);
     L.tcptr = take((size_t)ms + 1);
     L.counts = take(LORA_NUM_COUNTS);
+    L.shares = take(2 * ((size_t)kMaxShareGrid + 1));
     L.first_pos = take((size_t)n);
     L.adapter_cnt = take((size_t)n);
     L.adapter_group = take((size_t)n);
@@ -330,6 +341,10 @@ struct DeltaArgs {
     int32_t min_len, max_len;  // the CUDA-core kernel takes segments with min_len <= len < max_len
     int32_t split_tc;          // 1: segments >= max_len with a tensor-core rank go to the tensor-core kernel
     int32_t after_tc;          // 1: launched right after the tensor-core kernel, which waited on prepare
+    // CTA shares of the tensor-core row space computed by prepare for a grid
+    // of tc_share_grid CTAs: boundary b = {first row of CTA b, its segment}
+    const int2 *tc_share;
+    int32_t tc_share_grid;
     int32_t M_rows;            // rows of x and y
     int32_t n_adapters;
     // tensor-core row space: segment i covers rows [tc_ptr[i], tc_ptr[i+1]),

@@ -43,6 +43,8 @@ struct PrepArgs {
     int32_t off_ids, off_adapters, off_groups, off_hist;
     int32_t off_bits;   // first-appearance bitmap and its word prefix, or -1
     int32_t off_stage;  // shared-memory copies of every phase 4-5 output, or -1
+    int2 *shares;       // tensor-core CTA shares: boundary b = {first row, segment}, b <= share_grid
+    int32_t share_grid;
 };
 
 // Block-wide exclusive scan of one value per thread.  `ws` is shared scratch
@@ -452,6 +454,41 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
         for (int k = tid; k < ACT; k += nthr) p.sorted[k] = o_sorted[k];
     }
 
+    // Shares of the tensor-core row space for a grid of share_grid CTAs,
+    // by the rule the tensor-core kernel applies itself when it has no
+    // table: the share end e = rows * b / grid moves to the boundary between
+    // two adapters when one lies within half a share (chunks of one adapter
+    // do not count).  Written for every batch, zeros when it has no such row.
+    {
+        __syncthreads();  // the tensor-core list (shared or global) is complete
+        const int4 *tcl = o_tc;
+        const int32_t *tcp = o_tcptr;
+        const int G = p.share_grid, nseg = n_tc, rows = tc_rows;
+        const int half = G > 0 ? (int)(rows / (2 * (int64_t)G)) : 0;
+        auto seg_of = [&](int r) {  // largest i < nseg with tcp[i] <= r
+            int lo = 0, hi = nseg - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (tcp[mid] <= r) lo = mid;
+                else hi = mid - 1;
+            }
+            return lo;
+        };
+        for (int b = tid; G > 0 && b <= G; b += nthr) {
+            int e = (int)((int64_t)rows * b / G), sg = 0;
+            if (nseg > 0 && rows > 0) {
+                if (nseg >= 2 && e > 0 && e < rows) {
+                    const int i = seg_of(e);
+                    const int lo = tcp[i], hi = tcp[i + 1], a = tcl[i].z;
+                    if (e - lo <= half && i > 0 && tcl[i - 1].z != a) e = lo;
+                    else if (hi - e <= half && i + 1 < nseg && tcl[i + 1].z != a) e = hi;
+                }
+                sg = e < rows ? seg_of(e) : nseg;
+            }
+            p.shares[b] = make_int2(e, sg);
+        }
+    }
+
     // Phase 6: counters.
     if (tid == 0) {
         p.counts[LORA_COUNT_SEGS] = S;
@@ -469,7 +506,7 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
 constexpr size_t kPrepSmemMax = 200 * 1024;
 
 cudaError_t launch_prepare(const int32_t *ids, int32_t M, int32_t n, int32_t chunk,
-                           int32_t tc_min, char *ws, const WsLayout &L,
+                           int32_t tc_min, int32_t share_grid, char *ws, const WsLayout &L,
                            lora_batch_t *b, cudaStream_t stream) {
     PrepArgs p{};
     p.ids = ids;
@@ -489,6 +526,8 @@ cudaError_t launch_prepare(const int32_t *ids, int32_t M, int32_t n, int32_t chu
     p.tc = reinterpret_cast<int4 *>(ws + L.tc);
     p.tcptr = at(L.tcptr);
     p.counts = at(L.counts);
+    p.shares = reinterpret_cast<int2 *>(ws + L.shares);
+    p.share_grid = share_grid;
     p.first_pos = at(L.first_pos);
     p.acnt = at(L.adapter_cnt);
     p.agroup = at(L.adapter_group);

@@ -408,7 +408,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             n == k ? (uint16_t)0x3F80 : (uint16_t)0;
         fence_proxy_async_smem();
     }
-    if (warp == kMmaWarp) {
+    if (warp == kMmaWarp && p.tc_share != nullptr && p.tc_share_grid == (int)gridDim.x) {
+        // the shares prepare computed for this grid (the same rule as below)
+        if (lane == 0) {
+            const int2 s0 = p.tc_share[blockIdx.x], s1 = p.tc_share[blockIdx.x + 1];
+            range[0] = s0.x;
+            range[1] = max(s0.x, s1.x);
+            range[2] = s0.x < s1.x ? s0.y : 0;
+        }
+    } else if (warp == kMmaWarp) {
         // This CTA's row range: an equal share of the row space.
         const int nseg = min(p.counts[p.tc_count_index], p.max_list);
         const int Mrows = nseg > 0 ? p.counts[p.tc_rows_index] : 0;
