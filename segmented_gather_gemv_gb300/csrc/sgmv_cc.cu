@@ -131,6 +131,7 @@ __global__ void __launch_bounds__(kCcThreads, 1)
     const T *xg = static_cast<const T *>(p.x);
     const T *Ag = static_cast<const T *>(p.A);
     uint32_t gjob = 0;  // jobs issued so far by this CTA (ring position and barrier phase)
+    bool pushed = false;  // this CTA has pushed a tile's partial h before
 
     for (int li = (int)cid; li < p.max_list; li += (int)ncl) {
         __syncthreads();  // the previous segment is done with desc_s / rows_s
@@ -256,6 +257,15 @@ __global__ void __launch_bounds__(kCcThreads, 1)
                     }
                 }
                 __syncthreads();
+                // Before a second push: every CTA of the cluster is done reading
+                // its receive buffer for the previous tile (all CTAs of a cluster
+                // walk the same tiles).  A CTA's last tile needs no barrier after
+                // it, so the CTA leaves right after its expand.
+                if (pushed) {
+                    cluster_arrive_release();
+                    cluster_wait_acquire();
+                }
+                pushed = true;
                 for (int e = tid; e < R * r; e += kCcThreads) {
                     const int row = e / r, j = e - row * r;
                     const int b = (row >> 2) * njg + (j >> 2), idx = (row & 3) * 4 + (j & 3);
@@ -383,12 +393,6 @@ __global__ void __launch_bounds__(kCcThreads, 1)
                 else cp_async_commit();
             }
             gjob += (uint32_t)total;
-            // Every CTA is done reading its receive buffer before any CTA
-            // pushes the next tile's partial h into it.
-            if (MODE != kExpand) {
-                cluster_arrive_release();
-                cluster_wait_acquire();
-            }
         }
     }
     if (p.after_tc) griddep_wait();
