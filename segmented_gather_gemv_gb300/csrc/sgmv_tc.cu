@@ -531,42 +531,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             const uint32_t box_bytes = (uint32_t)__popc(mask8) * 8 * 128;  // per atom
-            // A rows j = i0 + 8q of the stacked block: adapter row, or -1 (zero)
             const int K16 = (t.K + 15) & ~15;
-            int arow[kTcMaxRank / 8];
-            const __nv_bfloat16 *abase[kTcMaxRank / 8];
-#pragma unroll
-            for (int q = 0; q < kTcMaxRank / 8; ++q) {
-                const int j = i0 + 8 * q;
-                arow[q] = -1;
-                abase[q] = Ag;
-#pragma unroll
-                for (int u = 0; u < kMaxPieces; ++u)
-                    if (u < t.np && j >= t.kofs[u] && j < t.kofs[u] + t.rk[u]) {
-                        arow[q] = j - t.kofs[u];
-                        abase[q] = Ag + (int64_t)t.a[u] * p.a_stride_adapter;
-                    }
-            }
-            // this thread's B chunk (8 rank columns; the same in every y job):
-            // adapter and first column, or -1 (zero)
             const int n8 = K16 / 8, sh8 = n8 == 2 ? 1 : 2;
-            const int bcb = lt & (n8 - 1);
-            int b_a = 0, b_j = -1;
-#pragma unroll
-            for (int u = 0; u < kMaxPieces; ++u)
-                if (u < t.np && 8 * bcb >= t.kofs[u] && 8 * bcb < t.kofs[u] + t.rk[u]) {
-                    b_a = t.a[u];
-                    b_j = 8 * bcb - t.kofs[u];
-                }
-            const int slot_hi = (lt >> 4) & 1;  // lrow index of row i0 + 8q is 2q + slot_hi
             if (m.use_ab) {
                 // TMA path.  Lane 0 of warp 0 issues the boxes of atom 0, lane 0 of
-                // warp 1 those of atom 1, A block included.  The 64 threads of warps
-                // 2-3 copy the B block (small and in L2; a TMA box of it would move
-                // 16-byte pieces) and the rows that no box covers (a group split by
-                // a piece boundary or by a break in the token rows), from a list
-                // built once per tile.  Warp 0 stands in for the arrivals of the
-                // other loader threads, which sit these stages out.
+                // warp 1 those of atom 1, A block included.  The 64 threads of the
+                // other two loader warps copy the B block (small and in L2; a TMA
+                // box of it would move 16-byte pieces) and the rows that no box
+                // covers (a group split by a piece boundary or by a break in the
+                // token rows), from a list built once per tile.  The other lanes
+                // of warps 0 and 1 sit these stages out (the full barriers do not
+                // count them).
                 const int njobs = nkb + n_nt;
                 int covered = 0;
                 for (int g = 0; g < 16; ++g)
@@ -766,6 +741,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 continue;
             }
+            // cp.async path: per-thread tables of the A rows and the B chunk
+            // A rows j = i0 + 8q of the stacked block: adapter row, or -1 (zero)
+            int arow[kTcMaxRank / 8];
+            const __nv_bfloat16 *abase[kTcMaxRank / 8];
+#pragma unroll
+            for (int q = 0; q < kTcMaxRank / 8; ++q) {
+                const int j = i0 + 8 * q;
+                arow[q] = -1;
+                abase[q] = Ag;
+#pragma unroll
+                for (int u = 0; u < kMaxPieces; ++u)
+                    if (u < t.np && j >= t.kofs[u] && j < t.kofs[u] + t.rk[u]) {
+                        arow[q] = j - t.kofs[u];
+                        abase[q] = Ag + (int64_t)t.a[u] * p.a_stride_adapter;
+                    }
+            }
+            // this thread's B chunk (8 rank columns; the same in every y job):
+            // adapter and first column, or -1 (zero)
+            const int bcb = lt & (n8 - 1);
+            int b_a = 0, b_j = -1;
+#pragma unroll
+            for (int u = 0; u < kMaxPieces; ++u)
+                if (u < t.np && 8 * bcb >= t.kofs[u] && 8 * bcb < t.kofs[u] + t.rk[u]) {
+                    b_a = t.a[u];
+                    b_j = 8 * bcb - t.kofs[u];
+                }
+            const int slot_hi = (lt >> 4) & 1;  // lrow index of row i0 + 8q is 2q + slot_hi
             for (int kbi = 0; kbi < nkb; ++kbi) {
                 const int kb = kbi + kb_rot < nkb ? kbi + kb_rot : kbi + kb_rot - nkb;
                 if (!wait_warp(&empty[s], ph ^ 1, ok, abort)) goto role_done;
