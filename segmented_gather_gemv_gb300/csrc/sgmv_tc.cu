@@ -347,8 +347,9 @@ __device__ __forceinline__ int tile_token(const DeltaArgs &p, const Tile &t, int
 // box moves them.  Called by all 32 lanes of a warp; every lane gets the
 // same masks.
 __device__ __forceinline__ void tile_box_masks(const DeltaArgs &p, const TcMaps &m, const Tile &t, int lane,
-                                               uint32_t &mask8, uint32_t &mask32, uint32_t &mask64) {
+                                               uint32_t &mask8, uint32_t &mask32, uint32_t &mask64, int &tok8) {
     bool ok = false;
+    tok8 = 0;  // lanes 0-15: token row of tile row 8 lane (0 past the tile or without maps)
     if (m.use) {
         int i0 = -1, i1 = 0;
         if (lane < 16 && 8 * lane < t.n) {
@@ -361,7 +362,11 @@ __device__ __forceinline__ void tile_box_masks(const DeltaArgs &p, const TcMaps 
             i0 = 64 * (lane - 20);
             i1 = i0 + 63;
         }
-        if (i0 >= 0) ok = t.piece_of(i0) == t.piece_of(i1) && tile_token(p, t, i1) - tile_token(p, t, i0) == i1 - i0;
+        if (i0 >= 0) {
+            const int k0 = tile_token(p, t, i0);
+            ok = t.piece_of(i0) == t.piece_of(i1) && tile_token(p, t, i1) - k0 == i1 - i0;
+            if (lane < 16) tok8 = k0;
+        }
     }
     const uint32_t b = __ballot_sync(0xffffffffu, ok);
     mask8 = b & 0xFFFFu;
@@ -500,19 +505,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         while (walker.next(t)) {
             if (t.K == 0) continue;
             uint32_t mask8, mask32, mask64;
-            tile_box_masks(p, m, t, lane, mask8, mask32, mask64);
-            // this lane's slot: tile row (2 warp + (lane & 1)) + 8 (lane >> 1)
+            int tok8;
+            tile_box_masks(p, m, t, lane, mask8, mask32, mask64, tok8);
+            // token rows of the 8-row groups (the boxes' first rows), from the masks' reads
             {
-                const int i = 2 * lw + (lane & 1) + 8 * (lane >> 1);
                 __syncwarp();  // the previous tile's readers are done
-                lrow[lane] = i < t.n ? tile_token(p, t, i) : 0;
-                if (lw < 2 && lane < 16) lgt[lane] = 8 * lane < t.n ? tile_token(p, t, 8 * lane) : 0;
+                if (lw < 2 && lane < 16) lgt[lane] = 8 * lane < t.n ? (m.use ? tok8 : tile_token(p, t, 8 * lane)) : 0;
                 __syncwarp();
             }
-            // cp.async rows of this thread: bit q = row i0 + 8q
-            uint32_t mine = 0;
-#pragma unroll
-            for (int q = 0; q < kBM / 8; ++q) mine |= (i0 + 8 * q < t.n && !((mask8 >> q) & 1)) ? 1u << q : 0u;
             int nbox = 0;
             if (lw < 2 && lane == 0) {
                 for (int h = 0; h < 2; ++h) {
@@ -741,7 +741,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 continue;
             }
-            // cp.async path: per-thread tables of the A rows and the B chunk
+            // cp.async path: this lane's slot, tile row (2 warp + (lane & 1)) + 8 (lane >> 1)
+            {
+                const int i = 2 * lw + (lane & 1) + 8 * (lane >> 1);
+                __syncwarp();  // the previous tile's readers are done
+                lrow[lane] = i < t.n ? tile_token(p, t, i) : 0;
+                __syncwarp();
+            }
+            // cp.async rows of this thread: bit q = row i0 + 8q
+            uint32_t mine = 0;
+#pragma unroll
+            for (int q = 0; q < kBM / 8; ++q) mine |= (i0 + 8 * q < t.n && !((mask8 >> q) & 1)) ? 1u << q : 0u;
+            // per-thread tables of the A rows and the B chunk
             // A rows j = i0 + 8q of the stacked block: adapter row, or -1 (zero)
             int arow[kTcMaxRank / 8];
             const __nv_bfloat16 *abase[kTcMaxRank / 8];
