@@ -120,7 +120,10 @@ constexpr int kOffLdr = kOffMisc + 64;               // loader tables: row token
 // loader tables, at kOffLdr: row tokens [4 warps][32] ints, group tokens
 // [2][16] ints, TMA boxes [2][16] uint2, then the helpers' row lists [2][128] int2
 constexpr int kLdrGtok = 4 * 32 * 4, kLdrBox = kLdrGtok + 2 * 16 * 4, kLdrRows = kLdrBox + 2 * 16 * 8;
-constexpr int kLdrBytes = kLdrRows + 2 * kBM * 8;
+// each TMA issuer's resolved copies of the tile: {smem offset, map code, row or rank, adapter}
+constexpr int kCmdMax = 24;  // <= 16 row boxes + <= 4 rank boxes + 1 zero box
+constexpr int kLdrCmd = kLdrRows + 2 * kBM * 8;
+constexpr int kLdrBytes = kLdrCmd + 2 * kCmdMax * 16;
 // 16 x 16 bf16 identity, the B operand that adds a y stage into D2
 constexpr int kOffIdent = (kOffLdr + kLdrBytes + 127) & ~127;
 constexpr int kIdentBytes = 16 * 16 * 2;
@@ -548,65 +551,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if ((mask8 >> g) & 1) covered += min(8, t.n - 8 * g);
                 const int nu = t.n - covered;  // rows moved by cp.async
                 if (lw < 2 && lane == 0) {
-                    // This atom's copies of the tile, resolved once: up to kCmds
-                    // boxes (row boxes first, then the stacked A block in rank
-                    // boxes of 32/16/8) with their shared-memory offset, map
-                    // code and coordinates; the job loop only adds the column.
-                    constexpr int kCmds = 6;
-                    uint32_t c_off[kCmds];
-                    int c_code[kCmds], c_r[kCmds], c_a[kCmds];
-                    int nrow = 0, ncmd = 0;
-                    bool fast = nbox <= kCmds;
-#pragma unroll
-                    for (int q = 0; q < kCmds; ++q) {
-                        c_off[q] = 0;
-                        c_code[q] = 0;
-                        c_r[q] = 0;
-                        c_a[q] = 0;
-                        if (q < nbox) {
-                            const uint2 bx = lbox[q];
-                            c_off[q] = (uint32_t)(hq * xatom + (int)(bx.x & 255) * 128);
-                            c_code[q] = 2 - (int)(bx.x >> 8);  // 0: 64 rows, 1: 32, 2: 8
-                            c_r[q] = (int)bx.y;
-                        }
+                    // This atom's copies of the tile, resolved once into shared
+                    // memory: row boxes first, then the stacked A block in rank
+                    // boxes of 32/16/8 (and zero boxes up to K16); the job loop
+                    // only adds the column.
+                    uint4 *cmd = reinterpret_cast<uint4 *>(smem + kOffLdr + kLdrCmd) + kCmdMax * lw;
+                    int ncmd = 0;
+                    for (int q = 0; q < nbox; ++q) {
+                        const uint2 bx = lbox[q];
+                        cmd[ncmd++] = make_uint4((uint32_t)(hq * xatom + (int)(bx.x & 255) * 128), 2u - (bx.x >> 8), bx.y, 0u);
                     }
-                    nrow = ncmd = fast ? nbox : 0;
+                    const int nrow = ncmd;
                     const uint32_t abase_off = (uint32_t)(xbytes + hq * aatom);
-                    for (int u = 0; fast && u < t.np; ++u) {
+                    for (int u = 0; u < t.np; ++u) {
                         const int rk = sel(t.rk, u), ko = sel(t.kofs, u), au = sel(t.a, u);
-                        for (int j = 0; fast && j < rk;) {
+                        for (int j = 0; j < rk;) {
                             const int w = (rk - j >= 32 && m.a_box_max >= 32) ? 32 : (rk - j >= 16 && m.a_box_max >= 16) ? 16 : 8;
-                            if (ncmd == kCmds) {
-                                fast = false;
-                                break;
-                            }
-#pragma unroll
-                            for (int q = 0; q < kCmds; ++q)
-                                if (q == ncmd) {
-                                    c_off[q] = abase_off + (uint32_t)(ko + j) * 128;
-                                    c_code[q] = w == 32 ? 5 : w == 16 ? 4 : 3;
-                                    c_r[q] = j;
-                                    c_a[q] = au;
-                                }
-                            ++ncmd;
+                            cmd[ncmd++] = make_uint4(abase_off + (uint32_t)(ko + j) * 128, w == 32 ? 5u : w == 16 ? 4u : 3u,
+                                                     (uint32_t)j, (uint32_t)au);
                             j += w;
                         }
                     }
-                    for (int j = t.K; fast && j < K16; j += 8) {
-                        if (ncmd == kCmds) {
-                            fast = false;
-                            break;
-                        }
-#pragma unroll
-                        for (int q = 0; q < kCmds; ++q)
-                            if (q == ncmd) {
-                                c_off[q] = abase_off + (uint32_t)j * 128;
-                                c_code[q] = 3;
-                                c_r[q] = m.r_pad;
-                                c_a[q] = 0;
-                            }
-                        ++ncmd;
-                    }
+                    for (int j = t.K; j < K16; j += 8)
+                        cmd[ncmd++] = make_uint4(abase_off + (uint32_t)j * 128, 3u, (uint32_t)m.r_pad, 0u);
                     const uint32_t x_tx = box_bytes + (uint32_t)(K16 / 8) * 1024;
                     for (int jb = 0; jb < njobs; ++jb) {
                         if (!wait1(&empty[s], ph ^ 1, ok, abort)) goto role_done;
@@ -615,30 +582,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             const int kb = jb + kb_rot < nkb ? jb + kb_rot : jb + kb_rot - nkb;
                             const int col = kb * kBK + 64 * hq;
                             mbar_arrive_expect_tx(&full[s], x_tx);
-                            if (fast) {
-#pragma unroll
-                                for (int q = 0; q < kCmds; ++q) {
-                                    if (q >= ncmd) break;
-                                    const int cd = c_code[q];
-                                    if (cd < 3)
-                                        tma_load_2d(st + c_off[q], cd == 0 ? &m.x64 : cd == 1 ? &m.x32 : &m.x8, col, c_r[q], &full[s]);
-                                    else
-                                        tma_load_3d(st + c_off[q], cd == 5 ? &m.a32 : cd == 4 ? &m.a16 : &m.a8, col, c_r[q], c_a[q],
-                                                    &full[s]);
-                                }
-                            } else {
-                                for (int e = 0; e < nbox; ++e) {
-                                    const uint2 bx = lbox[e];
-                                    const int code = bx.x >> 8, i = bx.x & 255;
-                                    tma_load_2d(st + hq * xatom + i * 128, code == 2 ? &m.x64 : code == 1 ? &m.x32 : &m.x8, col,
-                                                (int)bx.y, &full[s]);
-                                }
-                                // the stacked A block of this atom: 8 rank rows per box
-                                unsigned char *abuf = st + xbytes + hq * aatom;
-                                for (int u = 0; u < t.np; ++u)
-                                    for (int j = 0; j < sel(t.rk, u); j += 8)
-                                        tma_load_3d(abuf + (sel(t.kofs, u) + j) * 128, &m.a8, col, j, sel(t.a, u), &full[s]);
-                                for (int j = t.K; j < K16; j += 8) tma_load_3d(abuf + j * 128, &m.a8, col, m.r_pad, 0, &full[s]);
+                            for (int q = 0; q < ncmd; ++q) {
+                                const uint4 c = cmd[q];
+                                const int cd = (int)c.y;
+                                if (cd < 3)
+                                    tma_load_2d(st + c.x, cd == 0 ? &m.x64 : cd == 1 ? &m.x32 : &m.x8, col, (int)c.z, &full[s]);
+                                else
+                                    tma_load_3d(st + c.x, cd == 5 ? &m.a32 : cd == 4 ? &m.a16 : &m.a8, col, (int)c.z, (int)c.w,
+                                                &full[s]);
                             }
                         } else {
                             const int nti = jb - nkb, nt = nti + nt_rot < n_nt ? nti + nt_rot : nti + nt_rot - n_nt;
@@ -646,22 +597,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             ntile_cols(p, nt, sl, c0, nc);
                             const int col = c0 + 64 * hq;
                             mbar_arrive_expect_tx(&full[s], box_bytes);
-                            if (fast) {
-#pragma unroll
-                                for (int q = 0; q < kCmds; ++q) {
-                                    if (q >= nrow) break;
-                                    const int cd = c_code[q];
-                                    tma_load_2d(st + c_off[q], cd == 0 ? &m.y64[sl] : cd == 1 ? &m.y32[sl] : &m.y8[sl], col, c_r[q],
-                                                &full[s]);
-                                }
-                            } else {
-                                for (int e = 0; e < nbox; ++e) {
-                                    const uint2 bx = lbox[e];
-                                    const int code = bx.x >> 8, i = bx.x & 255;
-                                    tma_load_2d(st + hq * xatom + i * 128,
-                                                code == 2 ? &m.y64[sl] : code == 1 ? &m.y32[sl] : &m.y8[sl], col, (int)bx.y,
-                                                &full[s]);
-                                }
+                            for (int q = 0; q < nrow; ++q) {
+                                const uint4 c = cmd[q];
+                                const int cd = (int)c.y;
+                                tma_load_2d(st + c.x, cd == 0 ? &m.y64[sl] : cd == 1 ? &m.y32[sl] : &m.y8[sl], col, (int)c.z,
+                                            &full[s]);
                             }
                         }
                         if (++s == NS) {
