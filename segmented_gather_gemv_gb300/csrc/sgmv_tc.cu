@@ -355,7 +355,10 @@ __device__ __forceinline__ void tile_box_masks(const DeltaArgs &p, const TcMaps 
     tok8 = 0;  // lanes 0-15: token row of tile row 8 lane (0 past the tile or without maps)
     if (m.use) {
         int i0 = -1, i1 = 0;
-        if (lane < 16 && 8 * lane < t.n) {
+        if (lane < 16 && 8 * lane < t.n && (8 * lane + 8 <= t.n || t.n < 32)) {
+            // In a tile of 32 rows or more, full groups only: a partial last
+            // group costs a whole TMA issue for a few rows, which the cp.async
+            // helpers copy for much less (in small tiles they are busy enough).
             i0 = 8 * lane;
             i1 = min(i0 + 7, t.n - 1);
         } else if (lane >= 16 && lane < 20 && 32 * (lane - 16) + 32 <= t.n) {
