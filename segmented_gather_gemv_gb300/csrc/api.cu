@@ -56,6 +56,17 @@ int sm_count() {
     return cache[dev];
 }
 
+// Grid of the tensor-core kernel for a batch of M rows: one CTA per 64 rows,
+// at most one per SM.  A tensor-core job costs a CTA about the same for 8 rows
+// as for 64 (its epilogue works per warp, not per row), so a small batch
+// gains nothing from more CTAs and leaves the other SMs to the CUDA-core
+// kernel, which then runs beside it.
+int tc_grid(int M) {
+    const int sms = sm_count();
+    const int g = (M + 63) / 64;
+    return g < 1 ? 1 : (g < sms ? g : sms);
+}
+
 lora_status_t check_batch(const lora_batch_t *b) {
     if (!b) return fail(LORA_ERR_INVALID, "batch is NULL");
     if (b->magic != kBatchMagic || !b->counts || !b->sorted_token_ids)
@@ -160,7 +171,7 @@ lora_status_t dispatch(const lora_batch_t *b, int32_t dtype, int mode, int32_t p
         p.tc_count_index = LORA_COUNT_SEGS;
         p.tc_rows_index = LORA_COUNT_ACTIVE;
         p.tc_only = 1;
-        e = launch_tc(p, mode, sms, stream);
+        e = launch_tc(p, mode, tc_grid(b->M), stream);
         if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
     } else {
         const bool split = path == LORA_PATH_AUTO && tensor_ok && mode == kFused;
@@ -181,8 +192,9 @@ lora_status_t dispatch(const lora_batch_t *b, int32_t dtype, int mode, int32_t p
             q.tc_rows_index = LORA_COUNT_TC_ROWS;
             q.tc_only = 0;
             q.tc_share = share_table(b->counts);
-            q.tc_share_grid = sms <= kMaxShareGrid ? sms : -1;
-            e = launch_tc(q, mode, sms, stream);
+            const int g = tc_grid(b->M);
+            q.tc_share_grid = g <= kMaxShareGrid ? g : -1;
+            e = launch_tc(q, mode, g, stream);
             if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
         }
         if (e == cudaSuccess) {
@@ -220,7 +232,7 @@ lora_status_t lora_prepare_batch(const int32_t *ids, int32_t M, int32_t n_adapte
         return fail(LORA_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, L.total);
     const int32_t tc_min = tc_min_rows > 0 ? tc_min_rows : kDefaultTcMinRows;
     lora_batch_t b{};
-    const int grid = sm_count();
+    const int grid = tc_grid(M);
     cudaError_t e = launch_prepare(ids, M, n_adapters, chunk_size, tc_min, grid <= kMaxShareGrid ? grid : 0,
                                    static_cast<char *>(workspace), L, &b,
                                    static_cast<cudaStream_t>(stream));
