@@ -199,7 +199,8 @@ lora_status_t dispatch(const lora_batch_t *b, int32_t dtype, int mode, int32_t p
         }
         if (e == cudaSuccess) {
             p.after_tc = split && b->M >= b->tc_min_rows ? 1 : 0;
-            e = launch_cc(p, dtype, mode, cluster, sms, stream);
+            // beside a tensor-core grid, the SMs that grid leaves free
+            e = launch_cc(p, dtype, mode, cluster, p.after_tc ? sms - tc_grid(b->M) : sms, stream);
             if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
         }
     }

@@ -488,7 +488,16 @@ static cudaError_t launch_cc_t(const DeltaArgs &p, int cluster, int sms, cudaStr
         max_clusters = active;
         cache.put((const void *)kern, dev, cluster, g.total, active);
     }
+    // No more clusters than the SMs left to this kernel hold (a tensor-core
+    // grid may hold the others: clusters that cannot start with the rest
+    // finish their segments last, and the next kernel in the stream starts
+    // only once every CTA has), but at least kCcMinClusters, so that a large
+    // batch whose tensor-core grid fills the GPU still spreads many small
+    // segments widely once that grid's CTAs leave.
+    constexpr int kCcMinClusters = 8;
     int nclusters = p.max_list < max_clusters ? p.max_list : max_clusters;
+    const int cap = sms / cluster > kCcMinClusters ? sms / cluster : kCcMinClusters;
+    if (nclusters > cap) nclusters = cap;
     if (nclusters < 1) nclusters = 1;
     cfg.gridDim = dim3(nclusters * cluster);
     return cudaLaunchKernelEx(&cfg, kern, p, g);

@@ -259,3 +259,15 @@ def test_mixed_rank_nan_padding_full_size(B):
     w = wl.mixed_rank(proj="down", pad_value=float("nan"))
     y, _ = _run_delta(B, w)
     _assert_delta(w, y)
+
+
+def test_large_batch_of_small_groups(B):
+    """A batch large enough for a full tensor-core grid whose rows all sit in
+    small adapter groups: every segment goes to the CUDA-core kernel, which
+    then runs with the smallest cluster count it allows beside that grid."""
+    w = wl.random_batch(seed=77, M=10240, d_in=512, d_outs=[384], n_pool=1500, r_max=16,
+                        run_len=2, skip_frac=0.05)
+    y, batch = _run_delta(B, w)
+    c = batch.counts()
+    assert c["tc_rows"] == 0 and c["num_small_segs"] > 500
+    _assert_delta(w, y)
