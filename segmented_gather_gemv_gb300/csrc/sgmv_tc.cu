@@ -6,10 +6,13 @@
 // unit.
 //
 // Work split: the rows of all segments routed here form one row space; CTA b
-// of a persistent grid takes the equal share [M b / G, M (b+1) / G), so every
-// CTA moves the same amount of x and y whatever the segment lengths.  Its
-// rows are cut into tiles of up to 128 rows; a tile may span several
-// segments (pieces, see Tile below), so a share never costs two passes.
+// of a persistent grid takes the equal share [M b / G, M (b+1) / G), its end
+// moved to a nearby boundary between adapters (prepare computes the shares
+// for this grid), so every CTA moves about the same amount of x and y
+// whatever the segment lengths.  The grid has one CTA per 64 batch rows, at
+// most one per SM.  A share is cut into tiles of up to 128 rows; a tile may
+// span several segments (pieces, see Tile below), so a share never costs two
+// passes.
 //
 // Per tile:
 //   shrink  D1[128 x K] (TMEM, fp32) = x_tile[128 x d_in] . A^T, where A
@@ -19,8 +22,10 @@
 //           adapter's columns, multiply by s_a, round to bf16 and write
 //           H[128 x K] to shared memory (never to global memory);
 //   expand  per 128-column n-tile: D2[128 x 128] (TMEM, triple buffered)
-//           = H . B^T, B stacking the adapters' rows of that n-tile;
-//   store   y_tile += D2 in fp32, rounded once to bf16.
+//           = y_tile . I + H . B^T: the y stage times a 16 x 16 identity puts
+//           y into the fp32 accumulator exactly, then B stacks the adapters'
+//           rows of that n-tile;
+//   store   D2 rounded once to bf16 and written back as y.
 // Ranks are masked exactly: A rows / B columns past an adapter's rank are
 // never read, H columns past it are zero, so padding never reaches y.
 //
@@ -45,12 +50,14 @@
 // sorted_token_ids) move by TMA: tiled copies of 64 columns x 64, 32 or 8
 // rows in the 128-byte swizzle, for x and y; the A block comes by TMA from a
 // 3-D map of the pool.  Rows that no box covers (a group of 8 split by a
-// piece boundary or by a break in the token rows) and the B block (16-byte
-// pieces of L2-resident rows) move by 16-byte cp.async.  A loader that
+// piece boundary or by a break in the token rows, and in tiles of 32 rows or
+// more a partial last group) and the B block (16-byte pieces of L2-resident
+// rows) move by 16-byte cp.async.  A loader that
 // issues one cp.async per 16 bytes for everything spends its time issuing
 // and waiting on its own instruction stream, which is why the boxes matter.
-// y is stored with st.global, four 128-byte row pieces per instruction: TMA
-// stores mixed with such stores in one CTA stalled the CTA's loads.
+// y is stored with st.global, eight 64-byte row pieces per warp
+// instruction: TMA stores mixed with such stores in one CTA stalled the
+// CTA's loads.
 //
 // Warp roles (672 threads): warps 0, 1, 2 and 4 loaders (lane 0 of warps 0
 // and 1 issue the boxes of atoms 0 and 1; warps 2 and 4 the cp.async
