@@ -20,10 +20,20 @@
 // row-gathered data); B rows land in an XOR-swizzled layout and are read only
 // up to the adapter's rank.
 //
-// Compute (fp32, packed FFMA2): shrink -- every thread owns a 4-row x 4-rank
-// block of h and strides over K with its accumulators live across all K
-// chunks; lanes sharing a block are reduced once, at the end.  Expand --
-// every thread owns two adjacent output columns and all rows of the tile.
+// Compute, bf16 inputs: warp-level tensor-core products (16 x 8 x 16 bf16
+// tiles, fp32 accumulators in registers).  Shrink -- the R x r output is cut
+// into 16 x 8 tiles; each warp takes one tile and every (16 / tiles)-th K
+// step, with four accumulators so that four products are in flight; the
+// warps' partial tiles are summed in warp order.  Expand -- h (scaled fp32)
+// is rounded once to bf16 in fragment order; each warp takes four 8-column
+// tiles at a time, adds y in the stage and the stage leaves in 16-byte row
+// pieces.  A tile of a few rows costs a handful of instructions per warp,
+// with no tensor-memory allocation or commit round trip on the path.
+// fp32 inputs (packed FFMA2, exact fp32 products): shrink -- every thread
+// owns a 4-row x 4-rank block of h and strides over K with its accumulators
+// live across all K chunks; lanes sharing a block are reduced once, at the
+// end.  Expand -- every thread owns two adjacent output columns and all rows
+// of the tile.
 #include "common.cuh"
 
 namespace lora {
@@ -97,6 +107,21 @@ __device__ __forceinline__ void group_reduce16(float (&v)[16], int lane, int S) 
     }
 }
 
+// bf16 products of a tile: D[16 x 8] += A[16 x 16] . B[16 x 8] on the warp's
+// tensor cores, fp32 accumulators in registers.  With g = lane / 4 and
+// t = lane % 4: a[0] holds A row g, k = 2t, 2t+1 (lower k in the low half),
+// a[1] row g + 8, a[2] row g with k + 8, a[3] row g + 8 with k + 8; b0 holds
+// B column g at k = 2t, 2t+1 and b1 the same column at k + 8; d[0], d[1] are
+// D row g, columns 2t, 2t+1 and d[2], d[3] row g + 8.  No shared-memory
+// staging of operands or accumulators is needed, so a tile of a few rows
+// costs a handful of instructions per warp.
+__device__ __forceinline__ void mma_16x8x16_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t lds_u32(const unsigned char *p) { return *reinterpret_cast<const uint32_t *>(p); }
+
 template <typename T, int MODE>
 __global__ void __launch_bounds__(kCcThreads, 1)
     sgmv_cc_kernel(const __grid_constant__ DeltaArgs p, const __grid_constant__ CcGeom g) {
@@ -168,17 +193,34 @@ __global__ void __launch_bounds__(kCcThreads, 1)
             const int my_rb = ob / (njg > 0 ? njg : 1), my_jg = ob - my_rb * (njg > 0 ? njg : 1);
             const bool has_block = ob < n_ob && njg > 0;
 
-            int nK = 0, kc = 1, nN = 0, nc = 1;
+            // bf16 tensor-core map: the shrink output (R rows x r ranks) in
+            // mt x ntr tiles of 16 x 8; warp w takes tile w % ntt and the K
+            // steps w / ntt, w / ntt + kp_n, ... (ntt <= 16: a tile of 17 or
+            // more rows only exists for r_max <= 60, so ntr <= 8 then).
+            const int mt = (R + 15) >> 4, ntr = max(1, (r + 7) >> 3), ntt = mt * ntr;
+            const int kp_n = kCcThreads / 32 / ntt;
+            const int my_t = warp % ntt, my_kp = warp / ntt;
+            const bool mma_on = my_kp < kp_n;
+            const int kr = (r + 15) >> 4;  // K steps of the expand (K = rank)
+
+            // Jobs: shrink stages hold R + r rows of kc 16-byte chunks (kc
+            // even, so that K steps of 16 elements stay within a job), expand
+            // stages R rows of nc chunks of y and nc * V rows of B.  Rows are
+            // kcs = kc + 1 and ncs = nc | 1 chunks apart: an odd stride puts
+            // the eight rows a fragment load touches in eight different bank
+            // groups.
+            int nK = 0, kc = 2, nN = 0, nc = 1;
             if (MODE != kExpand && kv1 > kv0) {
-                const int kcmax = max(1, SB / ((Rp + r) * 16));
+                const int kcmax = max(2, (SB / ((Rp + r) * 16) - 1) & ~1);
                 nK = (kv1 - kv0 + kcmax - 1) / kcmax;
-                kc = (kv1 - kv0 + nK - 1) / nK;
+                kc = (((kv1 - kv0 + nK - 1) / nK) + 1) & ~1;
             }
             if (MODE != kShrink && nv1 > nv0) {
-                const int ncmax = max(1, SB / ((R + V * rvp) * 16));
+                const int ncmax = max(1, (SB / 16 - R) / (R + V * rvp));
                 nN = (nv1 - nv0 + ncmax - 1) / ncmax;
                 nc = (nv1 - nv0 + nN - 1) / nN;
             }
+            const int kcs = kc + 1, ncs = nc | 1;
             const int total = nK + nN;
 
             // ---- issue one job into its stage (called by every thread): all
@@ -189,26 +231,30 @@ __global__ void __launch_bounds__(kCcThreads, 1)
                 unsigned char *sb = ring + (size_t)(G % kCcStages) * SB;
                 if (j < nK) {
                     const int kb = kv0 + j * kc, kn = min(kc, kv1 - kb);
+                    // bf16: an odd last chunk gets a zero partner, so that
+                    // its K step reads no stale bytes
+                    const int knf = sizeof(T) == 2 ? (kn + 1) & ~1 : kn;
                     for (int row = warp; row < R + r; row += kCcThreads / 32) {
                         const T *src = row < R ? xg + (int64_t)rows_s[row] * p.ldx + (int64_t)kb * V
                                                : Ag + (int64_t)a * p.a_stride_adapter +
                                                      (int64_t)(row - R) * p.a_stride_r + (int64_t)kb * V;
-                        unsigned char *dst = sb + (size_t)(row < R ? row : Rp + (row - R)) * kc * 16;
-                        for (int c = lane; c < kn; c += 32) cp_async16(dst + c * 16, src + c * V, 16);
+                        unsigned char *dst = sb + (size_t)(row < R ? row : Rp + (row - R)) * kcs * 16;
+                        for (int c = lane; c < knf; c += 32)
+                            cp_async16(dst + c * 16, c < kn ? src + c * V : src, c < kn ? 16 : 0);
                     }
                 } else {
                     const int nb = nv0 + (j - nK) * nc, nn = min(nc, nv1 - nb);
                     const int c0 = nb * V;
                     for (int row = warp; row < R; row += kCcThreads / 32) {
                         const int64_t yrow = (int64_t)rows_s[row] * p.ldy;
-                        unsigned char *dst = sb + (size_t)row * nc * 16;
+                        unsigned char *dst = sb + (size_t)row * ncs * 16;
                         for (int c = lane; c < nn; c += 32) {
                             const int col = c0 + c * V;
                             const SliceDesc &S = p.slices[slice_of(p, col)];
                             cp_async16(dst + c * 16, static_cast<const T *>(p.y) + yrow + S.y_col + (col - S.col_begin), 16);
                         }
                     }
-                    unsigned char *bst = sb + (size_t)R * nc * 16;
+                    unsigned char *bst = sb + (size_t)R * ncs * 16;
                     const int nrows = nn * V;
                     const int rv_shift = (rv & (rv - 1)) == 0 ? ilog2(rv) : -1;
                     for (int e = tid; e < nrows * rv; e += kCcThreads) {
@@ -225,23 +271,40 @@ __global__ void __launch_bounds__(kCcThreads, 1)
                 cp_async_commit();
             };
 
-            float2 acc[4][4];
+            float2 acc[4][4];  // fp32: 4 rows x 4 ranks (pairs of K)
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) acc[i][jj] = make_float2(0.f, 0.f);
+            // bf16: this warp's 16 x 8 tile in four accumulators (K steps
+            // round-robin), so that four products are in flight at once
+            float macc[4][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) macc[u][0] = macc[u][1] = macc[u][2] = macc[u][3] = 0.f;
+            // bf16 partial tiles [warp][lane][4] and the expand's h fragments
+            // [m tile][K step][lane][4] share the slot area (8 KB + 4 KB).
+            float *red = slots;
+            uint32_t *hfrag = reinterpret_cast<uint32_t *>(slots) + 2048;
 
             // ---- partial h of this CTA -> every CTA of the cluster -> h_full.
             auto finish_shrink = [&]() {
+                const int S = ilog2(KS < 32 ? KS : 32);
+                const int wpb = KS > 32 ? KS / 32 : 1;  // warps per block
+                if constexpr (sizeof(T) == 2) {
+                    if (mma_on)
+                        *reinterpret_cast<float4 *>(red + (warp * 32 + lane) * 4) =
+                            make_float4((macc[0][0] + macc[1][0]) + (macc[2][0] + macc[3][0]),
+                                        (macc[0][1] + macc[1][1]) + (macc[2][1] + macc[3][1]),
+                                        (macc[0][2] + macc[1][2]) + (macc[2][2] + macc[3][2]),
+                                        (macc[0][3] + macc[1][3]) + (macc[2][3] + macc[3][3]));
+                } else {
                 float v[16];
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) v[i * 4 + jj] = acc[i][jj].x + acc[i][jj].y;
-                const int S = ilog2(KS < 32 ? KS : 32);
                 group_reduce16(v, lane, S);
                 const int nvals = 16 >> (S < 4 ? S : 4);
-                const int wpb = KS > 32 ? KS / 32 : 1;  // warps per block
                 if (has_block) {
                     // this lane's share of the block's 16 totals
                     int base = 0;
@@ -255,6 +318,7 @@ __global__ void __launch_bounds__(kCcThreads, 1)
                         for (int i = 0; i < 16; ++i)
                             if (i < nvals) slots[wslot * 16 + base + i] = v[i];
                     }
+                }
                 }
                 __syncthreads();
                 // Before a second push: every CTA of the cluster is done reading
@@ -270,7 +334,14 @@ __global__ void __launch_bounds__(kCcThreads, 1)
                     const int row = e / r, j = e - row * r;
                     const int b = (row >> 2) * njg + (j >> 2), idx = (row & 3) * 4 + (j & 3);
                     float s = 0.f;
-                    for (int w = 0; w < wpb; ++w) s += slots[(b * wpb + w) * 16 + idx];
+                    if constexpr (sizeof(T) == 2) {
+                        // tile of (row, j), then its K-split partials in warp order
+                        const int t = (row >> 4) * ntr + (j >> 3);
+                        const int at = (((row & 7) << 2) + ((j & 7) >> 1)) * 4 + ((row >> 3) & 1) * 2 + (j & 1);
+                        for (int kp = 0; kp < kp_n; ++kp) s += red[(kp * ntt + t) * 128 + at];
+                    } else {
+                        for (int w = 0; w < wpb; ++w) s += slots[(b * wpb + w) * 16 + idx];
+                    }
                     const uint32_t local = smem_u32(recv + ((int)q * RT + row) * HP + j);
                     for (uint32_t pr = 0; pr < CL; ++pr) st_dsmem_f32(map_to_rank(local, pr), s);
                 }
@@ -315,16 +386,45 @@ __global__ void __launch_bounds__(kCcThreads, 1)
                 if (j < nK) {
                     // ---- shrink job: acc += x[rows of my block, K] . A[ranks of my block, K]
                     const int kn = min(kc, kv1 - (kv0 + j * kc));
-                    if (has_block) {
-                        const uint4 *xs = reinterpret_cast<const uint4 *>(sb) + (my_rb * 4) * kc;
-                        const uint4 *As = reinterpret_cast<const uint4 *>(sb + (size_t)Rp * kc * 16) + (my_jg * 4) * kc;
+                    if constexpr (sizeof(T) == 2) {
+                        // tensor-core tile (rows 16 mi.., ranks 8 ni..) over this
+                        // warp's K steps; rows past R and ranks past r are zero
+                        if (mma_on) {
+                            const int mi = my_t / ntr, ni = my_t - mi * ntr;
+                            const int gq = lane >> 2, tq = lane & 3;
+                            const int xr = mi * 16 + gq, an = ni * 8 + gq;
+                            const bool v0 = xr < R, v1 = xr + 8 < R, va = an < r;
+                            const unsigned char *x0 = sb + (size_t)xr * kcs * 16 + tq * 4;
+                            const unsigned char *x1 = x0 + (size_t)8 * kcs * 16;
+                            const unsigned char *ap = sb + (size_t)(Rp + an) * kcs * 16 + tq * 4;
+                            const int nks = (kn + 1) >> 1;
+                            for (int st0 = my_kp; st0 < nks; st0 += 4 * kp_n) {
+                                uint32_t af[4][4], b0[4], b1[4];
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    const int st = st0 + u * kp_n;
+                                    const bool in = st < nks;
+                                    af[u][0] = in && v0 ? lds_u32(x0 + st * 32) : 0u;
+                                    af[u][1] = in && v1 ? lds_u32(x1 + st * 32) : 0u;
+                                    af[u][2] = in && v0 ? lds_u32(x0 + st * 32 + 16) : 0u;
+                                    af[u][3] = in && v1 ? lds_u32(x1 + st * 32 + 16) : 0u;
+                                    b0[u] = in && va ? lds_u32(ap + st * 32) : 0u;
+                                    b1[u] = in && va ? lds_u32(ap + st * 32 + 16) : 0u;
+                                }
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) mma_16x8x16_bf16(macc[u], af[u], b0[u], b1[u]);
+                            }
+                        }
+                    } else if (has_block) {
+                        const uint4 *xs = reinterpret_cast<const uint4 *>(sb) + (my_rb * 4) * kcs;
+                        const uint4 *As = reinterpret_cast<const uint4 *>(sb + (size_t)Rp * kcs * 16) + (my_jg * 4) * kcs;
                         const int jvalid = r - my_jg * 4;  // ranks of this block that exist
                         for (int kv = ks; kv < kn; kv += KS) {
                             uint4 av[4], xv[4];
 #pragma unroll
-                            for (int jj = 0; jj < 4; ++jj) av[jj] = jj < jvalid ? As[jj * kc + kv] : make_uint4(0, 0, 0, 0);
+                            for (int jj = 0; jj < 4; ++jj) av[jj] = jj < jvalid ? As[jj * kcs + kv] : make_uint4(0, 0, 0, 0);
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) xv[i] = xs[i * kc + kv];
+                            for (int i = 0; i < 4; ++i) xv[i] = xs[i * kcs + kv];
 #pragma unroll
                             for (int qq = 0; qq < PV; ++qq) {
                                 float2 ap[4], xp[4];
@@ -344,9 +444,93 @@ __global__ void __launch_bounds__(kCcThreads, 1)
                     // ---- expand job: y[rows, c..c+1] += h . B[c..c+1]^T
                     const int nb = nv0 + (j - nK) * nc, nn = min(nc, nv1 - nb);
                     const int npairs = nn * V / 2;
-                    const uint4 *Bs = reinterpret_cast<const uint4 *>(sb + (size_t)R * nc * 16);
+                    const uint4 *Bs = reinterpret_cast<const uint4 *>(sb + (size_t)R * ncs * 16);
                     const typename E::PairT *ys = reinterpret_cast<const typename E::PairT *>(sb);
-                    const int ystride = nc * V / 2;
+                    const int ystride = ncs * V / 2;
+                    if constexpr (sizeof(T) == 2) {
+                        if (j == nK) {
+                            // h (scaled, fp32) rounded once to bf16, in fragment
+                            // order: [m tile][K step][lane][a0..a3]
+                            for (int e = tid; e < mt * kr * 128; e += kCcThreads) {
+                                const int rg = e & 3, ln = (e >> 2) & 31, blk = e >> 7;
+                                const int mi = blk / kr, st = blk - mi * kr;
+                                const int row = mi * 16 + (ln >> 2) + ((rg & 1) ? 8 : 0);
+                                const int col = st * 16 + 2 * (ln & 3) + ((rg & 2) ? 8 : 0);
+                                const float lo = row < R && col < r ? h_full[row * HP + col] : 0.f;
+                                const float hi = row < R && col + 1 < r ? h_full[row * HP + col + 1] : 0.f;
+                                const __nv_bfloat162 hv = __floats2bfloat162_rn(lo, hi);
+                                hfrag[e] = *reinterpret_cast<const uint32_t *>(&hv);
+                            }
+                            __syncthreads();
+                        }
+                        // warp per 8-column tile: y[rows, 8 cols] += h . B[8 cols]^T,
+                        // B fragments from the swizzled rows (chunks past the
+                        // rank are zero); the sums replace y in the stage, which
+                        // then goes out in 16-byte row pieces
+                        const int gq = lane >> 2, tq = lane & 3;
+                        uint32_t *yst = reinterpret_cast<uint32_t *>(const_cast<unsigned char *>(sb));
+                        const unsigned char *Bb = reinterpret_cast<const unsigned char *>(Bs);
+                        constexpr int kW = kCcThreads / 32;
+                        for (int jt0 = warp; jt0 < nn; jt0 += 4 * kW) {
+                            // column tiles jt0, jt0 + kW, ... (four at a time)
+                            float d[2][4][4];
+#pragma unroll
+                            for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) d[mi][u][0] = d[mi][u][1] = d[mi][u][2] = d[mi][u][3] = 0.f;
+                            for (int st = 0; st < kr; ++st) {
+                                uint32_t bq0[4], bq1[4];
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    const int n = (jt0 + u * kW) * 8 + gq;
+                                    const bool in = jt0 + u * kW < nn;
+                                    bq0[u] = in && 2 * st < rv ? lds_u32(Bb + (size_t)(n * rvp + b_swizzle(n, 2 * st, rvp)) * 16 + tq * 4) : 0u;
+                                    bq1[u] = in && 2 * st + 1 < rv ? lds_u32(Bb + (size_t)(n * rvp + b_swizzle(n, 2 * st + 1, rvp)) * 16 + tq * 4) : 0u;
+                                }
+#pragma unroll
+                                for (int mi = 0; mi < 2; ++mi) {
+                                    if (mi < mt) {
+                                        const uint4 av = *reinterpret_cast<const uint4 *>(hfrag + ((mi * kr + st) * 32 + lane) * 4);
+                                        const uint32_t af[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+                                        for (int u = 0; u < 4; ++u) mma_16x8x16_bf16(d[mi][u], af, bq0[u], bq1[u]);
+                                    }
+                                }
+                            }
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int jt = jt0 + u * kW;
+                                if (jt < nn) {
+#pragma unroll
+                                    for (int mi = 0; mi < 2; ++mi) {
+                                        const int row0 = mi * 16 + gq, row1 = row0 + 8;
+                                        if (row0 < R) {
+                                            const int at = row0 * ystride + jt * 4 + tq;
+                                            const float2 yv = E::pair_to_f32(yst[at]);
+                                            const __nv_bfloat162 o = __floats2bfloat162_rn(yv.x + d[mi][u][0], yv.y + d[mi][u][1]);
+                                            yst[at] = *reinterpret_cast<const uint32_t *>(&o);
+                                        }
+                                        if (row1 < R) {
+                                            const int at = row1 * ystride + jt * 4 + tq;
+                                            const float2 yv = E::pair_to_f32(yst[at]);
+                                            const __nv_bfloat162 o = __floats2bfloat162_rn(yv.x + d[mi][u][2], yv.y + d[mi][u][3]);
+                                            yst[at] = *reinterpret_cast<const uint32_t *>(&o);
+                                        }
+                                    }
+                                }
+                            }
+                        }
+                        __syncthreads();
+                        for (int row = warp; row < R; row += kCcThreads / 32) {
+                            T *yrow = static_cast<T *>(p.y) + (int64_t)rows_s[row] * p.ldy;
+                            for (int c = lane; c < nn; c += 32) {
+                                const int col = nb * V + c * V;
+                                const SliceDesc &S = p.slices[slice_of(p, col)];
+                                *reinterpret_cast<uint4 *>(yrow + S.y_col + (col - S.col_begin)) =
+                                    *reinterpret_cast<const uint4 *>(sb + ((size_t)row * ncs + c) * 16);
+                            }
+                        }
+                    } else
                     for (int cp = tid; cp < npairs; cp += kCcThreads) {
                         const int c0 = 2 * cp, c1 = c0 + 1;
                         const int col = nb * V + c0;
