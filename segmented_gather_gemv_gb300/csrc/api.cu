@@ -178,12 +178,25 @@ lora_status_t dispatch(const lora_batch_t *b, int32_t dtype, int mode, int32_t p
         p.min_len = 0;
         p.max_len = split ? b->tc_min_rows : 0x7fffffff;
         p.split_tc = split ? 1 : 0;
-        // The two kernels write disjoint rows of y.  The tensor-core kernel
-        // goes first: when the batch has no long segment its CTAs leave right
-        // after prepare, instead of queueing for SMs behind the CUDA-core
-        // kernel's CTAs at the end of the call.
-        if (split && b->M >= b->tc_min_rows) {
+        // The two kernels write disjoint rows of y and run side by side, the
+        // second one launched as soon as the first has passed its wait on
+        // prepare.  Batches of up to kCcFirstMaxRows rows (decode steps,
+        // where a segment of tc_min_rows rows is rare) start the CUDA-core
+        // kernel first, so that it is resident and waiting when prepare
+        // ends; larger batches start the tensor-core kernel first, so that
+        // its long segments begin at once.  The tensor-core grid then waits
+        // for the CUDA-core kernel before it exits.
+        const bool with_tc = split && b->M >= b->tc_min_rows;
+        const int g = with_tc ? tc_grid(b->M) : 0;
+        const bool cc_first = with_tc && b->M <= kCcFirstMaxRows;
+        if (cc_first) {
+            // leaves the tensor-core grid and the next prepare an SM each
+            e = launch_cc(p, dtype, mode, cluster, sms - g - 1, stream);
+            if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
+        }
+        if (with_tc && e == cudaSuccess) {
             DeltaArgs q = p;
+            q.after_cc = cc_first ? 1 : 0;
             q.tc_ptr = b->tc_indptr;
             q.tc_start = b->tc_segs;
             q.tc_adapter = b->tc_segs + 2;
@@ -192,15 +205,14 @@ lora_status_t dispatch(const lora_batch_t *b, int32_t dtype, int mode, int32_t p
             q.tc_rows_index = LORA_COUNT_TC_ROWS;
             q.tc_only = 0;
             q.tc_share = share_table(b->counts);
-            const int g = tc_grid(b->M);
             q.tc_share_grid = g <= kMaxShareGrid ? g : -1;
             e = launch_tc(q, mode, g, stream);
             if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
         }
-        if (e == cudaSuccess) {
-            p.after_tc = split && b->M >= b->tc_min_rows ? 1 : 0;
+        if (e == cudaSuccess && !cc_first) {
+            p.after_tc = with_tc ? 1 : 0;
             // beside a tensor-core grid, the SMs that grid leaves free
-            e = launch_cc(p, dtype, mode, cluster, p.after_tc ? sms - tc_grid(b->M) : sms, stream);
+            e = launch_cc(p, dtype, mode, cluster, with_tc ? sms - g : sms, stream);
             if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
         }
     }

@@ -96,6 +96,9 @@ std::atomic<int64_t> &launch_counter();
 
 constexpr uint32_t kBatchMagic = 0x4C6F5241u;  // "LoRA"
 constexpr int kDefaultTcMinRows = 64;
+// Batches of at most this many rows start the CUDA-core kernel before the
+// tensor-core kernel (see the dispatch in api.cu).
+constexpr int kCcFirstMaxRows = 256;
 constexpr int kTcMaxRankCommon = 32;
 // Ranks the tensor-core kernel computes (exact 8-column masking, <= 32).
 __host__ __device__ __forceinline__ bool tc_rank_ok(int r) { return r > 0 && r <= kTcMaxRankCommon && (r & 7) == 0; }
@@ -341,6 +344,7 @@ struct DeltaArgs {
     int32_t min_len, max_len;  // the CUDA-core kernel takes segments with min_len <= len < max_len
     int32_t split_tc;          // 1: segments >= max_len with a tensor-core rank go to the tensor-core kernel
     int32_t after_tc;          // 1: launched right after the tensor-core kernel, which waited on prepare
+    int32_t after_cc;          // 1: tensor-core kernel launched right after the CUDA-core kernel, which waited on prepare
     // CTA shares of the tensor-core row space computed by prepare for a grid
     // of tc_share_grid CTAs: boundary b = {first row of CTA b, its segment}
     const int2 *tc_share;

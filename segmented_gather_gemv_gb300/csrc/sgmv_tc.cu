@@ -415,7 +415,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fence_mbar_init();
         *abort = 0;
     }
-    griddep_wait();
+    // Launched right after the CUDA-core kernel (which triggers only after
+    // its own wait on prepare), this grid starts at once and waits for its
+    // predecessor only before it exits, so that its completion implies the
+    // predecessor's.  Otherwise it waits first.
+    if (!p.after_cc) griddep_wait();
     griddep_launch_dependents();
 
     if (tid < 256) {
@@ -467,7 +471,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     // A CTA without rows (no tensor-core segments in this batch, or fewer
     // rows than CTAs) leaves before it takes TMEM.
-    if (range[0] >= range[1]) return;
+    if (range[0] >= range[1]) {
+        if (p.after_cc) griddep_wait();
+        return;
+    }
     if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(smem_u32(tmem_slot))
                      : "memory");
@@ -1027,6 +1034,7 @@ role_done:
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tmem) : "memory");
     }
+    if (p.after_cc) griddep_wait();
 }
 
 // ---------------------------------------------------------------------------

@@ -116,3 +116,39 @@ def test_auto_split_rank64_long_segments_use_cuda_cores(B):
     y, batch = _run(B, w, path=B.PATH_AUTO, tc_min=16)
     _check(w, y)
     assert batch.counts()["device_error"] == 0
+
+
+@pytest.mark.parametrize("n_decode", [0, 60, 106])
+def test_auto_split_small_batch_both_kernels(B, n_decode):
+    # batches of at most 256 rows start the CUDA-core kernel first; here the
+    # tensor-core kernel after it has long segments to do as well
+    w = wl.mixed_serving(n_prefill_seq=2, prefill_rows=150, len_lo=64, len_hi=100, n_decode=n_decode,
+                         n_pool=16, r=16, d_in=1024, d_outs=(512, 256, 256))
+    assert w.M <= 256
+    y, batch = _run(B, w, path=B.PATH_AUTO)
+    _check(w, y)
+    c = batch.counts()
+    assert c["tc_rows"] > 0 and c["device_error"] == 0
+    assert (c["num_small_segs"] > 0) == (n_decode > 0)
+
+
+@pytest.mark.parametrize("M", [200, 256, 257, 600])
+def test_auto_split_back_to_back_calls(B, M):
+    # two calls in a row on one batch and one y (the second kernel pair starts
+    # while the first may still be finishing): y gains the delta twice
+    n_dec = M // 3
+    w = wl.mixed_serving(n_prefill_seq=2, prefill_rows=M - n_dec, len_lo=64, len_hi=400, n_decode=n_dec,
+                         n_pool=16, r=16, d_in=1024, d_outs=(512, 256, 256))
+    d = to_dev(w)
+    batch = B.lora_prepare_batch(d["ids"], w.n_adapters, w.chunk_size)
+    y = d["y"]
+    for _ in range(2):
+        B.lora_delta(batch, d["x"], d["A"], d["B"], y, scale=w.scale, path=B.PATH_AUTO)
+    torch.cuda.synchronize()
+    yg = y.float().cpu().numpy().astype(np.float64)
+    base = w.y.astype(np.float64)
+    once = oracle_delta(w)
+    act = active_rows(w)
+    assert rel_err(yg, base + 2.0 * (once - base), base, act) <= 2 * TOL[w.dtype]
+    assert np.array_equal(yg[~act], base[~act])
+    assert batch.counts()["tc_rows"] > 0
