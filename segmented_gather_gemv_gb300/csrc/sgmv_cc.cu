@@ -12,6 +12,10 @@
 // distributed shared memory and summed in a fixed order, so every CTA holds
 // the same h; h never leaves the chip.
 //
+// Order: cluster c takes segments c, c + C, ... (C clusters); with
+// per-adapter ranks and more segments than clusters, the CTAs first deal the
+// tiles to the clusters by an estimate of their time (the work plan below).
+//
 // Latency: a segment is reached through one 128-byte descriptor that holds
 // its first rows inline, so every load address of the tile is known after a
 // single dependent read.  All x/A (shrink) and y/B (expand) bytes of a tile
@@ -41,13 +45,17 @@ namespace lora {
 constexpr int kCcThreads = 512;
 constexpr int kCcStages = 3;
 constexpr int kCcMaxCluster = 8;
+// Work plan limits: segment lists and tile counts above these are walked
+// round-robin instead.
+constexpr int kPlanMaxSegs = 256;
+constexpr int kPlanMaxTiles = 512;
 
 // Shared-memory layout of one launch (computed on the host).
 struct CcGeom {
     int RT;           // rows per tile (multiple of 4, <= kInlineRows)
     int HP;           // r_max rounded up to 8
     int stage_bytes;  // bytes per ring stage (multiple of 128)
-    int off_bars, off_desc, off_rows, off_slots, off_recv, off_hfull, off_ring;
+    int off_bars, off_desc, off_rows, off_slots, off_recv, off_hfull, off_plan, off_ring;
     int total;
 };
 
@@ -158,17 +166,135 @@ __global__ void __launch_bounds__(kCcThreads, 1)
     uint32_t gjob = 0;  // jobs issued so far by this CTA (ring position and barrier phase)
     bool pushed = false;  // this CTA has pushed a tile's partial h before
 
-    for (int li = (int)cid; li < p.max_list; li += (int)ncl) {
-        __syncthreads();  // the previous segment is done with desc_s / rows_s
-        if (tid < 32) desc_s[tid] = reinterpret_cast<const int32_t *>(p.desc + li)[tid];
+    // Segments this kernel takes (the others belong to the tensor-core
+    // kernel, or add nothing).
+    auto seg_taken = [&](int len, int flags, int r) {
+        if (len == 0 || len < p.min_len) return false;
+        // segments of long adapter groups (flagged by prepare) belong to the
+        // tensor-core kernel when it can take their rank
+        if (p.split_tc && (flags & LORA_DESC_TC_FLAG) && tc_rank_ok(r)) return false;
+        if (r == 0 && MODE != kShrink) return false;  // rank 0: nothing to add
+        return true;
+    };
+
+    // ---- work plan.  By default cluster c walks segments c, c + C, ...
+    // (C clusters).  With per-adapter ranks the tiles differ in cost several
+    // fold, and that order can leave one cluster with several heavy tiles;
+    // then, with more segments than clusters, every CTA builds the same
+    // plan: each tile of a taken segment gets an estimate of its time (a
+    // fixed part plus the bytes a CTA moves), the tiles are ranked by it
+    // (ties by position) and dealt to the clusters in snake order -- 0..C-1,
+    // then C-1..0, ... -- largest first.  The descriptors, ranks and the
+    // segment count are read in one round trip.
+    int32_t *plan = reinterpret_cast<int32_t *>(smem + g.off_plan);  // [0] = tiles of this cluster, then the tiles
+    int n_plan = -1;  // -1: round-robin over segments
+    const bool may_plan = p.ranks != nullptr && p.counts != nullptr && p.n_adapters <= kCcThreads;
+    int4 pd = make_int4(0, 0, 0, 0);  // this thread's descriptor head {start, len, adapter, flags}
+    int32_t *p_rank = reinterpret_cast<int32_t *>(ring);  // scratch in the (still unused) ring
+    if (tid < 32) desc_s[tid] = reinterpret_cast<const int32_t *>(p.desc + cid)[tid];  // round-robin's first
+    if (may_plan) {
+        if (tid < min(p.max_list, kPlanMaxSegs)) pd = *reinterpret_cast<const int4 *>(p.desc + tid);
+        if (tid < p.n_adapters) p_rank[tid] = p.ranks[tid];
+        if (tid == 32) plan[0] = min(p.counts[LORA_COUNT_SEGS], p.max_list);
+    }
+    __syncthreads();
+    const int S_all = may_plan ? plan[0] : -1;
+    if (S_all > (int)ncl && S_all <= kPlanMaxSegs) {
+        // per segment its tile count, then per tile its cost and code
+        // (segment << 16 | tile)
+        int32_t *s_tiles = p_rank + kCcThreads;                                 // [kPlanMaxSegs + 1]
+        float *t_cost = reinterpret_cast<float *>(s_tiles + kPlanMaxSegs + 1);  // [kPlanMaxTiles]
+        int32_t *t_code = reinterpret_cast<int32_t *>(t_cost + kPlanMaxTiles);  // [kPlanMaxTiles]
+        int my_r = 0, my_nt = 0;
+        if (tid < S_all) {
+            my_r = pd.z >= 0 && pd.z < p.n_adapters ? p_rank[pd.z] : -1;
+            if (seg_taken(pd.y, pd.w, my_r)) {
+                if (my_r < 0 || my_r > p.r_max) {
+                    if (cid == 0 && q == 0) raise_deverr(p.counts, LORA_DEVERR_RANK);
+                } else {
+                    my_nt = (pd.y + RT - 1) / RT;
+                }
+            }
+        }
+        // exclusive prefix sum of the tile counts over the first S_all
+        // threads (warp scans, then the warp totals)
+        int x = my_nt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        int *wsum = reinterpret_cast<int *>(t_code + kPlanMaxTiles);  // [16]
+        if (lane == 31) wsum[warp] = x;
         __syncthreads();
+        int base = 0;
+        for (int w = 0; w < warp; ++w) base += wsum[w];
+        if (tid < S_all) s_tiles[tid] = base + x - my_nt;
+        if (tid == kCcThreads - 1) s_tiles[S_all] = base + x;  // total (threads past S_all add 0)
+        __syncthreads();
+        const int NT = s_tiles[S_all];
+        if (NT > (int)ncl && NT <= kPlanMaxTiles) {
+            const float es = (float)sizeof(T);
+            const float per_rank = (float)(p.d_in + p.d_out_total) * es / (float)CL;
+            const float per_row = (float)(p.d_in + 2 * p.d_out_total) * es / (float)CL;
+            const float fixed = 120000.f;  // about 3 us of one CTA's streaming, in bytes
+            if (tid < S_all) {
+                const int b0 = s_tiles[tid];
+                for (int t = 0; t < my_nt; ++t) {
+                    const int R = min(RT, pd.y - t * RT);
+                    t_cost[b0 + t] = fixed + per_rank * (float)my_r + per_row * (float)R;
+                    t_code[b0 + t] = (tid << 16) | t;
+                }
+            }
+            __syncthreads();
+            const int C = (int)ncl;
+            for (int j = tid; j < NT; j += kCcThreads) {
+                const float cj = t_cost[j];
+                int pos = 0;
+                for (int k = 0; k < NT; ++k) {
+                    const float ck = t_cost[k];
+                    pos += (ck > cj || (ck == cj && k < j)) ? 1 : 0;
+                }
+                const int round = pos / C, m = pos - round * C;
+                const int cl = (round & 1) ? C - 1 - m : m;
+                if (cl == (int)cid) plan[1 + round] = t_code[j];
+            }
+            if (tid == 0) {
+                // rounds 0 .. full - 1 give every cluster a tile; the last
+                // round gives one to the clusters whose place is below its size
+                const int full = NT / C, rest = NT - full * C;
+                const int m = (full & 1) ? C - 1 - (int)cid : (int)cid;
+                plan[0] = full + (m < rest ? 1 : 0);
+            }
+            __syncthreads();
+            n_plan = plan[0];
+        }
+    }
+    __syncthreads();  // the scratch is dead before the ring is used
+
+    for (int e = 0;; ++e) {
+        int li, tb, te;  // segment and tiles [tb, te) of this entry
+        if (n_plan >= 0) {
+            if (e >= n_plan) break;
+            const int code = plan[1 + e];
+            li = code >> 16;
+            tb = code & 0xFFFF;
+            te = tb + 1;
+        } else {
+            li = (int)cid + e * (int)ncl;
+            if (li >= p.max_list) break;
+            tb = 0;
+            te = 0x7fffffff;
+        }
+        if (n_plan >= 0 || e > 0) {
+            __syncthreads();  // the previous segment is done with desc_s / rows_s
+            if (tid < 32) desc_s[tid] = reinterpret_cast<const int32_t *>(p.desc + li)[tid];
+            __syncthreads();
+        }
         const int start = desc_s[0], len = desc_s[1], a = desc_s[2];
         if (len == 0) break;  // descriptors are compacted: the list ends here
         const int r = p.ranks ? p.ranks[a] : p.r_max;
-        // Segments of long adapter groups (flagged by prepare) belong to the
-        // tensor-core kernel when it can take their rank.
-        if (len < p.min_len || (p.split_tc && (desc_s[3] & LORA_DESC_TC_FLAG) && tc_rank_ok(r))) continue;
-        if (r == 0 && MODE != kShrink) continue;  // rank 0: nothing to add
+        if (!seg_taken(len, desc_s[3], r)) continue;
         if (r < 0 || r > p.r_max) {
             if (q == 0 && tid == 0) raise_deverr(p.counts, LORA_DEVERR_RANK);
             continue;
@@ -178,7 +304,8 @@ __global__ void __launch_bounds__(kCcThreads, 1)
         const int rvp = next_pow2(rv > 0 ? rv : 1);
         const int njg = (r + 3) / 4;
 
-        for (int t0 = 0; t0 < len; t0 += RT) {
+        for (int tt = tb; tt < te && tt * RT < len; ++tt) {
+            const int t0 = tt * RT;
             const int R = min(RT, len - t0);
             const int nrb = (R + 3) / 4, Rp = nrb * 4;
             if (t0 > 0) __syncthreads();  // the previous tile is done with rows_s
@@ -601,6 +728,7 @@ static CcGeom cc_geometry(int r_max, int cluster) {
     g.off_slots = take(256 * 16 * 4);
     g.off_recv = take(cluster * g.RT * g.HP * 4);
     g.off_hfull = take(g.RT * g.HP * 4);
+    g.off_plan = take((kPlanMaxTiles + 4) * 4);
     g.off_ring = o;
     const int budget = 225 * 1024;
     g.stage_bytes = ((budget - o) / kCcStages) & ~127;
