@@ -83,9 +83,10 @@ typedef int lora_status_t;
 #define LORA_BF16 1
 
 /* Path selection for lora_delta / lora_shrink / lora_expand. */
-#define LORA_PATH_AUTO 0      /* groups with >= tc_min_rows rows use tensor cores (bf16) */
-#define LORA_PATH_CUDA_CORE 1 /* every segment on CUDA-core dot products */
-#define LORA_PATH_TENSOR 2    /* every segment on tcgen05 tensor cores (bf16 only) */
+#define LORA_PATH_AUTO 0      /* groups with >= tc_min_rows rows use the tcgen05 kernel (bf16) */
+#define LORA_PATH_CUDA_CORE 1 /* every segment on the small-segment kernel: clusters of CTAs,
+                                 warp-level bf16 tensor-core tiles (fp32: CUDA-core FMAs) */
+#define LORA_PATH_TENSOR 2    /* every segment on the tcgen05 kernel (bf16 only) */
 
 /* Largest supported sizes. */
 #define LORA_MAX_TOKENS (1 << 24)
