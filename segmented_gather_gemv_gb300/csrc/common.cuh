@@ -43,6 +43,29 @@ static inline const int2 *share_table(const int32_t *counts) {
     return reinterpret_cast<const int2 *>(reinterpret_cast<const char *>(counts) + align256(LORA_NUM_COUNTS * 4));
 }
 
+// prepare's outputs (descriptors, small and tensor-core lists, indptr,
+// lengths, adapters, tensor-core indptr, sorted rows) lie in one block whose
+// byte layout is the same in the workspace and in prepare's shared-memory
+// staging, so that the staged outputs leave in one contiguous copy.
+struct OutLayout {
+    size_t rec, small, tc, indptr, lens, widx, tcptr, sorted, total;  // bytes, multiples of 16
+};
+__host__ __device__ inline OutLayout out_layout(int64_t ms, int64_t M) {
+    OutLayout O{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o += (bytes + 15) & ~size_t(15); return at; };
+    O.rec = take((size_t)ms * 128);
+    O.small = take((size_t)ms * 16);
+    O.tc = take((size_t)ms * 16);
+    O.indptr = take(((size_t)ms + 1) * 4);
+    O.lens = take((size_t)ms * 4);
+    O.widx = take((size_t)ms * 4);
+    O.tcptr = take(((size_t)ms + 1) * 4);
+    O.sorted = take((M > 0 ? (size_t)M : 1) * 4);
+    O.total = o;
+    return O;
+}
+
 static inline WsLayout ws_layout(int32_t M, int32_t n, int32_t chunk) {
     WsLayout L{};
     int64_t ms = max_segments(M, n, chunk);
@@ -51,16 +74,17 @@ static inline WsLayout ws_layout(int32_t M, int32_t n, int32_t chunk) {
     if (gm < 1) gm = 1;
     L.max_segs = (int32_t)ms;
     L.g_max = (int32_t)gm;
-    size_t o = 0;
+    const OutLayout O = out_layout(ms, M);
+    L.rec = O.rec;
+    L.small = O.small;
+    L.tc = O.tc;
+    L.indptr = O.indptr;
+    L.lens = O.lens;
+    L.widx = O.widx;
+    L.tcptr = O.tcptr;
+    L.sorted = O.sorted;
+    size_t o = align256(O.total);
     auto take = [&](size_t ints) { size_t at = o; o = align256(o + ints * 4); return at; };
-    L.sorted = take(M > 0 ? (size_t)M : 1);
-    L.indptr = take((size_t)ms + 1);
-    L.lens = take((size_t)ms);
-    L.widx = take((size_t)ms);
-    L.rec = take((size_t)ms * 32);
-    L.small = take((size_t)ms * 4);
-    L.tc = take((size_t)ms * 4);
-    L.tcptr = take((size_t)ms + 1);
     L.counts = take(LORA_NUM_COUNTS);
     L.shares = take(2 * ((size_t)kMaxShareGrid + 1));
     L.first_pos = take((size_t)n);

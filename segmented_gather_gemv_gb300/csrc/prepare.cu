@@ -42,7 +42,8 @@ struct PrepArgs {
     // shared-memory placement (byte offsets into dynamic shared memory, -1 = global)
     int32_t off_ids, off_adapters, off_groups, off_hist;
     int32_t off_bits;   // first-appearance bitmap and its word prefix, or -1
-    int32_t off_stage;  // shared-memory copies of every phase 4-5 output, or -1
+    int32_t off_stage;  // shared-memory copy of the output block (phases 4-5), or -1
+    void *out_block;    // the workspace's output block (layout out_layout)
     int2 *shares;       // tensor-core CTA shares: boundary b = {first row, segment}, b <= share_grid
     int32_t share_grid;
 };
@@ -268,19 +269,18 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
     SegDesc *o_desc = p.desc;
     int4 *o_small = p.small, *o_tc = p.tc;
     int32_t *o_indptr = p.indptr, *o_lens = p.lens, *o_widx = p.widx, *o_tcptr = p.tcptr, *o_sorted = p.sorted;
+    const OutLayout O = out_layout(p.max_segs, p.M);
     if (stage) {
+        // the workspace's output block, byte for byte
         unsigned char *b = smem_raw + p.off_stage;
-        o_desc = reinterpret_cast<SegDesc *>(b);
-        b += size_t(p.max_segs) * sizeof(SegDesc);
-        o_small = reinterpret_cast<int4 *>(b);
-        b += size_t(p.max_segs) * 16;
-        o_tc = reinterpret_cast<int4 *>(b);
-        b += size_t(p.max_segs) * 16;
-        o_indptr = reinterpret_cast<int32_t *>(b);
-        o_lens = o_indptr + p.max_segs + 1;
-        o_widx = o_lens + p.max_segs;
-        o_tcptr = o_widx + p.max_segs;
-        o_sorted = o_tcptr + p.max_segs + 1;
+        o_desc = reinterpret_cast<SegDesc *>(b + O.rec);
+        o_small = reinterpret_cast<int4 *>(b + O.small);
+        o_tc = reinterpret_cast<int4 *>(b + O.tc);
+        o_indptr = reinterpret_cast<int32_t *>(b + O.indptr);
+        o_lens = reinterpret_cast<int32_t *>(b + O.lens);
+        o_widx = reinterpret_cast<int32_t *>(b + O.widx);
+        o_tcptr = reinterpret_cast<int32_t *>(b + O.tcptr);
+        o_sorted = reinterpret_cast<int32_t *>(b + O.sorted);
     }
     if (early && !stage) {
         griddep_wait();
@@ -439,19 +439,12 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
         __syncthreads();
         griddep_wait();
         griddep_launch_dependents();
-        const int4 *dsrc = reinterpret_cast<const int4 *>(o_desc);
-        int4 *ddst = reinterpret_cast<int4 *>(p.desc);
-        const int nd = p.max_segs * int(sizeof(SegDesc) / 16);
-        for (int k = tid; k < nd; k += nthr) ddst[k] = dsrc[k];
-        for (int k = tid; k < n_small; k += nthr) p.small[k] = o_small[k];
-        for (int k = tid; k < n_tc; k += nthr) p.tc[k] = o_tc[k];
-        for (int k = tid; k <= S; k += nthr) p.indptr[k] = o_indptr[k];
-        for (int k = tid; k < S; k += nthr) {
-            p.lens[k] = o_lens[k];
-            p.widx[k] = o_widx[k];
-        }
-        for (int k = tid; k <= n_tc; k += nthr) p.tcptr[k] = o_tcptr[k];
-        for (int k = tid; k < ACT; k += nthr) p.sorted[k] = o_sorted[k];
+        // one contiguous copy of the output block (entries past each
+        // array's valid length go along unread)
+        const int4 *src = reinterpret_cast<const int4 *>(smem_raw + p.off_stage);
+        int4 *dst = reinterpret_cast<int4 *>(p.out_block);
+        const int n16 = int(O.total / 16);
+        for (int k = tid; k < n16; k += nthr) dst[k] = src[k];
     }
 
     // Shares of the tensor-core row space for a grid of share_grid CTAs,
@@ -521,6 +514,7 @@ cudaError_t launch_prepare(const int32_t *ids, int32_t M, int32_t n, int32_t chu
     p.lens = at(L.lens);
     p.widx = at(L.widx);
     p.desc = reinterpret_cast<SegDesc *>(ws + L.rec);
+    p.out_block = ws;  // the output block starts the workspace
     p.max_segs = L.max_segs;
     p.small = reinterpret_cast<int4 *>(ws + L.small);
     p.tc = reinterpret_cast<int4 *>(ws + L.tc);
@@ -552,7 +546,7 @@ cudaError_t launch_prepare(const int32_t *ids, int32_t M, int32_t n, int32_t chu
     p.off_adapters = place(size_t(3) * n * 4);
     p.off_bits = M <= 65536 ? place(size_t(2) * ((M + 31) / 32) * 4) : -1;
     p.off_ids = place(size_t(M) * 4);
-    p.off_stage = place(size_t(L.max_segs) * (sizeof(SegDesc) + 32 + 16) + 8 + size_t(M) * 4);
+    p.off_stage = place(out_layout(L.max_segs, M).total);
 
     static DeviceOnce configured;
     cudaError_t e = configured.run([] {
