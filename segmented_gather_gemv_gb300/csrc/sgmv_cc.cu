@@ -38,6 +38,8 @@
 // live across all K chunks; lanes sharing a block are reduced once, at the
 // end.  Expand -- every thread owns two adjacent output columns and all rows
 // of the tile.
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace lora {
@@ -598,55 +600,70 @@ __global__ void __launch_bounds__(kCcThreads, 1)
                         uint32_t *yst = reinterpret_cast<uint32_t *>(const_cast<unsigned char *>(sb));
                         const unsigned char *Bb = reinterpret_cast<const unsigned char *>(Bs);
                         constexpr int kW = kCcThreads / 32;
-                        for (int jt0 = warp; jt0 < nn; jt0 += 4 * kW) {
-                            // column tiles jt0, jt0 + kW, ... (four at a time)
-                            float d[2][4][4];
+                        // swizzle of B row n: chunk c sits at c ^ ((n >> bsh) & bmask)
+                        const int bsh = rvp >= 8 ? 0 : (rvp == 1 ? 3 : rvp == 2 ? 2 : 1);
+                        const int bmask = rvp >= 8 ? 7 : rvp - 1;
+                        // NB column tiles per warp at a time (eight when the
+                        // tile has at most 16 rows), MT row tiles of 16
+                        auto expand_tiles = [&](auto nb_c, auto mt_c) {
+                            constexpr int NB = decltype(nb_c)::value, MT = decltype(mt_c)::value;
+                            for (int jt0 = warp; jt0 < nn; jt0 += NB * kW) {
+                                float d[MT][NB][4];
 #pragma unroll
-                            for (int mi = 0; mi < 2; ++mi)
+                                for (int mi = 0; mi < MT; ++mi)
 #pragma unroll
-                                for (int u = 0; u < 4; ++u) d[mi][u][0] = d[mi][u][1] = d[mi][u][2] = d[mi][u][3] = 0.f;
-                            for (int st = 0; st < kr; ++st) {
-                                uint32_t bq0[4], bq1[4];
+                                    for (int u = 0; u < NB; ++u) d[mi][u][0] = d[mi][u][1] = d[mi][u][2] = d[mi][u][3] = 0.f;
+                                uint32_t boff[NB];
+                                int bsw[NB];
 #pragma unroll
-                                for (int u = 0; u < 4; ++u) {
+                                for (int u = 0; u < NB; ++u) {
                                     const int n = (jt0 + u * kW) * 8 + gq;
-                                    const bool in = jt0 + u * kW < nn;
-                                    bq0[u] = in && 2 * st < rv ? lds_u32(Bb + (size_t)(n * rvp + b_swizzle(n, 2 * st, rvp)) * 16 + tq * 4) : 0u;
-                                    bq1[u] = in && 2 * st + 1 < rv ? lds_u32(Bb + (size_t)(n * rvp + b_swizzle(n, 2 * st + 1, rvp)) * 16 + tq * 4) : 0u;
+                                    boff[u] = (uint32_t)(n * rvp) * 16u + (uint32_t)tq * 4u;
+                                    bsw[u] = (n >> bsh) & bmask;
                                 }
+                                for (int st = 0; st < kr; ++st) {
+                                    const int c0 = 2 * st, c1 = c0 + 1;
+                                    uint32_t bq0[NB], bq1[NB];
 #pragma unroll
-                                for (int mi = 0; mi < 2; ++mi) {
-                                    if (mi < mt) {
+                                    for (int u = 0; u < NB; ++u) {
+                                        const bool in = jt0 + u * kW < nn;
+                                        bq0[u] = in && c0 < rv ? lds_u32(Bb + boff[u] + ((uint32_t)(c0 ^ bsw[u]) << 4)) : 0u;
+                                        bq1[u] = in && c1 < rv ? lds_u32(Bb + boff[u] + ((uint32_t)(c1 ^ bsw[u]) << 4)) : 0u;
+                                    }
+#pragma unroll
+                                    for (int mi = 0; mi < MT; ++mi) {
                                         const uint4 av = *reinterpret_cast<const uint4 *>(hfrag + ((mi * kr + st) * 32 + lane) * 4);
                                         const uint32_t af[4] = {av.x, av.y, av.z, av.w};
 #pragma unroll
-                                        for (int u = 0; u < 4; ++u) mma_16x8x16_bf16(d[mi][u], af, bq0[u], bq1[u]);
+                                        for (int u = 0; u < NB; ++u) mma_16x8x16_bf16(d[mi][u], af, bq0[u], bq1[u]);
+                                    }
+                                }
+#pragma unroll
+                                for (int u = 0; u < NB; ++u) {
+                                    const int jt = jt0 + u * kW;
+                                    if (jt < nn) {
+#pragma unroll
+                                        for (int mi = 0; mi < MT; ++mi) {
+                                            const int row0 = mi * 16 + gq, row1 = row0 + 8;
+                                            if (row0 < R) {
+                                                const int at = row0 * ystride + jt * 4 + tq;
+                                                const float2 yv = E::pair_to_f32(yst[at]);
+                                                const __nv_bfloat162 o = __floats2bfloat162_rn(yv.x + d[mi][u][0], yv.y + d[mi][u][1]);
+                                                yst[at] = *reinterpret_cast<const uint32_t *>(&o);
+                                            }
+                                            if (row1 < R) {
+                                                const int at = row1 * ystride + jt * 4 + tq;
+                                                const float2 yv = E::pair_to_f32(yst[at]);
+                                                const __nv_bfloat162 o = __floats2bfloat162_rn(yv.x + d[mi][u][2], yv.y + d[mi][u][3]);
+                                                yst[at] = *reinterpret_cast<const uint32_t *>(&o);
+                                            }
+                                        }
                                     }
                                 }
                             }
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const int jt = jt0 + u * kW;
-                                if (jt < nn) {
-#pragma unroll
-                                    for (int mi = 0; mi < 2; ++mi) {
-                                        const int row0 = mi * 16 + gq, row1 = row0 + 8;
-                                        if (row0 < R) {
-                                            const int at = row0 * ystride + jt * 4 + tq;
-                                            const float2 yv = E::pair_to_f32(yst[at]);
-                                            const __nv_bfloat162 o = __floats2bfloat162_rn(yv.x + d[mi][u][0], yv.y + d[mi][u][1]);
-                                            yst[at] = *reinterpret_cast<const uint32_t *>(&o);
-                                        }
-                                        if (row1 < R) {
-                                            const int at = row1 * ystride + jt * 4 + tq;
-                                            const float2 yv = E::pair_to_f32(yst[at]);
-                                            const __nv_bfloat162 o = __floats2bfloat162_rn(yv.x + d[mi][u][2], yv.y + d[mi][u][3]);
-                                            yst[at] = *reinterpret_cast<const uint32_t *>(&o);
-                                        }
-                                    }
-                                }
-                            }
-                        }
+                        };
+                        if (mt == 1) expand_tiles(std::integral_constant<int, 8>{}, std::integral_constant<int, 1>{});
+                        else expand_tiles(std::integral_constant<int, 4>{}, std::integral_constant<int, 2>{});
                         __syncthreads();
                         for (int row = warp; row < R; row += kCcThreads / 32) {
                             T *yrow = static_cast<T *>(p.y) + (int64_t)rows_s[row] * p.ldy;
