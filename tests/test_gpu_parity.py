@@ -221,6 +221,43 @@ def test_rank_out_of_range_sets_device_error(B):
     assert np.array_equal(y[bad], w.y[bad].astype(np.float64))
 
 
+# Per-adapter ranks with more segments than clusters: the small-segment
+# kernel deals its tiles to the clusters by estimated cost (the work plan).
+PLAN_CASES = [
+    dict(M=600, d_in=4096, d_outs=[2048], n_pool=120, r_max=64, ranks=[8, 16, 32, 64]),       # one tile each
+    dict(M=3200, d_in=2048, d_outs=[1024], n_pool=80, r_max=64, ranks=[8, 16, 32, 64], run_len=40),  # several tiles each
+    dict(M=700, d_in=2048, d_outs=[1536, 512], n_pool=90, r_max=32, ranks=[8, 16, 24, 32], chunk_size=7,
+         skip_frac=0.1, per_adapter_scale=True),                                              # chunks, slices, skips
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("ci", range(len(PLAN_CASES)))
+def test_work_plan_mixed_ranks(B, dtype, ci):
+    w = wl.random_batch(seed=500 + ci, dtype=dtype, **PLAN_CASES[ci])
+    y, batch = _run_delta(B, w, path=1)
+    _assert_delta(w, y)
+    c = batch.counts()
+    assert c["device_error"] == 0 and c["num_segs"] > 38  # more segments than clusters of 4 on 152 SMs
+
+
+def test_work_plan_rank_out_of_range(B):
+    # a bad rank inside a planned batch: flagged, its rows untouched, the rest exact
+    w = wl.random_batch(seed=510, M=600, d_in=4096, d_outs=[2048], n_pool=120, r_max=64,
+                        ranks=[8, 16, 32, 64], dtype="bf16")
+    bad_a = int(w.ids[0])
+    w.ranks = w.ranks.copy()
+    w.ranks[bad_a] = 99
+    y, batch = _run_delta(B, w, path=1)
+    assert batch.counts()["device_error"] & B.DEVERR_RANK
+    bad = w.ids == bad_a
+    assert np.array_equal(y[bad], w.y[bad].astype(np.float64))
+    good = wl.Workload(**{**w.__dict__})
+    good.ranks = w.ranks.copy()
+    good.ranks[bad_a] = 0  # the oracle's view: that adapter adds nothing
+    _assert_delta(good, y)
+
+
 def test_empty_and_all_skipped(B):
     for ids in (np.zeros(0, np.int32), np.full(9, -1, np.int32)):
         w = wl.random_batch(seed=302, M=len(ids), d_in=64, d_outs=[64], n_pool=3, r_max=8, dtype="bf16")
