@@ -1,4 +1,6 @@
-// sgmv_cc.cu -- CUDA-core SGMV kernel for small segments (decode).
+// sgmv_cc.cu -- SGMV kernel for small segments (decode): clusters of CTAs,
+// warp-level tensor-core tiles for bf16 (the "CUDA-core" path of the API,
+// where fp32 inputs run on CUDA-core FMAs).
 //
 // Each segment (rows that share one adapter) is handled by one thread-block
 // cluster of CL CTAs ("vLLM-Ascend LoRA" article, section 3.3: the rows of
@@ -29,9 +31,9 @@
 // into 16 x 8 tiles; each warp takes one tile and every (16 / tiles)-th K
 // step, with four accumulators so that four products are in flight; the
 // warps' partial tiles are summed in warp order.  Expand -- h (scaled fp32)
-// is rounded once to bf16 in fragment order; each warp takes four 8-column
-// tiles at a time, adds y in the stage and the stage leaves in 16-byte row
-// pieces.  A tile of a few rows costs a handful of instructions per warp,
+// is rounded once to bf16 in fragment order; each warp takes eight 8-column
+// tiles at a time (four when the tile has more than 16 rows), adds y in the
+// stage and the stage leaves in 16-byte row pieces.  A tile of a few rows costs a handful of instructions per warp,
 // with no tensor-memory allocation or commit round trip on the path.
 // fp32 inputs (packed FFMA2, exact fp32 products): shrink -- every thread
 // owns a 4-row x 4-rank block of h and strides over K with its accumulators
@@ -141,7 +143,7 @@ __global__ void __launch_bounds__(kCcThreads, 1)
     extern __shared__ __align__(128) unsigned char smem[];
     int32_t *desc_s = reinterpret_cast<int32_t *>(smem + g.off_desc);  // [32]
     int32_t *rows_s = reinterpret_cast<int32_t *>(smem + g.off_rows);  // [RT]
-    float *slots = reinterpret_cast<float *>(smem + g.off_slots);      // [warp][16]
+    float *slots = reinterpret_cast<float *>(smem + g.off_slots);      // 16 KB: fp32 block totals, bf16 partial tiles + h fragments
     float *recv = reinterpret_cast<float *>(smem + g.off_recv);        // [CL][RT][HP]
     float *h_full = reinterpret_cast<float *>(smem + g.off_hfull);     // [RT][HP]
     unsigned char *ring = smem + g.off_ring;
