@@ -64,6 +64,10 @@ def _load():
             lib.oracle_prepare_batch.argtypes = [
                 i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                 i32p, i32p, i32p, i32p, i32p]
+            lib.oracle_prepare_batch_ordered.restype = ctypes.c_int
+            lib.oracle_prepare_batch_ordered.argtypes = [
+                i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                i32p, i32p, i32p, i32p, i32p]
             for fn in (lib.oracle_shrink, lib.oracle_expand, lib.oracle_delta):
                 fn.restype = ctypes.c_int
             _lib = lib
@@ -87,8 +91,9 @@ def _i32(a) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
 
 
-def prepare_batch(ids, n_adapters: int, chunk_size: int = 0) -> dict:
-    """Segment metadata for a batch of per-token adapter ids.
+def prepare_batch(ids, n_adapters: int, chunk_size: int = 0, ascending: bool = False) -> dict:
+    """Segment metadata for a batch of per-token adapter ids: groups in
+    first-appearance order, or by increasing adapter id with ``ascending``.
 
     Returns a dict with ``sorted_token_ids``, ``seg_indptr``, ``seg_lens``,
     ``weight_indices`` (trimmed to their true lengths) and ``num_segs``,
@@ -103,8 +108,8 @@ def prepare_batch(ids, n_adapters: int, chunk_size: int = 0) -> dict:
     lens = np.zeros(cap, np.int32)
     widx = np.zeros(cap, np.int32)
     counts = np.zeros(3, np.int32)
-    rc = lib.oracle_prepare_batch(
-        _ptr(ids, ctypes.c_int32), M, int(n_adapters), int(chunk_size),
+    rc = lib.oracle_prepare_batch_ordered(
+        _ptr(ids, ctypes.c_int32), M, int(n_adapters), int(chunk_size), 1 if ascending else 0,
         _ptr(sorted_ids, ctypes.c_int32), _ptr(indptr, ctypes.c_int32),
         _ptr(lens, ctypes.c_int32), _ptr(widx, ctypes.c_int32),
         _ptr(counts, ctypes.c_int32))

@@ -32,7 +32,9 @@
  *     keep ascending token order, and each group may be cut into fixed-size
  *     chunks, each chunk a segment of its own (same page, section 代码:
  *     prepare_lora_batch regroups tokens by adapter, then cuts the
- *     regrouped stream into chunks).
+ *     regrouped stream into chunks).  Optionally the groups come by
+ *     increasing adapter id instead (the same "regroup by adapter" read as
+ *     a sort by id).
  *
  * Numerics: every input element is read as stored (fp32 storage; bf16
  * inputs are exactly representable in fp32) and widened to double; every
@@ -65,12 +67,13 @@ static int id_valid(int32_t id, int32_t n_adapters)
  * Buffers must hold M entries (seg_indptr M + 1); with chunking a group of
  * L rows yields ceil(L / chunk_size) segments, never more than L.
  */
-int oracle_prepare_batch(const int32_t *ids, int32_t M, int32_t n_adapters,
-                         int32_t chunk_size, int32_t *sorted_token_ids,
-                         int32_t *seg_indptr, int32_t *seg_lens,
-                         int32_t *weight_indices, int32_t *counts)
+int oracle_prepare_batch_ordered(const int32_t *ids, int32_t M, int32_t n_adapters,
+                                 int32_t chunk_size, int32_t ascending,
+                                 int32_t *sorted_token_ids, int32_t *seg_indptr,
+                                 int32_t *seg_lens, int32_t *weight_indices,
+                                 int32_t *counts)
 {
-    if (M < 0 || n_adapters < 0 || chunk_size < 0)
+    if (M < 0 || n_adapters < 0 || chunk_size < 0 || (ascending != 0 && ascending != 1))
         return ORACLE_ERR;
     char *seen = (char *)calloc((size_t)(n_adapters > 0 ? n_adapters : 1), 1);
     int32_t *order = (int32_t *)malloc(sizeof(int32_t) * (size_t)(M > 0 ? M : 1));
@@ -93,6 +96,14 @@ int oracle_prepare_batch(const int32_t *ids, int32_t M, int32_t n_adapters,
             seen[a] = 1;
             order[n_groups++] = a;
         }
+    }
+    /* Ascending order (the page's "regroup tokens by adapter" read as a sort
+     * by adapter id): the present adapters by increasing id instead. */
+    if (ascending) {
+        n_groups = 0;
+        for (int32_t a = 0; a < n_adapters; ++a)
+            if (seen[a])
+                order[n_groups++] = a;
     }
     /* Each group lists its token rows in ascending order, then is cut into
      * chunks of chunk_size rows (the last one may be shorter). */
@@ -125,6 +136,15 @@ int oracle_prepare_batch(const int32_t *ids, int32_t M, int32_t n_adapters,
     free(seen);
     free(order);
     return ORACLE_OK;
+}
+
+int oracle_prepare_batch(const int32_t *ids, int32_t M, int32_t n_adapters,
+                         int32_t chunk_size, int32_t *sorted_token_ids,
+                         int32_t *seg_indptr, int32_t *seg_lens,
+                         int32_t *weight_indices, int32_t *counts)
+{
+    return oracle_prepare_batch_ordered(ids, M, n_adapters, chunk_size, 0, sorted_token_ids,
+                                        seg_indptr, seg_lens, weight_indices, counts);
 }
 
 /* Rank used by adapter a: its own rank when a rank table is given, else the

@@ -93,6 +93,43 @@ def test_grouping_brute_force(seed, chunk):
             assert out["seg_lens"][s] <= chunk
 
 
+def test_ascending_order_punica_ids():
+    # the "III.Punica" page's ids 2 2 2 5 5 1 1, grouped by increasing adapter
+    # id instead of first appearance: adapter 1 (rows 5, 6), then 2, then 5
+    out = oracle.prepare_batch([2, 2, 2, 5, 5, 1, 1], 6, ascending=True)
+    assert out["sorted_token_ids"].tolist() == [5, 6, 0, 1, 2, 3, 4]
+    assert out["seg_indptr"].tolist() == [0, 2, 5, 7]
+    assert out["weight_indices"].tolist() == [1, 2, 5]
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("chunk", [0, 1, 3, 64])
+def test_ascending_order_is_a_stable_sort(seed, chunk):
+    # ascending grouping = numpy's stable sort of the valid rows by id, each
+    # group then cut into chunks
+    rng = np.random.default_rng(100 + seed)
+    M = int(rng.integers(0, 300))
+    n = int(rng.integers(1, 40))
+    ids = rng.integers(-1, n + 3, size=M).astype(np.int32)
+    out = oracle.prepare_batch(ids, n, chunk, ascending=True)
+    valid = np.nonzero((ids >= 0) & (ids < n))[0]
+    rows = valid[np.argsort(ids[valid], kind="stable")]
+    assert out["sorted_token_ids"].tolist() == rows.tolist()
+    segs = []
+    pos = 0
+    for a in np.unique(ids[valid]):
+        L = int((ids[valid] == a).sum())
+        step = chunk if chunk else L
+        for c in range(0, L, step):
+            segs.append((pos + c, min(step, L - c), int(a)))
+        pos += L
+    assert [(int(s), int(l), int(a)) for s, l, a in zip(out["seg_indptr"][:-1], out["seg_lens"], out["weight_indices"])] == segs
+    # the same segments as first-appearance order, only reordered
+    fa = oracle.prepare_batch(ids, n, chunk)
+    assert sorted(fa["weight_indices"].tolist()) == sorted(out["weight_indices"].tolist())
+    assert out["num_segs"] == fa["num_segs"] and out["num_active"] == fa["num_active"]
+
+
 def test_grouping_degenerate_cases():
     assert oracle.prepare_batch([], 5)["num_segs"] == 0
     out = oracle.prepare_batch([-1, -1, 9], 5)
