@@ -213,6 +213,25 @@ lora_status_t lora_prepare_batch(const int32_t *ids, int32_t M, int32_t n_adapte
                                  void *workspace, size_t workspace_bytes,
                                  lora_batch_t *batch, void *stream);
 
+/* Group orders for lora_prepare_batch_ordered. */
+#define LORA_ORDER_FIRST_APPEARANCE 0 /* the default: groups as their adapter first occurs */
+#define LORA_ORDER_ASCENDING 1        /* groups by increasing adapter id */
+
+/*
+ * lora_prepare_batch with a choice of group order.  "III.Punica:
+ * Multi-Tenant LoRA Serving", section 代码, says only that prepare_lora_batch
+ * regroups the tokens by adapter; LORA_ORDER_ASCENDING reads that as a sort
+ * by adapter id (ids 2 2 2 5 5 1 1 give seg_indptr = [0, 2, 5, 7] and
+ * weight_indices = [1, 2, 5]).  Rows inside a group keep ascending row
+ * order either way, and the segments, chunks and every other output are
+ * those of the same groups in the other order.  An order other than the two
+ * returns LORA_ERR_INVALID; everything else as for lora_prepare_batch.
+ */
+lora_status_t lora_prepare_batch_ordered(const int32_t *ids, int32_t M, int32_t n_adapters,
+                                         int32_t chunk_size, int32_t tc_min_rows, int32_t order,
+                                         void *workspace, size_t workspace_bytes,
+                                         lora_batch_t *batch, void *stream);
+
 /*
  * lora_prepare_batch with no caller workspace and no allocation: the
  * metadata goes to a device array that this library owns

@@ -7,7 +7,8 @@ or if a call returns an error status; there is no fallback.
 
 Calls (same names as the C ABI):
   lora_workspace_size(M, n_adapters, chunk_size) -> int
-  lora_prepare_batch(ids, n_adapters, chunk_size=0, tc_min_rows=0) -> Batch
+  lora_prepare_batch(ids, n_adapters, chunk_size=0, tc_min_rows=0, order=0) -> Batch
+    (calls lora_prepare_batch_ordered)
   lora_prepare_batch_static(ids, n_adapters, chunk_size=0, tc_min_rows=0) -> Batch
   lora_shrink(batch, x, A_pool, h=None, ranks=None, path=PATH_AUTO) -> h
   lora_expand(batch, h, B_pools, y, scale=1.0, adapter_scale=None,
@@ -33,6 +34,7 @@ LORA_ERR_WORKSPACE = -3
 LORA_ERR_CUDA = -4
 F32, BF16 = 0, 1
 PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR = 0, 1, 2
+LORA_ORDER_FIRST_APPEARANCE, LORA_ORDER_ASCENDING = 0, 1
 MAX_SLICES = 4
 COUNT_NAMES = ("num_segs", "num_active", "num_invalid", "num_small_segs",
                "num_tc_segs", "tc_rows", "device_error", "num_groups")
@@ -89,6 +91,9 @@ def lib() -> ctypes.CDLL:
             L.lora_prepare_batch.restype = ctypes.c_int
             L.lora_prepare_batch.argtypes = [vp, i32, i32, i32, i32, vp, ctypes.c_size_t,
                                              ctypes.POINTER(_Batch), vp]
+            L.lora_prepare_batch_ordered.restype = ctypes.c_int
+            L.lora_prepare_batch_ordered.argtypes = [vp, i32, i32, i32, i32, i32, vp, ctypes.c_size_t,
+                                                     ctypes.POINTER(_Batch), vp]
             L.lora_prepare_batch_static.restype = ctypes.c_int
             L.lora_prepare_batch_static.argtypes = [vp, i32, i32, i32, i32, ctypes.POINTER(_Batch), vp]
             L.lora_shrink.restype = ctypes.c_int
@@ -228,8 +233,10 @@ def lora_workspace_size(M: int, n_adapters: int, chunk_size: int = 0) -> int:
 
 def lora_prepare_batch(ids: torch.Tensor, n_adapters: int, chunk_size: int = 0,
                        tc_min_rows: int = 0, workspace: Optional[torch.Tensor] = None,
-                       stream=None) -> Batch:
-    """Build segment metadata on the device for per-token adapter ids."""
+                       stream=None, order: int = 0) -> Batch:
+    """Build segment metadata on the device for per-token adapter ids;
+    ``order`` is LORA_ORDER_FIRST_APPEARANCE (default) or
+    LORA_ORDER_ASCENDING."""
     if ids.dim() != 1:
         raise ValueError("ids must be 1-D")
     M = ids.shape[0]
@@ -242,9 +249,10 @@ def lora_prepare_batch(ids: torch.Tensor, n_adapters: int, chunk_size: int = 0,
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=ids.device if M else "cuda")
     raw = _Batch()
-    _check(lib().lora_prepare_batch(ids_ptr, M, int(n_adapters), int(chunk_size), int(tc_min_rows),
-                                    workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                                    ctypes.byref(raw), _stream(stream)))
+    _check(lib().lora_prepare_batch_ordered(ids_ptr, M, int(n_adapters), int(chunk_size), int(tc_min_rows),
+                                            int(order), workspace.data_ptr(),
+                                            workspace.numel() * workspace.element_size(),
+                                            ctypes.byref(raw), _stream(stream)))
     return Batch(raw, workspace, ids)
 
 

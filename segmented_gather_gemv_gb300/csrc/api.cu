@@ -10,7 +10,7 @@
 #include "common.cuh"
 
 namespace lora {
-cudaError_t launch_prepare(const int32_t *ids, int32_t M, int32_t n, int32_t chunk, int32_t tc_min,
+cudaError_t launch_prepare(const int32_t *ids, int32_t M, int32_t n, int32_t chunk, int32_t tc_min, bool ascending,
                            int32_t share_grid, char *ws, const WsLayout &L, lora_batch_t *b, cudaStream_t stream);
 cudaError_t launch_cc(const DeltaArgs &p, int dtype, int mode, int cluster, int sms, cudaStream_t stream);
 int cc_cluster_size(int d_in, int d_out);
@@ -232,7 +232,16 @@ size_t lora_workspace_size(int32_t M, int32_t n_adapters, int32_t chunk_size) {
 lora_status_t lora_prepare_batch(const int32_t *ids, int32_t M, int32_t n_adapters, int32_t chunk_size,
                                  int32_t tc_min_rows, void *workspace, size_t workspace_bytes,
                                  lora_batch_t *batch, void *stream) {
+    return lora_prepare_batch_ordered(ids, M, n_adapters, chunk_size, tc_min_rows, LORA_ORDER_FIRST_APPEARANCE,
+                                      workspace, workspace_bytes, batch, stream);
+}
+
+lora_status_t lora_prepare_batch_ordered(const int32_t *ids, int32_t M, int32_t n_adapters, int32_t chunk_size,
+                                         int32_t tc_min_rows, int32_t order, void *workspace,
+                                         size_t workspace_bytes, lora_batch_t *batch, void *stream) {
     g_err[0] = 0;
+    if (order != LORA_ORDER_FIRST_APPEARANCE && order != LORA_ORDER_ASCENDING)
+        return fail(LORA_ERR_INVALID, "order %d is not a LORA_ORDER_* value", order);
     if (!batch) return fail(LORA_ERR_INVALID, "batch is NULL");
     if (M < 0 || M > LORA_MAX_TOKENS) return fail(LORA_ERR_INVALID, "M %d outside [0, %d]", M, LORA_MAX_TOKENS);
     if (n_adapters < 1) return fail(LORA_ERR_INVALID, "n_adapters %d < 1", n_adapters);
@@ -246,7 +255,8 @@ lora_status_t lora_prepare_batch(const int32_t *ids, int32_t M, int32_t n_adapte
     const int32_t tc_min = tc_min_rows > 0 ? tc_min_rows : kDefaultTcMinRows;
     lora_batch_t b{};
     const int grid = tc_grid(M);
-    cudaError_t e = launch_prepare(ids, M, n_adapters, chunk_size, tc_min, grid <= kMaxShareGrid ? grid : 0,
+    cudaError_t e = launch_prepare(ids, M, n_adapters, chunk_size, tc_min, order == LORA_ORDER_ASCENDING,
+                                   grid <= kMaxShareGrid ? grid : 0,
                                    static_cast<char *>(workspace), L, &b,
                                    static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "prepare launch failed: %s", cudaGetErrorString(e));

@@ -45,6 +45,7 @@ struct PrepArgs {
     int32_t off_stage;  // shared-memory copy of the output block (phases 4-5), or -1
     void *out_block;    // the workspace's output block (layout out_layout)
     int2 *shares;       // tensor-core CTA shares: boundary b = {first row, segment}, b <= share_grid
+    int32_t ascending;  // 1: groups by increasing adapter id, else by first appearance
     int32_t share_grid;
 };
 
@@ -169,9 +170,23 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
     if (lane == 0 && bad) atomicAdd(&s_invalid, bad);
     __syncthreads();
 
-    // Phase 2: group number by order of first appearance.
+    // Phase 2: group number by order of first appearance (or, on request,
+    // by increasing adapter id: the number of present adapters below it).
     int G = 0;
-    if (p.off_bits >= 0 && p.off_adapters >= 0) {
+    if (p.ascending) {
+        for (int base = 0; base < n; base += nthr) {
+            const int a = base + tid;
+            const int flag = a < n && acnt[a] > 0 ? 1 : 0;
+            int tot;
+            const int ex = block_excl_scan(flag, &tot, scan_ws);
+            if (flag) {
+                agroup[a] = G + ex;
+                gadapter[G + ex] = a;
+            }
+            G += tot;
+        }
+        __syncthreads();
+    } else if (p.off_bits >= 0 && p.off_adapters >= 0) {
         // The group of a present adapter a is the number of present adapters
         // that first appear before it: set one bit per first appearance, then
         // count the bits below first_pos[a] (word prefix sums + popcount).
@@ -499,7 +514,7 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
 constexpr size_t kPrepSmemMax = 200 * 1024;
 
 cudaError_t launch_prepare(const int32_t *ids, int32_t M, int32_t n, int32_t chunk,
-                           int32_t tc_min, int32_t share_grid, char *ws, const WsLayout &L,
+                           int32_t tc_min, bool ascending, int32_t share_grid, char *ws, const WsLayout &L,
                            lora_batch_t *b, cudaStream_t stream) {
     PrepArgs p{};
     p.ids = ids;
@@ -507,6 +522,7 @@ cudaError_t launch_prepare(const int32_t *ids, int32_t M, int32_t n, int32_t chu
     p.n = n;
     p.chunk = chunk;
     p.tc_min = tc_min;
+    p.ascending = ascending ? 1 : 0;
     p.gcap = L.g_max;
     auto at = [&](size_t off) { return reinterpret_cast<int32_t *>(ws + off); };
     p.sorted = at(L.sorted);

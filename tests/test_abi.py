@@ -40,6 +40,14 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, n), n
 
 
+def test_ordered_prepare_rejects_unknown_order(lib):
+    # checked on the host before anything is enqueued
+    from segmented_gather_gemv_gb300 import binding as B
+    raw = B._Batch()
+    st = lib.lora_prepare_batch_ordered(None, 4, 4, 0, 0, 7, None, ctypes.c_size_t(0), ctypes.byref(raw), None)
+    assert st == B.LORA_ERR_INVALID
+
+
 def test_workspace_size_host_only(lib):
     f = lib.lora_workspace_size
     f.restype = ctypes.c_size_t

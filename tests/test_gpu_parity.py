@@ -27,11 +27,12 @@ def B():
 
 # ----------------------------------------------------------------- grouping
 
-def _check_prepare(B, ids_np, n, chunk, tc_min=0):
+def _check_prepare(B, ids_np, n, chunk, tc_min=0, ascending=False):
     ids = torch.from_numpy(np.asarray(ids_np, np.int32)).cuda()
-    batch = B.lora_prepare_batch(ids, n, chunk, tc_min_rows=tc_min)
+    batch = B.lora_prepare_batch(ids, n, chunk, tc_min_rows=tc_min,
+                                 order=B.LORA_ORDER_ASCENDING if ascending else B.LORA_ORDER_FIRST_APPEARANCE)
     got = batch.arrays()
-    ref = oracle.prepare_batch(ids_np, n, chunk)
+    ref = oracle.prepare_batch(ids_np, n, chunk, ascending=ascending)
     assert got["num_segs"] == ref["num_segs"]
     assert got["num_active"] == ref["num_active"]
     assert got["num_invalid"] == ref["num_invalid"]
@@ -82,6 +83,45 @@ def test_prepare_bit_exact(B, seed, chunk, M, n):
     if seed == 2:
         ids[rng.choice(M, size=max(1, M // 10), replace=False)] = n + 5  # out of range
     _check_prepare(B, ids, n, chunk, tc_min=[0, 16, 64, 1][seed])
+
+
+def test_prepare_ascending_punica_ids(B):
+    batch = _check_prepare(B, [2, 2, 2, 5, 5, 1, 1], 6, 0, ascending=True)
+    assert batch.arrays()["seg_indptr"].tolist() == [0, 2, 5, 7]
+    assert batch.arrays()["weight_indices"].tolist() == [1, 2, 5]
+
+
+@pytest.mark.parametrize("seed", range(3))
+@pytest.mark.parametrize("chunk", [0, 3, 64])
+@pytest.mark.parametrize("M,n", [(7, 6), (256, 64), (2047, 100), (9000, 3000), (20000, 8)])
+def test_prepare_ascending_bit_exact(B, seed, chunk, M, n):
+    rng = np.random.default_rng(seed * 1000 + M + 7)
+    ids = rng.integers(-1, n, size=M).astype(np.int32)
+    if seed == 1:
+        ids = np.repeat(rng.integers(0, n, size=(M + 99) // 100), 100)[:M].astype(np.int32)
+    if seed == 2:
+        ids[rng.choice(M, size=max(1, M // 10), replace=False)] = n + 5  # out of range
+    _check_prepare(B, ids, n, chunk, tc_min=[0, 16, 64][seed], ascending=True)
+
+
+def test_prepare_ascending_large_pool(B):
+    rng = np.random.default_rng(8)
+    _check_prepare(B, rng.integers(0, 200000, size=30000).astype(np.int32), 200000, 0, ascending=True)
+
+
+@pytest.mark.parametrize("n_decode", [60, 400])
+def test_delta_ascending_order(B, n_decode):
+    # the delta does not depend on the group order; both kernels take rows
+    w = wl.mixed_serving(n_prefill_seq=3, prefill_rows=500, len_lo=64, len_hi=300, n_decode=n_decode,
+                         n_pool=24, r=16, d_in=1024, d_outs=(512, 256, 256))
+    d = to_dev(w)
+    batch = B.lora_prepare_batch(d["ids"], w.n_adapters, 0, order=B.LORA_ORDER_ASCENDING)
+    assert batch.arrays()["weight_indices"].tolist() == sorted(set(int(a) for a in w.ids if a >= 0))
+    y = d["y"]
+    B.lora_delta(batch, d["x"], d["A"], d["B"], y, scale=w.scale)
+    torch.cuda.synchronize()
+    _assert_delta(w, y.float().cpu().numpy().astype(np.float64))
+    assert batch.counts()["tc_rows"] > 0 and batch.counts()["device_error"] == 0
 
 
 def test_prepare_degenerate(B):
