@@ -339,7 +339,7 @@ def random_batch(seed: int, M: int, d_in: int, d_outs, n_pool: int, r_max: int,
                     adapter_scale=adapter_scale, ranks=rk, chunk_size=chunk_size)
 
 
-def north_star_workloads() -> dict:
+def serving_workloads() -> dict:
     """The five serving scenarios at full size (name -> factory)."""
     return {
         "page1_toy": page1_toy,

@@ -323,7 +323,7 @@ FULL = ["decode", "prefill", "prefill_chunk64", "mixed_rank_up", "mixed_rank_dow
 
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_scenarios(B, name):
-    w = wl.north_star_workloads()[name]()
+    w = wl.serving_workloads()[name]()
     y, batch = _run_delta(B, w)
     err = _assert_delta(w, y)
     c = batch.counts()
