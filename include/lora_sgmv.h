@@ -83,7 +83,8 @@ typedef int lora_status_t;
 #define LORA_BF16 1
 
 /* Path selection for lora_delta / lora_shrink / lora_expand. */
-#define LORA_PATH_AUTO 0      /* groups with >= tc_min_rows rows use the tcgen05 kernel (bf16) */
+#define LORA_PATH_AUTO 0      /* groups with >= tc_min_rows rows use the tcgen05 kernel (bf16);
+                                 bf16 batches of at most 256 rows use the small-batch kernel */
 #define LORA_PATH_CUDA_CORE 1 /* every segment on the small-segment kernel: clusters of CTAs,
                                  warp-level bf16 tensor-core tiles (fp32: CUDA-core FMAs) */
 #define LORA_PATH_TENSOR 2    /* every segment on the tcgen05 kernel (bf16 only) */
@@ -154,6 +155,8 @@ typedef struct lora_batch {
     int32_t max_segs;    /* capacity of the segment arrays */
     int32_t tc_min_rows; /* tensor-core row threshold used for the split */
     uint32_t magic;      /* set by lora_prepare_batch */
+    const int32_t *ids;  /* the ids the batch was built from (device, not owned;
+                            read again by the small-batch delta kernel) */
 } lora_batch_t;
 
 /* One output slice of the expand step: B pool and the y columns it writes
@@ -207,6 +210,8 @@ size_t lora_workspace_size(int32_t M, int32_t n_adapters, int32_t chunk_size);
  * must therefore be final before that previous kernel starts, which holds
  * whenever ids come from a copy or from any kernel enqueued before it, and
  * when that previous kernel is one of this library's (they never write ids).
+ * The batch keeps the ids pointer: calls that use the batch may group the
+ * rows again from it, so ids must keep these values while the batch is used.
  */
 lora_status_t lora_prepare_batch(const int32_t *ids, int32_t M, int32_t n_adapters,
                                  int32_t chunk_size, int32_t tc_min_rows,
@@ -300,6 +305,15 @@ lora_status_t lora_expand(const lora_batch_t *batch, int32_t dtype,
  * never written to global memory ("vLLM-Ascend LoRA" article, section 4.3).
  * Arguments as for lora_shrink and lora_expand.  Each y element is read,
  * y + delta is formed in fp32 and rounded to y's type once.
+ * Small batches: a bf16 batch of at most 256 rows under LORA_PATH_AUTO (at
+ * most 1024 rows under LORA_PATH_CUDA_CORE) with r_max <= 64 runs on one
+ * kernel that groups the rows itself from the batch's ids (the same groups
+ * as lora_prepare_batch), so that it does not wait for the batch metadata.
+ * That kernel reads ids, the A and B pools, ranks and adapter_scale before
+ * it waits for the kernels ahead of it in the stream (programmatic dependent
+ * launch): they must be final before the kernel preceding this call starts
+ * (adapter weights loaded earlier, ids from a copy or an earlier kernel).
+ * x and y are read only after that wait.
  * Non-finite y: on the tensor-core path y enters the fp32 accumulator through
  * an MMA with a 16 x 16 identity, so a NaN or infinity in y[i, n] turns the
  * other outputs of row i in the same aligned 16-column group of the 128-column

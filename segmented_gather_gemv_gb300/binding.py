@@ -57,7 +57,8 @@ class _Batch(ctypes.Structure):
                 ("tc_indptr", ctypes.c_void_p), ("counts", ctypes.c_void_p),
                 ("M", ctypes.c_int32), ("n_adapters", ctypes.c_int32),
                 ("chunk_size", ctypes.c_int32), ("max_segs", ctypes.c_int32),
-                ("tc_min_rows", ctypes.c_int32), ("magic", ctypes.c_uint32)]
+                ("tc_min_rows", ctypes.c_int32), ("magic", ctypes.c_uint32),
+                ("ids", ctypes.c_void_p)]
 
 
 class _BSlice(ctypes.Structure):

@@ -16,6 +16,7 @@ cudaError_t launch_cc(const DeltaArgs &p, int dtype, int mode, int cluster, int 
 int cc_cluster_size(int d_in, int d_out);
 cudaError_t launch_tc(const DeltaArgs &p, int mode, int sms, cudaStream_t stream);
 bool tc_available();
+bool try_launch_small(const DeltaArgs &p, int sms, cudaStream_t stream, cudaError_t *err);
 }  // namespace lora
 
 namespace lora {
@@ -140,6 +141,7 @@ lora_status_t check_slices(const lora_batch_t *b, int32_t dtype, const lora_b_sl
 }
 
 void fill_batch(const lora_batch_t *b, DeltaArgs &p) {
+    p.ids = b->ids;
     p.sorted = b->sorted_token_ids;
     p.tc_indptr = b->tc_indptr;
     p.counts = b->counts;
@@ -158,6 +160,20 @@ lora_status_t dispatch(const lora_batch_t *b, int32_t dtype, int mode, int32_t p
     p.max_list = b->max_segs;
     p.M_rows = b->M;
     p.n_adapters = b->n_adapters;
+    // Small batches (decode steps): one kernel that groups the rows itself
+    // from the ids and takes every group, so nothing on its path waits for
+    // prepare's metadata.  Under LORA_PATH_AUTO a batch of at most
+    // kSmallAutoRows rows goes there whole (a group that long is a small
+    // dense contraction anyway); LORA_PATH_CUDA_CORE sends it any batch it
+    // can group.
+    if (mode == kFused && dtype == LORA_BF16 &&
+        ((path == LORA_PATH_AUTO && b->M <= kSmallAutoRows) || path == LORA_PATH_CUDA_CORE)) {
+        if (try_launch_small(p, sms, stream, &e)) {
+            if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+            launch_counter().fetch_add(1, std::memory_order_relaxed);
+            return LORA_OK;
+        }
+    }
     if (path == LORA_PATH_TENSOR) {
         if (!tensor_ok || mode != kFused)
             return fail(LORA_ERR_UNSUPPORTED, "the tensor-core path computes the fused bf16 delta only");
@@ -267,6 +283,7 @@ lora_status_t lora_prepare_batch_ordered(const int32_t *ids, int32_t M, int32_t 
     b.max_segs = L.max_segs;
     b.tc_min_rows = tc_min;
     b.magic = kBatchMagic;
+    b.ids = ids;
     *batch = b;
     return LORA_OK;
 }

@@ -123,6 +123,9 @@ constexpr int kDefaultTcMinRows = 64;
 // Batches of at most this many rows start the CUDA-core kernel before the
 // tensor-core kernel (see the dispatch in api.cu).
 constexpr int kCcFirstMaxRows = 256;
+// Batches of at most this many rows run whole on the small-batch kernel
+// under LORA_PATH_AUTO (see the dispatch in api.cu).
+constexpr int kSmallAutoRows = 256;
 constexpr int kTcMaxRankCommon = 32;
 // Ranks the tensor-core kernel computes (exact 8-column masking, <= 32).
 __host__ __device__ __forceinline__ bool tc_rank_ok(int r) { return r > 0 && r <= kTcMaxRankCommon && (r & 7) == 0; }
@@ -200,9 +203,12 @@ __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
 // Programmatic dependent launch: let the next grid in the stream start its
 // prologue early / wait until the previous grid has completed and its
 // memory is visible.  Both are no-ops when the launch did not opt in.
-// Every kernel of this library waits before it triggers, so a grid that
-// starts early finds every grid before its predecessor complete: the
-// predecessor itself is the only one still running.
+// The delta kernels of this library wait before they trigger; prepare
+// triggers at its start (it writes its workspace only after its wait).  So
+// a grid that starts early finds complete every grid before the last delta
+// kernel ahead of it: at most that delta kernel and a prepare after it are
+// still running.  Before its own wait a grid reads only what none of them
+// writes: ids, adapter pools, ranks and scales.
 __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
@@ -358,6 +364,7 @@ static_assert(sizeof(SegDesc) == 128, "segment descriptor is 128 bytes");
 
 struct DeltaArgs {
     // batch
+    const int32_t *ids;      // the batch's ids (the small-batch kernel groups rows from them)
     const int32_t *sorted;   // sorted_token_ids
     const SegDesc *desc;     // all segment descriptors (len 0 past the last)
     const int4 *recs;        // records {start, len, adapter, s} (tensor-core list)

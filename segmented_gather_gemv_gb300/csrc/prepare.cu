@@ -47,7 +47,41 @@ struct PrepArgs {
     int2 *shares;       // tensor-core CTA shares: boundary b = {first row, segment}, b <= share_grid
     int32_t ascending;  // 1: groups by increasing adapter id, else by first appearance
     int32_t share_grid;
+    // small-batch kernel: hash slots, their table and the group table
+    int32_t hs, off_hash, off_gtab;
 };
+
+// Shares of the tensor-core row space for a grid of `grid` CTAs, by the rule
+// the tensor-core kernel applies itself when it has no table: the share end
+// e = rows * b / grid moves to the boundary between two adapters when one
+// lies within half a share (chunks of one adapter do not count).  Written for
+// every batch, zeros when it has no such row.  `tcl` / `tcp` are the
+// tensor-core records and their row prefix (nseg of them).
+__device__ void write_shares(const int4 *tcl, const int32_t *tcp, int nseg, int rows, int grid, int2 *shares) {
+    const int half = grid > 0 ? (int)(rows / (2 * (int64_t)grid)) : 0;
+    auto seg_of = [&](int r) {  // largest i < nseg with tcp[i] <= r
+        int lo = 0, hi = nseg - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (tcp[mid] <= r) lo = mid;
+            else hi = mid - 1;
+        }
+        return lo;
+    };
+    for (int b = threadIdx.x; grid > 0 && b <= grid; b += blockDim.x) {
+        int e = (int)((int64_t)rows * b / grid), sg = 0;
+        if (nseg > 0 && rows > 0) {
+            if (nseg >= 2 && e > 0 && e < rows) {
+                const int i = seg_of(e);
+                const int lo = tcp[i], hi = tcp[i + 1], a = tcl[i].z;
+                if (e - lo <= half && i > 0 && tcl[i - 1].z != a) e = lo;
+                else if (hi - e <= half && i + 1 < nseg && tcl[i + 1].z != a) e = hi;
+            }
+            sg = e < rows ? seg_of(e) : nseg;
+        }
+        shares[b] = make_int2(e, sg);
+    }
+}
 
 // Block-wide exclusive scan of one value per thread.  `ws` is shared scratch
 // of 33 ints.  All threads must call it.
@@ -92,11 +126,13 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
     // griddep_launch_dependents).  The next kernel may start once this grid
     // has waited; it waits for this grid's completion before it reads what
     // this grid writes.
+    // The next grid may start at once: every kernel of this library reads
+    // what this grid writes only after its own wait (which returns once this
+    // grid has completed), and before that wait reads only data that is
+    // fixed before this grid starts (ids, adapter pools).
+    griddep_launch_dependents();
     const bool early = p.off_adapters >= 0 && p.off_groups >= 0;
-    if (!early) {
-        griddep_wait();
-        griddep_launch_dependents();
-    }
+    if (!early) griddep_wait();
 
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
@@ -297,10 +333,7 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
         o_tcptr = reinterpret_cast<int32_t *>(b + O.tcptr);
         o_sorted = reinterpret_cast<int32_t *>(b + O.sorted);
     }
-    if (early && !stage) {
-        griddep_wait();
-        griddep_launch_dependents();
-    }
+    if (early && !stage) griddep_wait();
 
     // Phase 4: segments, records and the tensor-core split (by group rows).
     int n_small = 0, n_tc = 0, tc_rows = 0;
@@ -453,7 +486,6 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
         // copy the staged outputs (descriptors as 16-byte pieces)
         __syncthreads();
         griddep_wait();
-        griddep_launch_dependents();
         // one contiguous copy of the output block (entries past each
         // array's valid length go along unread)
         const int4 *src = reinterpret_cast<const int4 *>(smem_raw + p.off_stage);
@@ -462,46 +494,228 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
         for (int k = tid; k < n16; k += nthr) dst[k] = src[k];
     }
 
-    // Shares of the tensor-core row space for a grid of share_grid CTAs,
-    // by the rule the tensor-core kernel applies itself when it has no
-    // table: the share end e = rows * b / grid moves to the boundary between
-    // two adapters when one lies within half a share (chunks of one adapter
-    // do not count).  Written for every batch, zeros when it has no such row.
-    {
-        __syncthreads();  // the tensor-core list (shared or global) is complete
-        const int4 *tcl = o_tc;
-        const int32_t *tcp = o_tcptr;
-        const int G = p.share_grid, nseg = n_tc, rows = tc_rows;
-        const int half = G > 0 ? (int)(rows / (2 * (int64_t)G)) : 0;
-        auto seg_of = [&](int r) {  // largest i < nseg with tcp[i] <= r
-            int lo = 0, hi = nseg - 1;
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (tcp[mid] <= r) lo = mid;
-                else hi = mid - 1;
-            }
-            return lo;
-        };
-        for (int b = tid; G > 0 && b <= G; b += nthr) {
-            int e = (int)((int64_t)rows * b / G), sg = 0;
-            if (nseg > 0 && rows > 0) {
-                if (nseg >= 2 && e > 0 && e < rows) {
-                    const int i = seg_of(e);
-                    const int lo = tcp[i], hi = tcp[i + 1], a = tcl[i].z;
-                    if (e - lo <= half && i > 0 && tcl[i - 1].z != a) e = lo;
-                    else if (hi - e <= half && i + 1 < nseg && tcl[i + 1].z != a) e = hi;
-                }
-                sg = e < rows ? seg_of(e) : nseg;
-            }
-            p.shares[b] = make_int2(e, sg);
-        }
-    }
+    __syncthreads();  // the tensor-core list (shared or global) is complete
+    write_shares(o_tc, o_tcptr, n_tc, tc_rows, p.share_grid, p.shares);
 
     // Phase 6: counters.
     if (tid == 0) {
         p.counts[LORA_COUNT_SEGS] = S;
         p.counts[LORA_COUNT_ACTIVE] = ACT;
         p.counts[LORA_COUNT_INVALID] = s_invalid;
+        p.counts[LORA_COUNT_SMALL_SEGS] = n_small;
+        p.counts[LORA_COUNT_TC_SEGS] = n_tc;
+        p.counts[LORA_COUNT_TC_ROWS] = tc_rows;
+        p.counts[LORA_COUNT_DEVERR] = 0;
+        p.counts[LORA_COUNT_GROUPS] = G;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Small batches (at most kPrepSmallMaxRows rows, groups by first appearance):
+// one row per thread and a handful of block-wide steps, every table and the
+// whole output block in shared memory, so that the part after the wait on
+// the previous grid is one copy.  The outputs are those of prepare_kernel,
+// bit for bit.
+//   1. a hash slot per adapter with its first row and row count; within each
+//      warp, every row's rank among the warp's rows of its adapter;
+//   2. one block scan over the rows of (first-row flag | segments << 16 |
+//      rows << 32): group number, segment base and row base of every group;
+//   3. per segment: start, length, adapter, the tensor-core flag; per warp
+//      and group: the warp's row count;
+//   4. per group: the warps' row counts turned into their first positions;
+//      one block scan over the segments of (tensor-core flag | rows << 32):
+//      the small and tensor-core lists and the tensor-core row prefix;
+//   5. every row's position (its warp's first position in its group plus its
+//      rank in the warp) and the descriptors' inline rows;
+//   6. after the wait: the copy, the tensor-core shares and the counters.
+constexpr int kPrepSmallThreads = 512;
+constexpr int kPrepSmallMaxRows = kPrepSmallThreads;
+
+__global__ void __launch_bounds__(kPrepSmallThreads, 1) prepare_small_kernel(const __grid_constant__ PrepArgs p) {
+    constexpr int NW = kPrepSmallThreads / 32;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    __shared__ unsigned long long wsum[NW];
+    // The next grid may start at once (see griddep_launch_dependents): this
+    // grid writes global memory only after its wait.
+    griddep_launch_dependents();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int M = p.M, n = p.n, HS = p.hs, gcap = p.gcap;
+    int32_t *key = reinterpret_cast<int32_t *>(smem_raw + p.off_hash), *first = key + HS, *cnt = first + HS;
+    int32_t *whist = reinterpret_cast<int32_t *>(smem_raw + p.off_hist);  // [NW][gcap]
+    int32_t *gad = reinterpret_cast<int32_t *>(smem_raw + p.off_gtab);
+    int32_t *gcnt = gad + gcap, *grb = gcnt + gcap, *gsb = grb + gcap + 1;
+    const OutLayout O = out_layout(p.max_segs, M);
+    unsigned char *stg = smem_raw + p.off_stage;
+    SegDesc *o_desc = reinterpret_cast<SegDesc *>(stg + O.rec);
+    int4 *o_small = reinterpret_cast<int4 *>(stg + O.small);
+    int4 *o_tc = reinterpret_cast<int4 *>(stg + O.tc);
+    int32_t *o_indptr = reinterpret_cast<int32_t *>(stg + O.indptr);
+    int32_t *o_lens = reinterpret_cast<int32_t *>(stg + O.lens);
+    int32_t *o_widx = reinterpret_cast<int32_t *>(stg + O.widx);
+    int32_t *o_tcptr = reinterpret_cast<int32_t *>(stg + O.tcptr);
+    int32_t *o_sorted = reinterpret_cast<int32_t *>(stg + O.sorted);
+
+    const int id = tid < M ? __ldcg(p.ids + tid) : -1;
+    for (int s = tid; s < HS; s += kPrepSmallThreads) {
+        key[s] = -1;
+        first[s] = INT_MAX;
+        cnt[s] = 0;
+    }
+    for (int k = tid; k < NW * gcap; k += kPrepSmallThreads) whist[k] = 0;
+    const bool valid = tid < M && id >= 0 && id < n;
+    const bool invalid = tid < M && id != -1 && !valid;
+    __syncthreads();
+
+    // 1. hash slots; ranks inside the warp
+    int slot = -1;
+    if (valid) {
+        slot = (int)(((uint32_t)id * 0x9E3779B1u) >> (32 - (31 - __clz(HS))));
+        for (;;) {  // at most M < HS distinct keys: a free slot always exists
+            const int k = atomicCAS(&key[slot], -1, id);
+            if (k == -1 || k == id) break;
+            slot = (slot + 1) & (HS - 1);
+        }
+        atomicMin(&first[slot], tid);
+        atomicAdd(&cnt[slot], 1);
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, valid ? id : (int)(0x80000000u | (unsigned)lane));
+    const int rank_w = __popc(peers & ((1u << lane) - 1u));
+    const int n_invalid = __syncthreads_count(invalid);
+
+    // 2. groups: number, segment base, row base
+    const bool lead = valid && first[slot] == tid;
+    const int c = lead ? cnt[slot] : 0;
+    const int nseg = lead ? (p.chunk > 0 ? (c + p.chunk - 1) / p.chunk : 1) : 0;
+    const unsigned long long v = lead ? (1ull | ((unsigned long long)nseg << 16) | ((unsigned long long)c << 32)) : 0ull;
+    unsigned long long incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    unsigned long long base = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        const unsigned long long s = wsum[w];
+        base += w < warp ? s : 0ull;
+        total += s;
+    }
+    const int G = (int)(total & 0xFFFFu), S = (int)((total >> 16) & 0xFFFFu), ACT = (int)(total >> 32);
+    if (lead) {
+        const unsigned long long ex = base + incl - v;
+        const int g = (int)(ex & 0xFFFFu);
+        gad[g] = id;
+        gcnt[g] = c;
+        grb[g] = (int)(ex >> 32);
+        gsb[g] = (int)((ex >> 16) & 0xFFFFu);
+        first[slot] = g;  // from here on: the slot's group
+    }
+    if (tid == 0) {
+        grb[G] = ACT;
+        gsb[G] = S;
+    }
+    __syncthreads();
+
+    // 3. warps' row counts per group; segments
+    const int myg = valid ? first[slot] : -1;
+    if (valid && rank_w == 0) whist[warp * gcap + myg] = __popc(peers);
+    for (int s = tid; s < S; s += kPrepSmallThreads) {
+        int lo = 0, hi = G - 1;  // largest group whose first segment is <= s
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (gsb[mid] <= s) lo = mid;
+            else hi = mid - 1;
+        }
+        const int gc = gcnt[lo], cs = s - gsb[lo];
+        int st = grb[lo], len = gc;
+        if (p.chunk > 0) {
+            st += cs * p.chunk;
+            len = min(p.chunk, gc - cs * p.chunk);
+        }
+        o_indptr[s] = st;
+        o_lens[s] = len;
+        o_widx[s] = gad[lo];
+        // the split follows the adapter group's rows (see prepare_kernel)
+        *reinterpret_cast<int4 *>(&o_desc[s]) = make_int4(st, len, gad[lo], s | (gc >= p.tc_min ? LORA_DESC_TC_FLAG : 0));
+    }
+    for (int s = S + tid; s < p.max_segs; s += kPrepSmallThreads)
+        *reinterpret_cast<int4 *>(&o_desc[s]) = make_int4(0, 0, 0, s);
+    __syncthreads();
+
+    // 4. first position of every warp's rows in each group; the two lists
+    if (tid < G) {
+        int run = grb[tid];
+        for (int w = 0; w < NW; ++w) {
+            const int t = whist[w * gcap + tid];
+            whist[w * gcap + tid] = run;
+            run += t;
+        }
+    }
+    int4 rec = make_int4(0, 0, 0, 0);
+    bool is_tc = false;
+    if (tid < S) {
+        rec = *reinterpret_cast<const int4 *>(&o_desc[tid]);
+        is_tc = (rec.w & LORA_DESC_TC_FLAG) != 0;
+        rec.w = tid;
+    }
+    const unsigned long long v2 = is_tc ? (1ull | ((unsigned long long)rec.y << 32)) : 0ull;
+    unsigned long long incl2 = v2;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long t = __shfl_up_sync(0xffffffffu, incl2, o);
+        if (lane >= o) incl2 += t;
+    }
+    if (lane == 31) wsum[warp] = incl2;
+    __syncthreads();
+    unsigned long long base2 = 0, total2 = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        const unsigned long long s = wsum[w];
+        base2 += w < warp ? s : 0ull;
+        total2 += s;
+    }
+    const int n_tc = (int)(total2 & 0xFFFFFFFFu), tc_rows = (int)(total2 >> 32), n_small = S - n_tc;
+    if (tid < S) {
+        const unsigned long long ex = base2 + incl2 - v2;
+        const int before = (int)(ex & 0xFFFFFFFFu);
+        if (is_tc) {
+            o_tc[before] = rec;
+            o_tcptr[before] = (int)(ex >> 32);
+        } else {
+            o_small[tid - before] = rec;
+        }
+    }
+    if (tid == 0) {
+        o_indptr[S] = ACT;
+        o_tcptr[n_tc] = tc_rows;
+    }
+
+    // 5. positions and the descriptors' inline rows
+    if (valid) {
+        const int pos = whist[warp * gcap + myg] + rank_w;
+        o_sorted[pos] = tid;
+        const int off = pos - grb[myg];
+        const int s = gsb[myg] + (p.chunk > 0 ? off / p.chunk : 0);
+        const int k = p.chunk > 0 ? off - (off / p.chunk) * p.chunk : off;
+        if (k < kInlineRows) o_desc[s].rows[k] = tid;
+    }
+    __syncthreads();
+
+    // 6. after the previous grid: the copy, the shares, the counters
+    griddep_wait();
+    {
+        const int4 *src = reinterpret_cast<const int4 *>(stg);
+        int4 *dst = reinterpret_cast<int4 *>(p.out_block);
+        const int n16 = int(O.total / 16);
+        for (int k = tid; k < n16; k += kPrepSmallThreads) dst[k] = src[k];
+    }
+    write_shares(o_tc, o_tcptr, n_tc, tc_rows, p.share_grid, p.shares);
+    if (tid == 0) {
+        p.counts[LORA_COUNT_SEGS] = S;
+        p.counts[LORA_COUNT_ACTIVE] = ACT;
+        p.counts[LORA_COUNT_INVALID] = n_invalid;
         p.counts[LORA_COUNT_SMALL_SEGS] = n_small;
         p.counts[LORA_COUNT_TC_SEGS] = n_tc;
         p.counts[LORA_COUNT_TC_ROWS] = tc_rows;
@@ -546,8 +760,55 @@ cudaError_t launch_prepare(const int32_t *ids, int32_t M, int32_t n, int32_t chu
     p.gseg = at(L.group_seg);
     p.whist = at(L.warp_hist);
 
-    const int threads = M > 8192 ? 1024 : (M > 1024 ? 512 : 256);
     const int gcap = L.g_max;
+    if (M <= kPrepSmallMaxRows && !ascending) {
+        // hash table, warp counts, group table and the output block
+        int hs = 64;
+        while (hs < 2 * M) hs <<= 1;
+        size_t o = 0;
+        auto take = [&](size_t bytes) {
+            const size_t at = o;
+            o += (bytes + 15) & ~size_t(15);
+            return (int32_t)at;
+        };
+        p.hs = hs;
+        p.off_hash = take(size_t(3) * hs * 4);
+        p.off_hist = take(size_t(kPrepSmallThreads / 32) * gcap * 4);
+        p.off_gtab = take((size_t(4) * gcap + 2) * 4);
+        p.off_stage = take(out_layout(L.max_segs, M).total);
+        if (o <= kPrepSmemMax) {
+            static DeviceOnce configured_small;
+            cudaError_t e = configured_small.run([] {
+                return cudaFuncSetAttribute(prepare_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            (int)kPrepSmemMax);
+            });
+            if (e != cudaSuccess) return e;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(1);
+            cfg.blockDim = dim3(kPrepSmallThreads);
+            cfg.dynamicSmemBytes = o;
+            cfg.stream = stream;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            e = cudaLaunchKernelEx(&cfg, prepare_small_kernel, p);
+            if (e != cudaSuccess) return e;
+            b->sorted_token_ids = p.sorted;
+            b->seg_indptr = p.indptr;
+            b->seg_lens = p.lens;
+            b->weight_indices = p.widx;
+            b->seg_records = reinterpret_cast<int32_t *>(p.desc);
+            b->small_segs = reinterpret_cast<int32_t *>(p.small);
+            b->tc_segs = reinterpret_cast<int32_t *>(p.tc);
+            b->tc_indptr = p.tcptr;
+            b->counts = p.counts;
+            return cudaSuccess;
+        }
+    }
+
+    const int threads = M > 8192 ? 1024 : (M > 1024 ? 512 : 256);
     // Place tables in shared memory, most latency-critical first.
     size_t smem = 0;
     auto place = [&](size_t bytes) -> int32_t {
