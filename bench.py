@@ -9,16 +9,22 @@ adapters active, bf16).
 
 Timing: W eager warm-up steps, then exactly K steps captured in CUDA graphs
 and replayed between CUDA events on the launching stream, bracketed by a
-barrier and a device synchronize.  Every step uses one of S rotating input
-sets (x, y, pools, ids, workspace) whose total exceeds L2, so no step finds
-its inputs in L2.  The kernels of a step are chained by programmatic
-dependent launch.  Kernel durations (for the roofline) come from one more
-replay of the same steps in which event nodes bracket every call; event
-nodes cut the programmatic overlap, so that replay is kept out of the timed
-region.  When one kernel takes every active row (the tensor-core kernel on
-prefill, the CUDA-core kernel on decode) a further replay forces the path to
-it, so the roofline divides by that kernel's own launch time; otherwise by
-the time of the whole lora_delta call.
+barrier and a device synchronize.  A GPU-side delay is enqueued just before
+the start event, so that the host has submitted the graphs before the start
+event runs and the region times the device, not the submission.  Every step
+uses one of S rotating input sets (x, y, pools, ids, workspace) whose total
+exceeds L2, so no step finds its inputs in L2.  The kernels of a step are
+chained by programmatic dependent launch.
+
+Roofline: the dominant kernel is the one the library reports for the delta
+call (``lora_last_kernels``); when one kernel takes every active row the path
+is forced to it.  Its average launch duration comes from a chain of G
+back-to-back ``lora_delta`` calls (prepared batches, rotating input sets)
+replayed between CUDA events on the launching stream: the time of the chain
+over G.  Per-kernel event times of single launches are reported beside it.
+
+The other serving workloads are measured in the same run (fewer steps, the
+same rules) under ``other_workloads``.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
 a bounded sample of the same workload instead.
@@ -30,6 +36,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import shutil
 import statistics
 import subprocess
@@ -59,14 +66,19 @@ WORKLOADS = {
 }
 # Kernel sources whose counters a committed ncu summary refers to.
 KERNEL_SOURCES = {
+    "sgmv_small_kernel": ["segmented_gather_gemv_gb300/csrc/sgmv_small.cu",
+                          "segmented_gather_gemv_gb300/csrc/common.cuh"],
     "sgmv_cc_kernel": ["segmented_gather_gemv_gb300/csrc/sgmv_cc.cu",
                        "segmented_gather_gemv_gb300/csrc/common.cuh"],
     "sgmv_tc_kernel": ["segmented_gather_gemv_gb300/csrc/sgmv_tc.cu",
                        "segmented_gather_gemv_gb300/csrc/common.cuh"],
 }
+# Device delay before a timed region: longer than the host needs to submit
+# the region's graphs (cycles at about 2 GHz).
+DELAY_CYCLES = 4_000_000
 
 
-def parse_args():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
@@ -78,7 +90,9 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
+    ap.add_argument("--extra-steps", type=int, default=500)
+    return ap.parse_args(argv)
 
 
 # ------------------------------------------------------------------ helpers
@@ -131,6 +145,25 @@ def committed_traffic(kernel: str, workload: str):
     if not e or e.get("source_sha256_16") != source_hash(kernel):
         return None
     return int(e["dram_bytes_per_launch"])
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k = line.split(":")[0].strip().lower()
+                if k in ("model name", "cpu model", "hardware"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
 
 class ClockSampler:
@@ -192,21 +225,33 @@ class ClockSampler:
 
 def cpu_baseline(w: wl.Workload, seconds: float) -> dict:
     """The oracle, as it stands, on the host: full batches (prepare + delta)
-    repeated until `seconds` have passed; single-threaded."""
+    repeated for about `seconds`, once on all host cores (the rows shared
+    out by OpenMP) and once single-threaded."""
     import oracle
-    t0 = time.perf_counter()
-    reps = 0
-    while True:
-        oracle.prepare_batch(w.ids, w.n_adapters, w.chunk_size)
-        oracle.delta(w.x, w.ids, w.A, w.B, w.y, scale=w.scale,
-                     adapter_scale=w.adapter_scale, ranks=w.ranks)
-        reps += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": reps * w.M / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": "%d full batches of %d rows (grouping + fp64 per-token delta), %.1f s"
-                      % (reps, w.M, dt)}
+
+    def run(threads, budget):
+        t0 = time.perf_counter()
+        reps, used = 0, 1
+        while True:
+            oracle.prepare_batch(w.ids, w.n_adapters, w.chunk_size)
+            oracle.delta(w.x, w.ids, w.A, w.B, w.y, scale=w.scale,
+                         adapter_scale=w.adapter_scale, ranks=w.ranks, threads=threads)
+            used = oracle.delta.last_threads
+            reps += 1
+            if time.perf_counter() - t0 >= budget:
+                break
+        dt = time.perf_counter() - t0
+        return reps * w.M / dt, reps, dt, used
+
+    cores = host_cores()
+    v_all, reps_all, dt_all, used = run(cores, seconds / 2)
+    v_one, reps_one, dt_one, _ = run(1, seconds / 2)
+    return {"value": v_all, "unit": "tokens/s", "cores": used, "kind": "oracle",
+            "sample": "%d full batches of %d rows (grouping + fp64 per-token delta, rows over %d "
+                      "threads), %.1f s" % (reps_all, w.M, used, dt_all),
+            "cpu_model": cpu_model(), "nproc": cores,
+            "single_thread": {"value": v_one, "unit": "tokens/s", "cores": 1,
+                              "sample": "%d full batches, %.1f s" % (reps_one, dt_one)}}
 
 
 def replica_seed(rank: int) -> int:
@@ -239,19 +284,20 @@ def run_reference(args, rank: int, world: int):
     oracle.build()
     K = args.steps if args.steps is not None else 20
     W = max(3, args.warmup)
+    cores = host_cores()
     # Per step: a bounded sample of the batch's rows, sized so the whole run
     # takes about two minutes at most.
     t0 = time.perf_counter()
-    oracle.delta(w.x[:8], w.ids[:8], w.A, w.B, w.y[:8], scale=w.scale,
-                 adapter_scale=w.adapter_scale, ranks=w.ranks)
-    per_row = max((time.perf_counter() - t0) / 8, 1e-6)
+    oracle.delta(w.x[:64], w.ids[:64], w.A, w.B, w.y[:64], scale=w.scale,
+                 adapter_scale=w.adapter_scale, ranks=w.ranks, threads=cores)
+    per_row = max((time.perf_counter() - t0) / 64, 1e-6)
     rows = int(max(1, min(w.M, 100.0 / (K + W) / per_row)))
     sel = np.arange(rows)
 
     def step():
         oracle.prepare_batch(w.ids[sel], w.n_adapters, w.chunk_size)
         oracle.delta(w.x[sel], w.ids[sel], w.A, w.B, w.y[sel], scale=w.scale,
-                     adapter_scale=w.adapter_scale, ranks=w.ranks)
+                     adapter_scale=w.adapter_scale, ranks=w.ranks, threads=cores)
 
     for _ in range(W):
         step()
@@ -259,6 +305,7 @@ def run_reference(args, rank: int, world: int):
     for _ in range(K):
         step()
     dt = time.perf_counter() - t0
+    used = oracle.delta.last_threads
     value = K * rows / dt
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
@@ -267,9 +314,10 @@ def run_reference(args, rank: int, world: int):
         "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "tokens_per_step": rows,
                    "sample": "first %d of %d rows per step" % (rows, w.M)},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": "first %d of %d rows of %s per step, %d steps"
-                                   % (rows, w.M, w.name, K)},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                         "sample": "first %d of %d rows of %s per step, %d steps, rows over %d "
+                                   "threads" % (rows, w.M, w.name, K, used),
+                         "cpu_model": cpu_model(), "nproc": cores},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -278,10 +326,262 @@ def run_reference(args, rank: int, world: int):
 
 # ------------------------------------------------------------------ GPU side
 
+class Bench:
+    """Input sets, graphs and timings of one workload on one GPU."""
+
+    def __init__(self, w: wl.Workload, args, dev, stream, path: int):
+        import torch
+        from segmented_gather_gemv_gb300 import binding as B
+        self.torch, self.B = torch, B
+        self.w, self.args, self.dev, self.stream, self.path = w, args, dev, stream, path
+        self.es = 2 if w.dtype == "bf16" else 4
+        self.tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        # Rotating input sets: enough copies that the sets together exceed L2.
+        self.set_bytes = (w.x.size + w.y.size + w.A.size + sum(b.size for b in w.B)) * self.es
+        self.n_sets = int(min(64, max(2, math.ceil(3 * L2_BYTES / self.set_bytes))))
+        x0 = torch.from_numpy(w.x).to(dev, self.tdt)
+        y0 = torch.from_numpy(w.y).to(dev, self.tdt)
+        A0 = torch.from_numpy(w.A).to(dev, self.tdt)
+        B0 = [torch.from_numpy(b).to(dev, self.tdt) for b in w.B]
+        ids0 = torch.from_numpy(w.ids).to(dev)
+        self.ranks = None if w.ranks is None else torch.from_numpy(w.ranks).to(dev)
+        self.ascale = None if w.adapter_scale is None else torch.from_numpy(w.adapter_scale).to(dev)
+        ws_bytes = B.lora_workspace_size(w.M, w.n_adapters, w.chunk_size)
+        self.sets = []
+        for i in range(self.n_sets):
+            self.sets.append({
+                "x": x0 if i == 0 else x0.clone(), "y": y0 if i == 0 else y0.clone(),
+                "A": A0 if i == 0 else A0.clone(), "B": B0 if i == 0 else [b.clone() for b in B0],
+                "ids": ids0 if i == 0 else ids0.clone(),
+                "ws": torch.empty(ws_bytes, dtype=torch.uint8, device=dev),
+            })
+
+    def prepare(self, s):
+        return self.B.lora_prepare_batch(s["ids"], self.w.n_adapters, self.w.chunk_size,
+                                         workspace=s["ws"], stream=self.stream)
+
+    def delta(self, batch, s, path=None):
+        self.B.lora_delta(batch, s["x"], s["A"], s["B"], s["y"], scale=self.w.scale,
+                          adapter_scale=self.ascale, ranks=self.ranks,
+                          path=self.path if path is None else path, stream=self.stream)
+
+    def step(self, s):
+        batch = self.prepare(s)
+        self.delta(batch, s)
+        return batch
+
+    def delay(self):
+        self.torch.cuda._sleep(DELAY_CYCLES)
+
+    def graph(self, nsteps, offset=0, event_nodes=False):
+        """Graph of `nsteps` steps; with `event_nodes`, events bracket every
+        kernel (they also cut the programmatic overlap between kernels)."""
+        torch = self.torch
+        evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True))
+               for _ in range(nsteps if event_nodes else 0)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream, capture_error_mode="thread_local"):
+            for i in range(nsteps):
+                s = self.sets[(offset + i) % self.n_sets]
+                if event_nodes:
+                    evs[i][0].record(self.stream)
+                batch = self.prepare(s)
+                if event_nodes:
+                    evs[i][1].record(self.stream)
+                self.delta(batch, s)
+                if event_nodes:
+                    evs[i][2].record(self.stream)
+        return g, evs
+
+    def timed(self, graphs, world, dev):
+        """Device time of replaying `graphs` (ms), max over ranks."""
+        torch = self.torch
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            self.delay()
+            t0.record(self.stream)
+            for g in graphs:
+                g.replay()
+            t1.record(self.stream)
+        t1.synchronize()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        return max_over_ranks(t0.elapsed_time(t1), world, dev)
+
+    def delta_chain_us(self, G, path):
+        """Average launch time (us) of lora_delta in a chain of G back-to-back
+        calls on prepared batches of the rotating sets."""
+        torch = self.torch
+        batches = []
+        for s in self.sets:
+            batches.append(self.prepare(s))
+        self.stream.synchronize()
+        with torch.cuda.stream(self.stream):
+            for i in range(3):
+                self.delta(batches[i % self.n_sets], self.sets[i % self.n_sets], path)
+        self.stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream, capture_error_mode="thread_local"):
+            for i in range(G):
+                self.delta(batches[i % self.n_sets], self.sets[i % self.n_sets], path)
+        with torch.cuda.stream(self.stream):
+            g.replay()
+        self.stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            self.delay()
+            e0.record(self.stream)
+            g.replay()
+            e1.record(self.stream)
+        e1.synchronize()
+        return 1e3 * e0.elapsed_time(e1) / G
+
+
+def measure(b: Bench, key: str, K: int, W: int, world: int, dev, graph_steps: int, clocks=None,
+            kernel_events=True) -> dict:
+    """One workload: W warm-up steps, K timed steps, the dominant kernel's
+    average launch time and the roofline."""
+    torch, B, w = b.torch, b.B, b.w
+    ab = algorithmic_bytes(w)
+    with torch.cuda.stream(b.stream):
+        for i in range(W):
+            b.step(b.sets[i % b.n_sets])
+    b.stream.synchronize()
+    b0 = b.prepare(b.sets[0])
+    b.stream.synchronize()
+    counts = b0.counts()
+    n_launch0 = B.lora_launch_count()
+    with torch.cuda.stream(b.stream):
+        batch = b.prepare(b.sets[0])
+        b.delta(batch, b.sets[0])
+    kernels_bits = B.lora_last_kernels()
+    launches_per_step = B.lora_launch_count() - n_launch0
+    b.stream.synchronize()
+
+    # The dominant kernel: the only one of the delta call, or, when one
+    # kernel takes every active row, the path forced to it.
+    dom_path, dom_bits = None, kernels_bits
+    if bin(kernels_bits).count("1") > 1 and b.path == 0 and counts["num_active"] > 0:
+        if counts["tc_rows"] == counts["num_active"]:
+            dom_path = 2
+        elif counts["tc_rows"] == 0:
+            dom_path = 1
+        if dom_path is not None:
+            with torch.cuda.stream(b.stream):
+                b.delta(b0, b.sets[0], dom_path)
+            dom_bits = B.lora_last_kernels()
+            b.stream.synchronize()
+    kernel = (B.KERNEL_NAMES.get(dom_bits) if bin(dom_bits).count("1") == 1
+              else "+".join(B.KERNEL_NAMES[k] for k in sorted(B.KERNEL_NAMES) if dom_bits & k))
+
+    G = max(1, min(graph_steps, K))
+    reps, rem = divmod(K, G)
+    g_main, _ = b.graph(G)
+    g_rem = b.graph(rem)[0] if rem else None
+    with torch.cuda.stream(b.stream):
+        g_main.replay()
+        if g_rem is not None:
+            g_rem.replay()
+    b.stream.synchronize()
+    graphs = [g_main] * reps + ([g_rem] if g_rem is not None else [])
+    if clocks is not None:
+        clocks.start()
+        time.sleep(0.3)
+    wall0 = time.perf_counter()
+    elapsed_ms = b.timed(graphs, world, dev)
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop() if clocks is not None else None
+
+    # the dominant kernel's average launch time (a chain of delta calls)
+    Gc = max(32, min(512, K))
+    chain_us = b.delta_chain_us(Gc, dom_path)
+    # single launches with event nodes around each kernel, for context
+    kern = {}
+    if kernel_events:
+        Ge = min(64, max(8, K))
+        g_ev, evs = b.graph(Ge, event_nodes=True)
+        with torch.cuda.stream(b.stream):
+            g_ev.replay()
+            g_ev.replay()
+        b.stream.synchronize()
+        prep = [1e3 * e0.elapsed_time(e1) for e0, e1, e2 in evs]
+        dlt = [1e3 * e1.elapsed_time(e2) for e0, e1, e2 in evs]
+        kern = {"prepare_single_launch_mean": statistics.mean(prep),
+                "delta_single_launch_mean": statistics.mean(dlt)}
+    kern["delta_chain_mean"] = chain_us
+
+    peak, peak_kind = load_peaks()
+    achieved = ab["total"] / (chain_us * 1e-6) / 1e9
+    ms_per_step = elapsed_ms / K
+    out = {
+        "workload": w.name, "steps": K, "warmup": W, "ms_per_step": ms_per_step,
+        "value": whole_job_tokens_per_s(world, K, w.M, elapsed_ms), "elapsed_ms": elapsed_ms,
+        "wall_s_timed": wall, "counts": counts, "ab": ab, "launches_per_step": launches_per_step,
+        "n_sets": b.n_sets, "graph_steps": G, "clocks": clk,
+        "kernels_us": kern,
+        "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
+                     "duration": ("mean launch time of %s in a chain of %d back-to-back lora_delta "
+                                  "calls%s (CUDA events on the launching stream around the chain)"
+                                  % (kernel, Gc, " with the path forced to it" if dom_path else "")),
+                     "traffic": committed_traffic(kernel, key) if kernel in KERNEL_SOURCES else None},
+        "step_gbs": ab["total"] / (ms_per_step * 1e-3) / 1e9,
+    }
+    return out
+
+
+def e2e_measure(b: Bench, steps: int) -> dict:
+    """The public API from pinned host buffers, copies inside the region."""
+    torch, w = b.torch, b.w
+    x_h = torch.from_numpy(w.x).to(b.tdt).pin_memory()
+    y_h = torch.from_numpy(w.y).to(b.tdt).pin_memory()
+    ids_h = torch.from_numpy(w.ids).pin_memory()
+    y_out = torch.empty_like(y_h).pin_memory()
+    s0 = b.sets[0]
+    with torch.cuda.stream(b.stream):
+        for i in range(3 + steps):
+            if i == 3:
+                b.stream.synchronize()
+                e_a = torch.cuda.Event(enable_timing=True)
+                e_b = torch.cuda.Event(enable_timing=True)
+                e_a.record(b.stream)
+            s0["x"].copy_(x_h, non_blocking=True)
+            s0["y"].copy_(y_h, non_blocking=True)
+            s0["ids"].copy_(ids_h, non_blocking=True)
+            b.step(s0)
+            y_out.copy_(s0["y"], non_blocking=True)
+        e_b.record(b.stream)
+    e_b.synchronize()
+    e2e_ms = e_a.elapsed_time(e_b) / steps
+    h2d = (x_h.numel() + y_h.numel()) * b.es + ids_h.numel() * 4
+    d2h = y_out.numel() * b.es
+    return {"value": w.M / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+
+def summary(m: dict) -> dict:
+    r = m["roofline"]
+    return {"workload": m["workload"], "tokens_per_s": m["value"], "ms_per_step": m["ms_per_step"],
+            "steps": m["steps"], "algorithmic_bytes_per_step": m["ab"]["total"],
+            "step_gbs": m["step_gbs"], "kernel": r["kernel"], "kernel_chain_us": m["kernels_us"]["delta_chain_mean"],
+            "roofline_frac": r["frac"], "frac_of_8tbs": r["frac_of_8tbs"], "traffic": r["traffic"],
+            "tc_rows": m["counts"]["tc_rows"], "active_rows": m["counts"]["num_active"],
+            "num_segs": m["counts"]["num_segs"]}
+
+
 def run_ours(args, rank: int, world: int, local_rank: int):
     import torch
-    import torch.distributed as dist
-    from segmented_gather_gemv_gb300 import binding as B
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
@@ -289,229 +589,70 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     K = args.steps if args.steps is not None else default_steps
     W = max(3, args.warmup)
     w = factory(replica_seed(rank))
-    es = 2 if w.dtype == "bf16" else 4
-    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
-    ab = algorithmic_bytes(w)
-
-    # Rotating input sets: enough copies that the sets together exceed L2.
-    set_bytes = (w.x.size + w.y.size + w.A.size + sum(b.size for b in w.B)) * es
-    n_sets = int(min(64, max(2, math.ceil(3 * L2_BYTES / set_bytes))))
-    x0 = torch.from_numpy(w.x).to(dev, tdt)
-    y0 = torch.from_numpy(w.y).to(dev, tdt)
-    A0 = torch.from_numpy(w.A).to(dev, tdt)
-    B0 = [torch.from_numpy(b).to(dev, tdt) for b in w.B]
-    ids0 = torch.from_numpy(w.ids).to(dev)
-    ranks = None if w.ranks is None else torch.from_numpy(w.ranks).to(dev)
-    ascale = None if w.adapter_scale is None else torch.from_numpy(w.adapter_scale).to(dev)
-    ws_bytes = B.lora_workspace_size(w.M, w.n_adapters, w.chunk_size)
-    sets = []
-    for i in range(n_sets):
-        sets.append({
-            "x": x0 if i == 0 else x0.clone(), "y": y0 if i == 0 else y0.clone(),
-            "A": A0 if i == 0 else A0.clone(), "B": B0 if i == 0 else [b.clone() for b in B0],
-            "ids": ids0 if i == 0 else ids0.clone(),
-            "ws": torch.empty(ws_bytes, dtype=torch.uint8, device=dev),
-        })
     stream = torch.cuda.Stream(device=dev)
+    b = Bench(w, args, dev, stream, args.path)
 
-    def step(s):
-        batch = B.lora_prepare_batch(s["ids"], w.n_adapters, w.chunk_size, workspace=s["ws"],
-                                     stream=stream)
-        B.lora_delta(batch, s["x"], s["A"], s["B"], s["y"], scale=w.scale,
-                     adapter_scale=ascale, ranks=ranks, path=args.path, stream=stream)
-        return batch
-
-    with torch.cuda.stream(stream):
-        for i in range(W):
-            step(sets[i % n_sets])
-    stream.synchronize()
-    b0 = B.lora_prepare_batch(sets[0]["ids"], w.n_adapters, w.chunk_size, workspace=sets[0]["ws"],
-                              stream=stream)
-    stream.synchronize()
-    counts = b0.counts()
-    n_launch0 = B.lora_launch_count()
-    step(sets[0])
-    launches_per_step = B.lora_launch_count() - n_launch0
-    stream.synchronize()
-
-    # Graphs of G steps with event nodes around each kernel.
-    G = max(1, min(args.graph_steps, K))
-    use_graph = True
-    try:
-        probe = torch.cuda.Event(enable_timing=True, external=True)
-        del probe
-    except TypeError:
-        use_graph = False
-
-    # The dominant kernel alone: when one kernel takes every active row, the
-    # path forced to it launches exactly that kernel with the same work.
-    dom_path = None
-    if args.path == 0 and counts["num_active"] > 0:
-        if counts["tc_rows"] == counts["num_active"]:
-            dom_path = 2
-        elif counts["tc_rows"] == 0:
-            dom_path = 1
-
-    def capture(nsteps, offset, timed, path=None):
-        """Graph of `nsteps` steps.  With `timed`, event nodes bracket every
-        kernel (they also cut the programmatic overlap between kernels, so
-        the step-time graph has none)."""
-        path = args.path if path is None else path
-        evs = [(torch.cuda.Event(enable_timing=True, external=True),
-                torch.cuda.Event(enable_timing=True, external=True),
-                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(nsteps if timed else 0)]
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
-            for i in range(nsteps):
-                s = sets[(offset + i) % n_sets]
-                if timed:
-                    evs[i][0].record(stream)
-                batch = B.lora_prepare_batch(s["ids"], w.n_adapters, w.chunk_size,
-                                             workspace=s["ws"], stream=stream)
-                if timed:
-                    evs[i][1].record(stream)
-                B.lora_delta(batch, s["x"], s["A"], s["B"], s["y"], scale=w.scale,
-                             adapter_scale=ascale, ranks=ranks, path=path, stream=stream)
-                if timed:
-                    evs[i][2].record(stream)
-        return g, evs
-
-    reps, rem = divmod(K, G)
-    if use_graph:
-        g_main, _ = capture(G, 0, False)
-        g_rem, _ = capture(rem, 0, False) if rem else (None, [])
-        g_kern, ev_main = capture(G, 0, True)
-        g_dom, ev_dom = capture(G, 0, True, dom_path) if dom_path is not None else (None, [])
-        with torch.cuda.stream(stream):
-            g_main.replay()
-            g_kern.replay()
-            if g_dom is not None:
-                g_dom.replay()
-        stream.synchronize()
-
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     clocks = ClockSampler(vis.split(",")[local_rank].strip() if vis else str(local_rank))
-    clocks.start()
-    time.sleep(0.3)
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    wall0 = time.perf_counter()
-    t_start.record(stream)
-    if use_graph:
-        with torch.cuda.stream(stream):     # a graph replays on the current stream
-            for _ in range(reps):
-                g_main.replay()
-            if g_rem is not None:
-                g_rem.replay()
-    else:
-        with torch.cuda.stream(stream):
-            for i in range(K):
-                step(sets[i % n_sets])
-    t_end.record(stream)
-    t_end.synchronize()
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
-    wall = time.perf_counter() - wall0
-    clk = clocks.stop()
-    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
+    m = measure(b, args.workload, K, W, world, dev, args.graph_steps, clocks=clocks)
+    e2e = e2e_measure(b, args.e2e_steps)
+    del b
+    torch.cuda.empty_cache()
 
-    # Kernel durations: the same steps replayed once more with event nodes
-    # around every kernel, right after the timed region.
-    prep_us, delta_us, dom_us = [], [], []
-    if use_graph:
-        with torch.cuda.stream(stream):
-            g_kern.replay()
-            if g_dom is not None:
-                g_dom.replay()
-        stream.synchronize()
-        for e0, e1, e2 in ev_main:
-            prep_us.append(1e3 * e0.elapsed_time(e1))
-            delta_us.append(1e3 * e1.elapsed_time(e2))
-        for e0, e1, e2 in ev_dom:
-            dom_us.append(1e3 * e1.elapsed_time(e2))
-    ms_per_step = elapsed_ms / K
-    value = whole_job_tokens_per_s(world, K, w.M, elapsed_ms)
-
-    # e2e: the public API from pinned host buffers, copies inside the region.
-    x_h = torch.from_numpy(w.x).to(tdt).pin_memory()
-    y_h = torch.from_numpy(w.y).to(tdt).pin_memory()
-    ids_h = torch.from_numpy(w.ids).pin_memory()
-    y_out = torch.empty_like(y_h).pin_memory()
-    s0 = sets[0]
-    E = args.e2e_steps
-    with torch.cuda.stream(stream):
-        for i in range(3 + E):
-            if i == 3:
-                stream.synchronize()
-                e_a = torch.cuda.Event(enable_timing=True)
-                e_b = torch.cuda.Event(enable_timing=True)
-                e_a.record(stream)
-            s0["x"].copy_(x_h, non_blocking=True)
-            s0["y"].copy_(y_h, non_blocking=True)
-            s0["ids"].copy_(ids_h, non_blocking=True)
-            step(s0)
-            y_out.copy_(s0["y"], non_blocking=True)
-        e_b.record(stream)
-    e_b.synchronize()
-    e2e_ms = e_a.elapsed_time(e_b) / E
-    h2d = (x_h.numel() + y_h.numel()) * es + ids_h.numel() * 4
-    d2h = y_out.numel() * es
-
-    peak, peak_kind = load_peaks()
-    d_us = statistics.mean(delta_us) if delta_us else None
-    k_us = statistics.mean(dom_us) if dom_us else d_us
-    achieved = ab["total"] / (k_us * 1e-6) / 1e9 if k_us else None
-    # dominant kernel: the tensor-core one when most active rows are in its segments
-    kernel = "sgmv_tc_kernel" if 2 * counts["tc_rows"] > max(1, counts["num_active"]) else "sgmv_cc_kernel"
-    traffic = committed_traffic(kernel, args.workload)
+    others = {}
+    if not args.no_extras and args.path == 0:
+        for name, (fac, _) in WORKLOADS.items():
+            if name == args.workload:
+                continue
+            wo = fac(replica_seed(rank))
+            bo = Bench(wo, args, dev, stream, 0)
+            mo = measure(bo, name, args.extra_steps, W, world, dev, args.graph_steps, kernel_events=False)
+            others[name] = summary(mo)
+            del bo
+            torch.cuda.empty_cache()
 
     if rank != 0:
         return
+    ab, r = m["ab"], m["roofline"]
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
-        "warmup": W, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": m["value"], "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": m["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {
             "workload": w.name, "tokens_per_step": w.M, "active_rows": ab["active_rows"],
-            "touched_adapters": ab["touched_adapters"], "num_segs": counts["num_segs"],
+            "touched_adapters": ab["touched_adapters"], "num_segs": m["counts"]["num_segs"],
             "chunk_size": w.chunk_size, "path": ["auto", "cuda_core", "tensor"][args.path],
             "l2": "inputs rotate over %d sets (%.0f MB > %d MB L2)"
-                  % (n_sets, n_sets * set_bytes / 1e6, L2_BYTES // 2**20),
-            "timing": ("CUDA graphs of %d steps (kernels chained by programmatic dependent "
-                       "launch); kernel durations from a replay of the same steps with event "
-                       "nodes around each kernel" % G) if use_graph else "eager launches",
+                  % (m["n_sets"], m["n_sets"] * b_set_bytes(w) / 1e6, L2_BYTES // 2**20),
+            "timing": ("CUDA graphs of %d steps (kernels chained by programmatic dependent launch), "
+                       "a device-side delay before the start event so the host's submission is "
+                       "not timed" % m["graph_steps"]),
             "parallelism": "replicas: one independent batch per GPU" if world > 1 else "single GPU",
         },
-        "kernels_us": {"prepare_mean": statistics.mean(prep_us) if prep_us else None,
-                       "delta_mean": d_us,
-                       "delta_median": statistics.median(delta_us) if delta_us else None,
-                       "kernel_mean": k_us},
+        "kernels_us": m["kernels_us"],
         "algorithmic_bytes_per_step": ab["total"],
         "algorithmic_bytes_padded_rank": ab["total_padded_rank"],
-        "hbm_gbs_delta": ab["total"] / (d_us * 1e-6) / 1e9 if d_us else None,
-        "frac_of_8tbs_delta": ab["total"] / (d_us * 1e-6) / 1e9 / NOMINAL_HBM_GBS if d_us else None,
-        "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": peak,
-                     "peak_kind": peak_kind, "unit": "GB/s",
-                     "duration": ("mean event time of %s alone: a replay of the same steps with "
-                                  "the path forced to it, which then does the same work (it "
-                                  "takes every active row)" % kernel) if dom_us else
-                                 "mean event time of the lora_delta call (its CUDA-core and "
-                                 "tensor-core launches together: both have rows)",
-                     "frac": achieved / peak if achieved else None, "traffic": traffic},
-        "e2e": {"value": w.M / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": K * launches_per_step,
-        "launches_per_step": launches_per_step,
-        "clocks": clk,
-        "wall_s_timed": wall,
+        "step_gbs": m["step_gbs"],
+        "step_frac_of_8tbs": m["step_gbs"] / NOMINAL_HBM_GBS,
+        "roofline": {k: r[k] for k in ("bound", "kernel", "achieved", "peak", "peak_kind", "unit",
+                                      "frac", "traffic", "duration")},
+        "e2e": {k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step",
+                                   "ms_per_step")},
+        "gpu_launches": K * m["launches_per_step"],
+        "launches_per_step": m["launches_per_step"],
+        "clocks": m["clocks"],
+        "wall_s_timed": m["wall_s_timed"],
     }
+    if others:
+        line["other_workloads"] = others
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     print(json.dumps(line), flush=True)
+
+
+def b_set_bytes(w: wl.Workload) -> int:
+    es = 2 if w.dtype == "bf16" else 4
+    return (w.x.size + w.y.size + w.A.size + sum(b.size for b in w.B)) * es
 
 
 def main():

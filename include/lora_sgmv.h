@@ -339,6 +339,16 @@ int32_t lora_abi_version(void);
  * capture). */
 int64_t lora_launch_count(void);
 
+/* Kernels of the library (bits of lora_last_kernels). */
+#define LORA_KERNEL_PREPARE 1   /* segment metadata (lora_prepare_batch*) */
+#define LORA_KERNEL_SMALL 2     /* small-batch fused kernel: rows grouped on chip */
+#define LORA_KERNEL_CUDA_CORE 4 /* small-segment kernel (clusters, warp-level tiles) */
+#define LORA_KERNEL_TENSOR 8    /* tcgen05 kernel for long segments */
+
+/* The kernels the calling thread's last call of this library enqueued, as a
+ * bit set of LORA_KERNEL_* (0 if it enqueued none; a diagnostic). */
+int32_t lora_last_kernels(void);
+
 #ifdef __cplusplus
 }
 #endif

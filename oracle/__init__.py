@@ -49,7 +49,10 @@ def build(force: bool = False) -> str:
     tmp = _LIB_PATH + ".tmp.%d" % os.getpid()
     cmd = ["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-fno-fast-math",
            "-ffp-contract=off", _SRC, "-o", tmp]
-    subprocess.run(cmd, check=True)
+    # OpenMP shares the rows of delta_parallel out over host threads; without
+    # it that function runs on one thread (same result either way)
+    if subprocess.run(cmd[:1] + ["-fopenmp"] + cmd[1:], capture_output=True).returncode != 0:
+        subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -68,7 +71,8 @@ def _load():
             lib.oracle_prepare_batch_ordered.argtypes = [
                 i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                 i32p, i32p, i32p, i32p, i32p]
-            for fn in (lib.oracle_shrink, lib.oracle_expand, lib.oracle_delta):
+            for fn in (lib.oracle_shrink, lib.oracle_expand, lib.oracle_delta,
+                       lib.oracle_delta_parallel):
                 fn.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -209,8 +213,12 @@ def expand(h, ids, B_pools, y_base, scale=1.0, adapter_scale=None,
 
 
 def delta(x, ids, A_pool, B_pools, y_base, scale=1.0, adapter_scale=None,
-          ranks=None, return_h=False):
-    """y = y_base + s_id (x_i . A_id^T) . B_id^T, token by token (fp64)."""
+          ranks=None, return_h=False, threads=1):
+    """y = y_base + s_id (x_i . A_id^T) . B_id^T, token by token (fp64).
+
+    ``threads`` > 1 shares the token rows out over that many host threads
+    (``oracle_delta_parallel``: the same per-row arithmetic, bit-identical
+    result); the number of threads used is then in ``delta.last_threads``."""
     lib = _load()
     if not isinstance(B_pools, (list, tuple)):
         B_pools = [B_pools]
@@ -226,6 +234,23 @@ def delta(x, ids, A_pool, B_pools, y_base, scale=1.0, adapter_scale=None,
     y = np.array(y_base, dtype=np.float64, copy=True).reshape(M, sl.total)
     rk = None if ranks is None else _i32(ranks)
     sc, asc = _scale_args(scale, adapter_scale)
+    if threads > 1 and not return_h:
+        used = ctypes.c_int32(0)
+        rc = lib.oracle_delta_parallel(
+            ctypes.c_int32(M), ctypes.c_int32(d_in), ctypes.c_int32(r_max),
+            _ptr(x, ctypes.c_float), ctypes.c_int64(d_in), _ptr(ids, ctypes.c_int32),
+            ctypes.c_int32(n), _ptr(A, ctypes.c_float),
+            ctypes.c_int64(r_max * d_in), ctypes.c_int64(d_in),
+            _ptr(rk, ctypes.c_int32), ctypes.c_double(sc), _ptr(asc, ctypes.c_double),
+            ctypes.c_int32(sl.n), sl.ptrs, _ptr(sl.s_adapter, ctypes.c_int64),
+            _ptr(sl.s_n, ctypes.c_int64), _ptr(sl.d_out, ctypes.c_int32),
+            _ptr(sl.col_off, ctypes.c_int32), _ptr(y, ctypes.c_double),
+            ctypes.c_int64(sl.total), ctypes.c_int32(int(threads)), ctypes.byref(used))
+        if rc != 0:
+            raise ValueError("oracle_delta_parallel rejected its arguments")
+        delta.last_threads = int(used.value)
+        return y
+    delta.last_threads = 1
     h = np.full((M, r_max), np.nan, np.float64) if return_h else None
     rc = lib.oracle_delta(
         ctypes.c_int32(M), ctypes.c_int32(d_in), ctypes.c_int32(r_max),

@@ -44,6 +44,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define ORACLE_OK 0
 #define ORACLE_ERR (-1)
@@ -264,3 +267,54 @@ int oracle_delta(int32_t M, int32_t d_in, int32_t r_max, const float *x,
     free(hrow);
     return rc;
 }
+
+/*
+ * The same fused delta with the token rows shared out over `threads` host
+ * threads (OpenMP when the oracle is built with it; otherwise one thread).
+ * Every row runs exactly the arithmetic of oracle_delta -- rows are
+ * independent and each writes only its own y row -- so the result is
+ * bit-identical; only the time differs.  Returns the threads used.
+ */
+int oracle_delta_parallel(int32_t M, int32_t d_in, int32_t r_max, const float *x,
+                          int64_t ldx, const int32_t *ids, int32_t n_adapters,
+                          const float *A, int64_t sA_adapter, int64_t sA_r,
+                          const int32_t *ranks, double scale,
+                          const double *adapter_scale, int32_t n_slices,
+                          const float *const *B, const int64_t *sB_adapter,
+                          const int64_t *sB_n, const int32_t *d_out,
+                          const int32_t *col_off, double *y, int64_t ldy,
+                          int32_t threads, int32_t *threads_used)
+{
+    int rc_all = ORACLE_OK, used = 1;
+    if (threads < 1)
+        threads = 1;
+#ifdef _OPENMP
+#pragma omp parallel num_threads(threads)
+#endif
+    {
+        int rc = ORACLE_OK;
+#ifdef _OPENMP
+#pragma omp single
+        used = omp_get_num_threads();
+#pragma omp for schedule(dynamic, 4)
+#endif
+        for (int32_t i = 0; i < M; ++i) {
+            if (rc != ORACLE_OK)
+                continue;
+            rc = oracle_delta(1, d_in, r_max, x + (int64_t)i * ldx, ldx, ids + i, n_adapters, A,
+                              sA_adapter, sA_r, ranks, scale, adapter_scale, n_slices, B,
+                              sB_adapter, sB_n, d_out, col_off, y + (int64_t)i * ldy, ldy,
+                              NULL, 0);
+        }
+        if (rc != ORACLE_OK) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+            rc_all = rc;
+        }
+    }
+    if (threads_used)
+        *threads_used = used;
+    return rc_all;
+}
+

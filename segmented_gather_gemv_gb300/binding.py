@@ -39,6 +39,9 @@ MAX_SLICES = 4
 COUNT_NAMES = ("num_segs", "num_active", "num_invalid", "num_small_segs",
                "num_tc_segs", "tc_rows", "device_error", "num_groups")
 DEVERR_RANK, DEVERR_WAIT = 1, 2
+KERNEL_PREPARE, KERNEL_SMALL, KERNEL_CUDA_CORE, KERNEL_TENSOR = 1, 2, 4, 8
+KERNEL_NAMES = {KERNEL_PREPARE: "prepare_kernel", KERNEL_SMALL: "sgmv_small_kernel",
+                KERNEL_CUDA_CORE: "sgmv_cc_kernel", KERNEL_TENSOR: "sgmv_tc_kernel"}
 
 _STATUS = {LORA_ERR_INVALID: "invalid argument", LORA_ERR_UNSUPPORTED: "unsupported",
            LORA_ERR_WORKSPACE: "workspace too small", LORA_ERR_CUDA: "CUDA error"}
@@ -112,6 +115,8 @@ def lib() -> ctypes.CDLL:
             L.lora_last_error_string.argtypes = []
             L.lora_abi_version.restype = ctypes.c_int32
             L.lora_launch_count.restype = ctypes.c_int64
+            L.lora_last_kernels.restype = ctypes.c_int32
+            L.lora_last_kernels.argtypes = []
             _lib = L
     return _lib
 
@@ -226,6 +231,11 @@ class Batch:
 def lora_launch_count() -> int:
     """Kernel launches the library has enqueued in this process."""
     return int(lib().lora_launch_count())
+
+
+def lora_last_kernels() -> int:
+    """Bit set (KERNEL_*) of the kernels the calling thread's last call enqueued."""
+    return int(lib().lora_last_kernels())
 
 
 def lora_workspace_size(M: int, n_adapters: int, chunk_size: int = 0) -> int:

@@ -31,6 +31,7 @@ using namespace lora;
 namespace {
 
 thread_local char g_err[512];
+thread_local int32_t g_last_kernels = 0;  // LORA_KERNEL_* bits of the last call
 
 lora_status_t fail(lora_status_t code, const char *fmt, ...) {
     va_list ap;
@@ -150,6 +151,7 @@ void fill_batch(const lora_batch_t *b, DeltaArgs &p) {
 // Launches the kernels of one call according to the path.
 lora_status_t dispatch(const lora_batch_t *b, int32_t dtype, int mode, int32_t path, int d_in, DeltaArgs &p,
                        cudaStream_t stream) {
+    g_last_kernels = 0;
     fill_batch(b, p);
     if (b->M == 0) return LORA_OK;
     const int sms = sm_count();
@@ -171,6 +173,7 @@ lora_status_t dispatch(const lora_batch_t *b, int32_t dtype, int mode, int32_t p
         if (try_launch_small(p, sms, stream, &e)) {
             if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
             launch_counter().fetch_add(1, std::memory_order_relaxed);
+            g_last_kernels = LORA_KERNEL_SMALL;
             return LORA_OK;
         }
     }
@@ -188,7 +191,10 @@ lora_status_t dispatch(const lora_batch_t *b, int32_t dtype, int mode, int32_t p
         p.tc_rows_index = LORA_COUNT_ACTIVE;
         p.tc_only = 1;
         e = launch_tc(p, mode, tc_grid(b->M), stream);
-        if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
+        if (e == cudaSuccess) {
+            launch_counter().fetch_add(1, std::memory_order_relaxed);
+            g_last_kernels |= LORA_KERNEL_TENSOR;
+        }
     } else {
         const bool split = path == LORA_PATH_AUTO && tensor_ok && mode == kFused;
         p.min_len = 0;
@@ -208,7 +214,10 @@ lora_status_t dispatch(const lora_batch_t *b, int32_t dtype, int mode, int32_t p
         if (cc_first) {
             // leaves the tensor-core grid and the next prepare an SM each
             e = launch_cc(p, dtype, mode, cluster, sms - g - 1, stream);
-            if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
+            if (e == cudaSuccess) {
+                launch_counter().fetch_add(1, std::memory_order_relaxed);
+                g_last_kernels |= LORA_KERNEL_CUDA_CORE;
+            }
         }
         if (with_tc && e == cudaSuccess) {
             DeltaArgs q = p;
@@ -223,13 +232,19 @@ lora_status_t dispatch(const lora_batch_t *b, int32_t dtype, int mode, int32_t p
             q.tc_share = share_table(b->counts);
             q.tc_share_grid = g <= kMaxShareGrid ? g : -1;
             e = launch_tc(q, mode, g, stream);
-            if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
+            if (e == cudaSuccess) {
+                launch_counter().fetch_add(1, std::memory_order_relaxed);
+                g_last_kernels |= LORA_KERNEL_TENSOR;
+            }
         }
         if (e == cudaSuccess && !cc_first) {
             p.after_tc = with_tc ? 1 : 0;
             // beside a tensor-core grid, the SMs that grid leaves free
             e = launch_cc(p, dtype, mode, cluster, with_tc ? sms - g : sms, stream);
-            if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
+            if (e == cudaSuccess) {
+                launch_counter().fetch_add(1, std::memory_order_relaxed);
+                g_last_kernels |= LORA_KERNEL_CUDA_CORE;
+            }
         }
     }
     if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
@@ -256,6 +271,7 @@ lora_status_t lora_prepare_batch_ordered(const int32_t *ids, int32_t M, int32_t 
                                          int32_t tc_min_rows, int32_t order, void *workspace,
                                          size_t workspace_bytes, lora_batch_t *batch, void *stream) {
     g_err[0] = 0;
+    g_last_kernels = 0;
     if (order != LORA_ORDER_FIRST_APPEARANCE && order != LORA_ORDER_ASCENDING)
         return fail(LORA_ERR_INVALID, "order %d is not a LORA_ORDER_* value", order);
     if (!batch) return fail(LORA_ERR_INVALID, "batch is NULL");
@@ -277,6 +293,7 @@ lora_status_t lora_prepare_batch_ordered(const int32_t *ids, int32_t M, int32_t 
                                    static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "prepare launch failed: %s", cudaGetErrorString(e));
     launch_counter().fetch_add(1, std::memory_order_relaxed);
+    g_last_kernels = LORA_KERNEL_PREPARE;
     b.M = M;
     b.n_adapters = n_adapters;
     b.chunk_size = chunk_size;
@@ -361,6 +378,8 @@ const char *lora_last_error_string(void) { return g_err; }
 int32_t lora_abi_version(void) { return 100; }
 
 int64_t lora_launch_count(void) { return launch_counter().load(std::memory_order_relaxed); }
+
+int32_t lora_last_kernels(void) { return g_last_kernels; }
 
 }  // extern "C"
 

@@ -64,6 +64,17 @@ constexpr int kSmMaxRows = 1024;  // rows a batch may have for this kernel (two 
 constexpr int kSmRT = 16;         // rows per tile: one 16-row MMA tile
 constexpr int kSmNtBatch = 4;     // 8-column tiles a warp keeps in flight in the expand
 
+// The CTA's columns [n0, n1) by output slice t: columns [cb, ce) (ce <= cb:
+// the slice has none of them), y column = column + go, B rows at byte off of
+// the B block with a row pitch of str bytes.  Computed on the host for every
+// cluster rank and read from the launch parameters.
+struct PieceTab {
+    int cb[LORA_MAX_SLICES], ce[LORA_MAX_SLICES], str[LORA_MAX_SLICES], go[LORA_MAX_SLICES];
+    uint32_t off[LORA_MAX_SLICES];
+};
+
+constexpr int kSmMaxCluster = 8;
+
 struct SmGeom {
     int CL;              // CTAs per cluster
     int KC;              // shrink columns per CTA
@@ -72,17 +83,10 @@ struct SmGeom {
     int HS;              // hash slots (power of two, >= 2 M)
     int tcap;            // tile records per CTA
     uint32_t ncl_magic;  // ceil(2^32 / clusters): x / clusters = umulhi(x, magic) for x < 2^16
-    int off_bars, off_key, off_first, off_cnt, off_scan, off_tl, off_rows, off_pt, off_red, off_recv, off_hbf, off_A,
-        off_x, off_y, off_B, total;
-};
-
-// The CTA's columns [n0, n1) by output slice t: columns [cb, ce) (ce <= cb:
-// the slice has none of them), y column = column + go, B rows at byte off of
-// the B block with a row pitch of str bytes.  Kept in shared memory: the
-// kernel's registers go to the tiles in flight.
-struct PieceTab {
-    int cb[LORA_MAX_SLICES], ce[LORA_MAX_SLICES], str[LORA_MAX_SLICES], go[LORA_MAX_SLICES];
-    uint32_t off[LORA_MAX_SLICES];
+    int ncol0[kSmMaxCluster + 1];  // first expand column of cluster rank q (multiples of 8)
+    PieceTab pt[kSmMaxCluster];    // the slices of each cluster rank's columns
+    int off_bars, off_key, off_first, off_cnt, off_scan, off_tl, off_rows, off_red, off_recv, off_hbf, off_A, off_x,
+        off_y, off_B, total;
 };
 
 // One tile of this cluster: adapter, rank, first and last row (exclusive)
@@ -192,7 +196,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     int32_t *wsum2 = wsum + 32;                                         // [kSmWarps]
     TileRec *tl = reinterpret_cast<TileRec *>(smem + g.off_tl);        // [tcap]
     int32_t *rows_s = reinterpret_cast<int32_t *>(smem + g.off_rows);  // [kSmRT]
-    PieceTab *pt = reinterpret_cast<PieceTab *>(smem + g.off_pt);
+    const PieceTab *pt = &g.pt[cluster_ctarank()];  // launch parameters
     float *red = reinterpret_cast<float *>(smem + g.off_red);          // [warps][16][20]
     float *recv = reinterpret_cast<float *>(smem + g.off_recv);        // [2][CL][16][R16]
     unsigned char *hbf = smem + g.off_hbf;                              // [16][R16 + 8] bf16
@@ -258,28 +262,6 @@ __global__ void __launch_bounds__(kSmThreads, 1)
             atomicMin(&first[s], tid * RPT + k);
             atomicAdd(&cnt[s], 1);
             slot[k] = s;
-        }
-    }
-    if (tid == kSmThreads - 1) {
-        // the piece table (published by the barrier below)
-        const int nv8 = p.d_out_total / 8;
-        const int c0 = (int)((int64_t)nv8 * q / CL) * 8, c1 = (int)((int64_t)nv8 * (q + 1) / CL) * 8;
-        uint32_t run = 0;
-        for (int t = 0; t < LORA_MAX_SLICES; ++t) {
-            int cb = 0, ce = 0, str = 0, go = 0;
-            if (t < p.n_slices) {
-                const SliceDesc &sl = p.slices[t];
-                cb = max(c0, sl.col_begin);
-                ce = min(c1, sl.col_begin + sl.d_out);
-                str = (int)sl.stride_n * 2;
-                go = sl.y_col - sl.col_begin;
-            }
-            pt->cb[t] = cb;
-            pt->ce[t] = ce;
-            pt->str[t] = str;
-            pt->go[t] = go;
-            pt->off[t] = run;
-            if (cb < ce) run += (uint32_t)(ce - cb) * (uint32_t)str;
         }
     }
     __syncthreads();
@@ -351,8 +333,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         (int)cid < T ? min((int)__umulhi((uint32_t)(T - 1 - (int)cid), g.ncl_magic) + 1, g.tcap) : 0;
 
     const int k0 = (int)q * g.KC;
-    const int nv = p.d_out_total / 8;
-    const int n0 = (int)((int64_t)nv * q / CL) * 8, n1 = (int)((int64_t)nv * (q + 1) / CL) * 8;
+    const int n0 = g.ncol0[q], n1 = g.ncol0[q + 1];
     const int ncols = n1 - n0;
     const int kc8 = g.KC / 8;
 
@@ -712,6 +693,28 @@ static bool small_geometry(const DeltaArgs &p, int R16, int cl, int ncl, SmGeom 
     for (int t = 0; t < p.n_slices; ++t) max_stride = std::max(max_stride, (int)p.slices[t].stride_n);
     g.HS = pow2_at_least(std::max(64, 2 * M));
     g.tcap = (M + ncl - 1) / ncl + 1;
+    if (cl > kSmMaxCluster) return false;
+    for (int qq = 0; qq <= cl; ++qq) g.ncol0[qq] = (int)((int64_t)nv * qq / cl) * 8;
+    for (int qq = 0; qq < cl; ++qq) {
+        PieceTab &t = g.pt[qq];
+        uint32_t run = 0;
+        for (int u = 0; u < LORA_MAX_SLICES; ++u) {
+            int cb = 0, ce = 0, str = 0, go = 0;
+            if (u < p.n_slices) {
+                const SliceDesc &sl = p.slices[u];
+                cb = std::max(g.ncol0[qq], sl.col_begin);
+                ce = std::min(g.ncol0[qq + 1], sl.col_begin + sl.d_out);
+                str = (int)sl.stride_n * 2;
+                go = sl.y_col - sl.col_begin;
+            }
+            t.cb[u] = cb;
+            t.ce[u] = ce;
+            t.str[u] = str;
+            t.go[u] = go;
+            t.off[u] = run;
+            if (cb < ce) run += (uint32_t)(ce - cb) * (uint32_t)str;
+        }
+    }
     g.ncl_magic = (uint32_t)((0x100000000ull + (uint64_t)ncl - 1) / (uint64_t)ncl);
     g.xpitch = g.KC * 2 + 16;
     g.ypitch = g.NCmax * 2 + 16;
@@ -728,7 +731,6 @@ static bool small_geometry(const DeltaArgs &p, int R16, int cl, int ncl, SmGeom 
     g.off_scan = take(64 * 4);
     g.off_tl = take((size_t)g.tcap * sizeof(TileRec));
     g.off_rows = take(kSmRT * 4);
-    g.off_pt = take(sizeof(PieceTab));
     g.off_red = take((size_t)kSmWarps * 16 * 20 * 4);
     g.off_recv = take((size_t)2 * cl * 16 * R16 * 4);
     g.off_hbf = take((size_t)16 * (R16 + 8) * 2);

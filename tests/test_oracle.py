@@ -313,3 +313,20 @@ def test_round_bf16_matches_torch():
     ours = wl.round_bf16(v)
     ref = torch.from_numpy(v).to(torch.bfloat16).to(torch.float32).numpy()
     assert np.array_equal(ours, ref)
+
+
+@pytest.mark.parametrize("case", range(3))
+def test_parallel_delta_is_bit_identical(case):
+    # the all-core variant shares the rows out over host threads; each row's
+    # arithmetic is that of the serial loop, so the results must be identical
+    kw = [dict(M=300, d_in=96, d_outs=[64, 32], n_pool=7, r_max=16, skip_frac=0.2, bad_frac=0.05),
+          dict(M=129, d_in=64, d_outs=[40], n_pool=9, r_max=32, ranks=[8, 16, 24, 32],
+               per_adapter_scale=True),
+          dict(M=1, d_in=32, d_outs=[16], n_pool=2, r_max=8)][case]
+    w = wl.random_batch(seed=900 + case, dtype="f32", **kw)
+    y1 = oracle.delta(w.x, w.ids, w.A, w.B, w.y, scale=w.scale, adapter_scale=w.adapter_scale,
+                      ranks=w.ranks)
+    y4 = oracle.delta(w.x, w.ids, w.A, w.B, w.y, scale=w.scale, adapter_scale=w.adapter_scale,
+                      ranks=w.ranks, threads=4)
+    assert np.array_equal(y1, y4)
+    assert oracle.delta.last_threads >= 1
