@@ -54,6 +54,10 @@
  *  - y is rounded once: fp32(y) + delta, converted to y's type (round to
  *    nearest even).
  *
+ * Device state: the library keeps per-device set-up (kernel attributes,
+ * occupancy figures, the static workspace's device address) for the life
+ * of the process; it assumes no cudaDeviceReset while it is in use.
+ *
  * Errors: every call returns lora_status_t.  Host-side argument checks
  * return LORA_ERR_INVALID / LORA_ERR_UNSUPPORTED / LORA_ERR_WORKSPACE
  * before anything is enqueued; a failed kernel launch returns
@@ -250,8 +254,10 @@ lora_status_t lora_prepare_batch_ordered(const int32_t *ids, int32_t M, int32_t 
  *
  * Arguments and result are those of lora_prepare_batch, without workspace
  * and workspace_bytes.  The batch needs lora_workspace_size(M, n_adapters,
- * chunk_size) <= LORA_STATIC_WORKSPACE_BYTES (4 MiB: for example M up to
- * 131072 rows with 4096 adapters unchunked); a larger batch returns
+ * chunk_size) <= LORA_STATIC_WORKSPACE_BYTES (4 MiB: about 4 bytes per
+ * row plus a fixed part that grows with n_adapters, so for example up to
+ * about 710000 rows with 4096 adapters unchunked, 420000 with 64-row
+ * chunks); a larger batch returns
  * LORA_ERR_WORKSPACE and launches nothing.  The call allocates no memory:
  * no cudaMalloc, no cudaFree, no allocating library routine.
  *
@@ -314,10 +320,8 @@ lora_status_t lora_expand(const lora_batch_t *batch, int32_t dtype,
  * launch): they must be final before the kernel preceding this call starts
  * (adapter weights loaded earlier, ids from a copy or an earlier kernel).
  * x and y are read only after that wait.
- * Non-finite y: on the tensor-core path y enters the fp32 accumulator through
- * an MMA with a 16 x 16 identity, so a NaN or infinity in y[i, n] turns the
- * other outputs of row i in the same aligned 16-column group of the 128-column
- * tile into NaN (0 * inf); finite y is added exactly.
+ * Non-finite y: every path adds y per element, so a NaN or infinity in
+ * y[i, n] gives a non-finite result there and nowhere else.
  */
 lora_status_t lora_delta(const lora_batch_t *batch, int32_t dtype,
                          const void *x, int64_t ldx, int32_t d_in,
@@ -348,6 +352,16 @@ int64_t lora_launch_count(void);
 /* The kernels the calling thread's last call of this library enqueued, as a
  * bit set of LORA_KERNEL_* (0 if it enqueued none; a diagnostic). */
 int32_t lora_last_kernels(void);
+
+/*
+ * Diagnostic of the bounded device waits.  Enqueues one CTA that waits, with
+ * the same bounded wait the kernels use on their mbarriers, on a barrier that
+ * nothing completes (no copy is in flight); the wait gives up after its limit
+ * (about 0.1 s) and the CTA sets LORA_DEVERR_WAIT in counts[LORA_COUNT_DEVERR]
+ * and returns.  counts: device int32[LORA_NUM_COUNTS] (the caller's; a batch's
+ * counts work).  The context stays usable afterwards.
+ */
+lora_status_t lora_selftest_wait(int32_t *counts, void *stream);
 
 #ifdef __cplusplus
 }

@@ -117,6 +117,8 @@ def lib() -> ctypes.CDLL:
             L.lora_launch_count.restype = ctypes.c_int64
             L.lora_last_kernels.restype = ctypes.c_int32
             L.lora_last_kernels.argtypes = []
+            L.lora_selftest_wait.restype = ctypes.c_int
+            L.lora_selftest_wait.argtypes = [vp, vp]
             _lib = L
     return _lib
 
@@ -148,6 +150,11 @@ def _dev_ptr(t: Optional[torch.Tensor], what: str, dtype=None) -> Optional[int]:
         return None
     if not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % what)
+    # the library launches on the current device (and keeps a static
+    # workspace per device): tensors of another device would be read across
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError("%s is on cuda:%d, the current device is cuda:%d"
+                         % (what, t.device.index, torch.cuda.current_device()))
     if dtype is not None and t.dtype != dtype:
         raise TypeError("%s must be %s" % (what, dtype))
     return t.data_ptr()
@@ -233,6 +240,13 @@ def lora_launch_count() -> int:
     return int(lib().lora_launch_count())
 
 
+def lora_selftest_wait(counts: torch.Tensor, stream=None) -> None:
+    """Run the bounded-wait diagnostic: sets DEVERR_WAIT in counts[6]."""
+    if counts.dtype != torch.int32 or not counts.is_cuda or counts.numel() < len(COUNT_NAMES):
+        raise ValueError("counts must be a CUDA int32 tensor of %d entries" % len(COUNT_NAMES))
+    _check(lib().lora_selftest_wait(ctypes.c_void_p(counts.data_ptr()), ctypes.c_void_p(_stream(stream))))
+
+
 def lora_last_kernels() -> int:
     """Bit set (KERNEL_*) of the kernels the calling thread's last call enqueued."""
     return int(lib().lora_last_kernels())
@@ -259,9 +273,10 @@ def lora_prepare_batch(ids: torch.Tensor, n_adapters: int, chunk_size: int = 0,
         raise LoraError(LORA_ERR_INVALID, "bad batch size arguments")
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=ids.device if M else "cuda")
+    ws_ptr = _dev_ptr(workspace, "workspace")
     raw = _Batch()
     _check(lib().lora_prepare_batch_ordered(ids_ptr, M, int(n_adapters), int(chunk_size), int(tc_min_rows),
-                                            int(order), workspace.data_ptr(),
+                                            int(order), ws_ptr,
                                             workspace.numel() * workspace.element_size(),
                                             ctypes.byref(raw), _stream(stream)))
     return Batch(raw, workspace, ids)

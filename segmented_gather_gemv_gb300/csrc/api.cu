@@ -28,6 +28,18 @@ std::atomic<int64_t> &launch_counter() {
 
 using namespace lora;
 
+// A wait that cannot end: the barrier expects one arrival that never comes
+// and no copy targets it.  The bounded wait gives up, the error bit is set.
+__global__ void selftest_wait_kernel(int32_t *counts) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (threadIdx.x == 0 && !mbar_wait(&bar, 0)) raise_deverr(counts, LORA_DEVERR_WAIT);
+}
+
 namespace {
 
 thread_local char g_err[512];
@@ -380,6 +392,16 @@ int32_t lora_abi_version(void) { return 100; }
 int64_t lora_launch_count(void) { return launch_counter().load(std::memory_order_relaxed); }
 
 int32_t lora_last_kernels(void) { return g_last_kernels; }
+
+lora_status_t lora_selftest_wait(int32_t *counts, void *stream) {
+    g_err[0] = 0;
+    g_last_kernels = 0;
+    if (!counts) return fail(LORA_ERR_INVALID, "counts is NULL");
+    selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(counts);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "self-test launch failed: %s", cudaGetErrorString(e));
+    return LORA_OK;
+}
 
 }  // extern "C"
 

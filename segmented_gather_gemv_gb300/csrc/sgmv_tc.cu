@@ -25,7 +25,10 @@
 //           = y_tile . I + H . B^T: the y stage times a 16 x 16 identity puts
 //           y into the fp32 accumulator exactly, then B stacks the adapters'
 //           rows of that n-tile;
-//   store   D2 rounded once to bf16 and written back as y.
+//   store   D2 rounded once to bf16 and written back as y.  An output that
+//           comes out non-finite (a non-finite y reaches its whole 16-column
+//           group through the identity: 0 * inf is NaN) is formed again as y
+//           + sum_j h_j B_j in fp32, so every element is y + delta exactly.
 // Ranks are masked exactly: A rows / B columns past an adapter's rank are
 // never read, H columns past it are zero, so padding never reaches y.
 //
@@ -385,6 +388,27 @@ __device__ __forceinline__ void tile_box_masks(const DeltaArgs &p, const TcMaps 
     mask8 = b & 0xFFFFu;
     mask32 = (b >> 16) & 0xFu;
     mask64 = (b >> 20) & 0x3u;
+}
+
+// y + delta in fp32 for element e of a stage chunk of tile row `row` (yword:
+// the chunk's 32-bit word holding it): delta = sum over the adapter's rank
+// columns j of H[row][k_lo + j]
+// (bf16, scaled) times B[a][col][j] (the rare path of outputs the identity
+// product made non-finite).
+__device__ __forceinline__ float exact_output(uint32_t yword, int e, const unsigned char *H, int row, int k_lo, int rk,
+                                              const SliceDesc &S, int a, int col) {
+    const float yv = __uint_as_float((e & 1) ? (yword & 0xFFFF0000u) : (yword << 16));
+    const __nv_bfloat16 *Bp = static_cast<const __nv_bfloat16 *>(S.B) + (int64_t)a * S.stride_adapter +
+                              (int64_t)col * S.stride_n;
+    float dsum = 0.f;
+#pragma unroll 1
+    for (int j = 0; j < rk; ++j) {
+        const int kc = k_lo + j;
+        const float hj =
+            __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(H + (kc >> 3) * kHChunk + row * 16 + (kc & 7) * 2));
+        dsum = fmaf(hj, __bfloat162float(Bp[j]), dsum);
+    }
+    return yv + dsum;
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -969,6 +993,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int st_off[kEpiChunks];
 #pragma unroll
             for (int q = 0; q < kEpiChunks; ++q) st_off[q] = schunk(xatom, row, kEpiChunks * chalf + q);
+            // this row's first H column and rank (for the rare exact path)
+            const int rinfo = k_lo | ((k_hi - k_lo) << 8), radapter = live ? sel(t.a, pq) : 0;
             for (int nti = 0; nti < n_nt; ++nti, ++job, ++ts) {
                 const int nt = nti + nt_rot < n_nt ? nti + nt_rot : nti + nt_rot - n_nt;
                 const int s = job % NS, sd = ts % kST;
@@ -994,14 +1020,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int q = 0; q < kEpiChunks; ++q) {
                     if (!live) break;
-                    uint32_t o[4];
+                    // Any output not finite?  (x * 0 is 0 for finite x and NaN
+                    // for an infinity or NaN; the sum of eight such products is
+                    // NaN exactly when one of the eight is.)
+                    float z = 0.f;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[q >> 1][(q & 1) * 8 + 2 * e]),
-                                                                        __uint_as_float(v[q >> 1][(q & 1) * 8 + 2 * e + 1]));
-                        o[e] = *reinterpret_cast<const uint32_t *>(&h2);
+                    for (int e = 0; e < 8; ++e) z = fmaf(__uint_as_float(v[q >> 1][(q & 1) * 8 + e]), 0.f, z);
+                    if (z == z) {
+                        uint32_t o[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[q >> 1][(q & 1) * 8 + 2 * e]),
+                                                                            __uint_as_float(v[q >> 1][(q & 1) * 8 + 2 * e + 1]));
+                            o[e] = *reinterpret_cast<const uint32_t *>(&h2);
+                        }
+                        *reinterpret_cast<uint4 *>(ys + st_off[q]) = make_uint4(o[0], o[1], o[2], o[3]);
+                    } else {
+                        // A y value that is not finite reaches every output of its
+                        // row's 16-column group through the identity product
+                        // (0 * inf is NaN).  This chunk's outputs are formed again,
+                        // y + delta in fp32 from the chunk's y (still in the
+                        // stage), the row's H and the adapter's B rows (see
+                        // exact_output): exact for every element.
+                        unsigned char *yc = ys + st_off[q];
+#pragma unroll 1
+                        for (int e = 0; e < 8; ++e) {
+                            const uint32_t w = reinterpret_cast<const uint32_t *>(yc)[e >> 1];
+                            const float out = exact_output(w, e, H, row, rinfo & 0xFF, rinfo >> 8, S, radapter,
+                                                           c0 + kEpiCols * chalf + 8 * q + e);
+                            *reinterpret_cast<__nv_bfloat16 *>(yc + 2 * e) = __float2bfloat16_rn(out);
+                        }
                     }
-                    *reinterpret_cast<uint4 *>(ys + st_off[q]) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
                 __syncwarp();
                 // store the warp's live rows: 8 row pieces of kEpiCols columns

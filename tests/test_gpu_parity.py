@@ -348,3 +348,45 @@ def test_large_batch_of_small_groups(B):
     c = batch.counts()
     assert c["tc_rows"] == 0 and c["num_small_segs"] > 500
     _assert_delta(w, y)
+
+
+# ----------------------------------------------------- non-finite base outputs
+
+NONFINITE_CASES = [
+    # (workload kwargs, path): every kernel of the path sees NaN and infinities in y
+    (dict(M=256, d_in=1024, d_outs=[768], n_pool=40, r_max=16), 0),          # small-batch kernel
+    (dict(M=1500, d_in=512, d_outs=[384], n_pool=60, r_max=16), 1),          # small-segment kernel
+    (dict(M=700, d_in=512, d_outs=[256, 128], n_pool=6, r_max=16, run_len=120), 2),  # tensor cores only
+    (dict(M=900, d_in=512, d_outs=[384], n_pool=30, r_max=32, run_len=40, ranks=[8, 16, 32],
+          per_adapter_scale=True), 0),                                        # both kernels
+]
+
+
+@pytest.mark.parametrize("ci", range(len(NONFINITE_CASES)))
+def test_nonfinite_y_stays_per_element(B, ci):
+    kw, path = NONFINITE_CASES[ci]
+    w = wl.random_batch(seed=700 + ci, dtype="bf16", **kw)
+    rng = np.random.default_rng(701 + ci)
+    act_rows = np.flatnonzero(active_rows(w))
+    y = w.y.copy()
+    # several non-finite values, some in the same row and 16-column group
+    for v in (np.nan, np.inf, -np.inf):
+        for _ in range(6):
+            i = int(rng.choice(act_rows))
+            c = int(rng.integers(0, y.shape[1]))
+            y[i, c] = v
+            y[i, c ^ 1] = v
+    w.y = y
+    got, batch = _run_delta(B, w, path=path)
+    ref = oracle_delta(w)
+    assert np.array_equal(np.isnan(got), np.isnan(ref)), "NaN positions differ"
+    assert np.array_equal(np.isposinf(got), np.isposinf(ref)), "+inf positions differ"
+    assert np.array_equal(np.isneginf(got), np.isneginf(ref)), "-inf positions differ"
+    act = active_rows(w)
+    fin = np.isfinite(ref) & np.isfinite(y) & act[:, None]
+    den = np.abs(ref[fin] - y.astype(np.float64)[fin]).max()
+    assert np.abs(got[fin] - ref[fin]).max() / den <= TOL["bf16"]
+    ok = ~act
+    assert np.array_equal(got[ok], y[ok].astype(np.float64), equal_nan=True), "inactive rows changed"
+    if path == 2 or ci == 3:
+        assert batch.counts()["tc_rows"] > 0
