@@ -68,6 +68,8 @@ WORKLOADS = {
 KERNEL_SOURCES = {
     "sgmv_small_kernel": ["segmented_gather_gemv_gb300/csrc/sgmv_small.cu",
                           "segmented_gather_gemv_gb300/csrc/common.cuh"],
+    "sgmv_stream_kernel": ["segmented_gather_gemv_gb300/csrc/sgmv_stream.cu",
+                           "segmented_gather_gemv_gb300/csrc/common.cuh"],
     "sgmv_cc_kernel": ["segmented_gather_gemv_gb300/csrc/sgmv_cc.cu",
                        "segmented_gather_gemv_gb300/csrc/common.cuh"],
     "sgmv_tc_kernel": ["segmented_gather_gemv_gb300/csrc/sgmv_tc.cu",

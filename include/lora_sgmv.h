@@ -87,10 +87,13 @@ typedef int lora_status_t;
 #define LORA_BF16 1
 
 /* Path selection for lora_delta / lora_shrink / lora_expand. */
-#define LORA_PATH_AUTO 0      /* groups with >= tc_min_rows rows use the tcgen05 kernel (bf16);
-                                 bf16 batches of at most 256 rows use the small-batch kernel */
-#define LORA_PATH_CUDA_CORE 1 /* every segment on the small-segment kernel: clusters of CTAs,
-                                 warp-level bf16 tensor-core tiles (fp32: CUDA-core FMAs) */
+#define LORA_PATH_AUTO 0      /* fused bf16: batches of at most 256 rows on the small-batch kernel,
+                                 of at most 4096 on the streaming kernel (see lora_delta); larger
+                                 batches: groups with >= tc_min_rows rows on the tcgen05 kernel,
+                                 the others on the small-segment kernel */
+#define LORA_PATH_CUDA_CORE 1 /* no tcgen05 kernel: the small-batch or streaming kernel where they
+                                 take the batch, else the small-segment kernel (clusters of CTAs,
+                                 warp-level bf16 tensor-core tiles; fp32: CUDA-core FMAs) */
 #define LORA_PATH_TENSOR 2    /* every segment on the tcgen05 kernel (bf16 only) */
 
 /* Largest supported sizes. */
@@ -311,15 +314,19 @@ lora_status_t lora_expand(const lora_batch_t *batch, int32_t dtype,
  * never written to global memory ("vLLM-Ascend LoRA" article, section 4.3).
  * Arguments as for lora_shrink and lora_expand.  Each y element is read,
  * y + delta is formed in fp32 and rounded to y's type once.
- * Small batches: a bf16 batch of at most 256 rows under LORA_PATH_AUTO (at
- * most 1024 rows under LORA_PATH_CUDA_CORE) with r_max <= 64 runs on one
- * kernel that groups the rows itself from the batch's ids (the same groups
- * as lora_prepare_batch), so that it does not wait for the batch metadata.
- * That kernel reads ids, the A and B pools, ranks and adapter_scale before
- * it waits for the kernels ahead of it in the stream (programmatic dependent
- * launch): they must be final before the kernel preceding this call starts
- * (adapter weights loaded earlier, ids from a copy or an earlier kernel).
- * x and y are read only after that wait.
+ * Batches of up to 4096 rows (bf16, LORA_PATH_AUTO or LORA_PATH_CUDA_CORE):
+ * a kernel that groups the rows itself from the batch's ids (the same groups
+ * as lora_prepare_batch) runs the whole batch, so that it does not wait for
+ * the batch metadata: up to 256 rows (a decode step) the single-pass
+ * small-batch kernel (r_max <= 64, d_in a multiple of 16 per cluster CTA),
+ * above that the streaming kernel (r_max 16, 32 or 64, d_in a multiple of
+ * 64 per cluster CTA, min(M, n_adapters) <= 2048), whose
+ * tiles stream through a ring of TMA copies.  A batch neither takes runs on
+ * the kernels of larger batches.  These kernels read ids, the A and B pools,
+ * ranks and adapter_scale before they wait for the kernels ahead of them in
+ * the stream (programmatic dependent launch): those must be final before the
+ * kernel preceding this call starts (adapter weights loaded earlier, ids from
+ * a copy or an earlier kernel).  x and y are read only after that wait.
  * Non-finite y: every path adds y per element, so a NaN or infinity in
  * y[i, n] gives a non-finite result there and nowhere else.
  */
@@ -348,6 +355,7 @@ int64_t lora_launch_count(void);
 #define LORA_KERNEL_SMALL 2     /* small-batch fused kernel: rows grouped on chip */
 #define LORA_KERNEL_CUDA_CORE 4 /* small-segment kernel (clusters, warp-level tiles) */
 #define LORA_KERNEL_TENSOR 8    /* tcgen05 kernel for long segments */
+#define LORA_KERNEL_STREAM 16   /* streaming fused kernel: rows grouped on chip, chunks through a TMA ring */
 
 /* The kernels the calling thread's last call of this library enqueued, as a
  * bit set of LORA_KERNEL_* (0 if it enqueued none; a diagnostic). */

@@ -39,9 +39,10 @@ MAX_SLICES = 4
 COUNT_NAMES = ("num_segs", "num_active", "num_invalid", "num_small_segs",
                "num_tc_segs", "tc_rows", "device_error", "num_groups")
 DEVERR_RANK, DEVERR_WAIT = 1, 2
-KERNEL_PREPARE, KERNEL_SMALL, KERNEL_CUDA_CORE, KERNEL_TENSOR = 1, 2, 4, 8
+KERNEL_PREPARE, KERNEL_SMALL, KERNEL_CUDA_CORE, KERNEL_TENSOR, KERNEL_STREAM = 1, 2, 4, 8, 16
 KERNEL_NAMES = {KERNEL_PREPARE: "prepare_kernel", KERNEL_SMALL: "sgmv_small_kernel",
-                KERNEL_CUDA_CORE: "sgmv_cc_kernel", KERNEL_TENSOR: "sgmv_tc_kernel"}
+                KERNEL_CUDA_CORE: "sgmv_cc_kernel", KERNEL_TENSOR: "sgmv_tc_kernel",
+                KERNEL_STREAM: "sgmv_stream_kernel"}
 
 _STATUS = {LORA_ERR_INVALID: "invalid argument", LORA_ERR_UNSUPPORTED: "unsupported",
            LORA_ERR_WORKSPACE: "workspace too small", LORA_ERR_CUDA: "CUDA error"}

@@ -123,9 +123,13 @@ constexpr int kDefaultTcMinRows = 64;
 // Batches of at most this many rows start the CUDA-core kernel before the
 // tensor-core kernel (see the dispatch in api.cu).
 constexpr int kCcFirstMaxRows = 256;
-// Batches of at most this many rows run whole on the small-batch kernel
-// under LORA_PATH_AUTO (see the dispatch in api.cu).
+// Batches of at most this many rows run whole on the single-pass small-batch
+// kernel under LORA_PATH_AUTO; larger ones that the streaming kernel takes
+// run on it (see the dispatch in api.cu).
 constexpr int kSmallAutoRows = 256;
+// Whether LORA_PATH_AUTO gives the long groups of a streaming-kernel batch to
+// the tensor-core kernel (false: the streaming kernel takes the whole batch).
+constexpr bool kStreamSplitTc = false;
 constexpr int kTcMaxRankCommon = 32;
 // Ranks the tensor-core kernel computes (exact 8-column masking, <= 32).
 __host__ __device__ __forceinline__ bool tc_rank_ok(int r) { return r > 0 && r <= kTcMaxRankCommon && (r & 7) == 0; }
@@ -376,6 +380,7 @@ struct DeltaArgs {
     int32_t split_tc;          // 1: segments >= max_len with a tensor-core rank go to the tensor-core kernel
     int32_t after_tc;          // 1: launched right after the tensor-core kernel, which waited on prepare
     int32_t after_cc;          // 1: tensor-core kernel launched right after the CUDA-core kernel, which waited on prepare
+    int32_t trigger_after_wait;  // small-batch kernel: trigger the next grid only after its own wait
     // CTA shares of the tensor-core row space computed by prepare for a grid
     // of tc_share_grid CTAs: boundary b = {first row of CTA b, its segment}
     const int2 *tc_share;

@@ -390,3 +390,31 @@ def test_nonfinite_y_stays_per_element(B, ci):
     assert np.array_equal(got[ok], y[ok].astype(np.float64), equal_nan=True), "inactive rows changed"
     if path == 2 or ci == 3:
         assert batch.counts()["tc_rows"] > 0
+
+
+# ------------------------------------------------ the streaming kernel
+
+# Shapes that stream several K and N chunks per tile and several tiles per
+# cluster through the streaming kernel: more rows than threads (2, 4 and 8
+# rows per thread), projections wider than one stage, per-slice B pools,
+# padded ranks, groups of hundreds of rows, and very small d.
+PIPE_CASES = [
+    dict(M=2048, d_in=4096, d_outs=[4096, 1024, 1024], n_pool=128, r_max=32, run_len=9),
+    dict(M=512, d_in=4096, d_outs=[14336], n_pool=100, r_max=64, ranks=[8, 16, 32, 64], skip_frac=0.25),
+    dict(M=512, d_in=14336, d_outs=[4096], n_pool=100, r_max=64, ranks=[8, 16, 32, 64], skip_frac=0.25,
+         per_adapter_scale=True),
+    dict(M=4096, d_in=1024, d_outs=[1024], n_pool=300, r_max=16, run_len=3),
+    dict(M=3000, d_in=2048, d_outs=[2048], n_pool=4, r_max=16, run_len=1000),
+    dict(M=1000, d_in=256, d_outs=[200], n_pool=50, r_max=16, ranks=[1, 3, 5, 8, 16], skip_frac=0.1),
+    dict(M=777, d_in=1536, d_outs=[520, 264], n_pool=20, r_max=32, ranks=[8, 16, 24, 32], run_len=30,
+         bad_frac=0.05),
+]
+
+
+@pytest.mark.parametrize("ci", range(len(PIPE_CASES)))
+def test_stream_kernel_pipeline(B, ci):
+    w = wl.random_batch(seed=800 + ci, dtype="bf16", **PIPE_CASES[ci])
+    y, batch = _run_delta(B, w, path=1, guard_cols=8)
+    assert B.lora_last_kernels() == B.KERNEL_STREAM
+    _assert_delta(w, y)
+    assert batch.counts()["device_error"] == 0
