@@ -88,7 +88,7 @@ typedef int lora_status_t;
 
 /* Path selection for lora_delta / lora_shrink / lora_expand. */
 #define LORA_PATH_AUTO 0      /* fused bf16: batches of at most 256 rows on the small-batch kernel,
-                                 of at most 4096 on the streaming kernel (see lora_delta); larger
+                                 of at most 2048 on the streaming kernel (see lora_delta); larger
                                  batches: groups with >= tc_min_rows rows on the tcgen05 kernel,
                                  the others on the small-segment kernel */
 #define LORA_PATH_CUDA_CORE 1 /* no tcgen05 kernel: the small-batch or streaming kernel where they
@@ -314,7 +314,7 @@ lora_status_t lora_expand(const lora_batch_t *batch, int32_t dtype,
  * never written to global memory ("vLLM-Ascend LoRA" article, section 4.3).
  * Arguments as for lora_shrink and lora_expand.  Each y element is read,
  * y + delta is formed in fp32 and rounded to y's type once.
- * Batches of up to 4096 rows (bf16, LORA_PATH_AUTO or LORA_PATH_CUDA_CORE):
+ * Batches of up to 2048 rows (bf16, LORA_PATH_AUTO or LORA_PATH_CUDA_CORE):
  * a kernel that groups the rows itself from the batch's ids (the same groups
  * as lora_prepare_batch) runs the whole batch, so that it does not wait for
  * the batch metadata: up to 256 rows (a decode step) the single-pass

@@ -35,20 +35,23 @@
 // of a padded pool moves its own rank's bytes (section 3.4 of the same
 // article: padding to the largest rank wastes traffic).
 //
-// Data movement.  Every load is a TMA copy, issued by one lane of each warp
-// and completing on the stage's mbarrier: the rank rows of A by a 3-D tensor
-// map in 64-column x 16-rank boxes (128-byte swizzle), the rank columns of
-// B by a 3-D tensor map in w-rank x 128-column boxes, w the adapter's rank
-// rounded up to 16, 32 or 64 (rows of 2w bytes, swizzled for w >= 32), and
-// the gathered x and y rows by one bulk copy each.  The copy engine's cost
-// grows with the number of rows a box has, not with their width: boxes are a
-// few KB with rows as wide as the adapter's rank allows.  The
+// Data movement.  Every load is a TMA copy, issued by a producer warp that
+// runs ahead of the sixteen consumer warps (a stage is refilled once all of
+// them have released it) and completing on the stage's mbarrier: the rank
+// rows of A by a 3-D tensor map in 64-column x 16-rank boxes (128-byte
+// swizzle), the rank columns of B by a 3-D tensor map in w-rank x 128-column
+// boxes, w the adapter's rank rounded up to 16, 32 or 64 (rows of 2w bytes,
+// swizzled for w >= 32), and the gathered x and y rows by one bulk copy
+// each.  The copy engine's cost grows with the number of rows a box has, not
+// with their width, so boxes are a few KB with rows as wide as the adapter's
+// rank allows; and the consumers never wait on a copy being issued.  The
 // load/store unit stays free for the shared-memory traffic of the compute
 // (16-byte cp.async copies in flight slow every shared-memory access behind
 // them).  The weights (A and B) depend only on the adapter, so those of the
-// first chunks are requested before the kernel waits on the previous grid in
-// the stream (programmatic dependent launch); x and y are requested after
-// that wait.  y + delta leaves by 16-byte stores.
+// first chunks are requested before the kernel waits on the previous grid
+// in the stream (programmatic dependent launch), and so are the rows of
+// every tile; x and y are requested after that wait.  y + delta leaves by
+// 16-byte stores.
 //
 // Compute.  Shrink: warp-level bf16 tensor-core tiles (16 x 8 x 16, fp32
 // accumulators in registers across the K chunks; operands by ldmatrix from
@@ -79,12 +82,12 @@
 namespace lora {
 namespace stream {
 
-constexpr int kSmThreads = 512;
+constexpr int kSmThreads = 512;                       // consumer threads (16 warps): grouping and compute
 constexpr int kSmWarps = kSmThreads / 32;
-constexpr int kSmMaxRPT = 8;                          // rows per thread at most
+constexpr int kStThreads = kSmThreads + 32;           // + one producer warp that issues every copy
+constexpr int kSmMaxRPT = 4;                          // rows per thread at most
 constexpr int kSmMaxRows = kSmThreads * kSmMaxRPT;    // rows a batch may have for this kernel
 constexpr int kSmRT = 16;                             // rows per tile: one 16-row MMA tile
-constexpr int kSmNtBatch = 4;                         // 8-column tiles a warp keeps in flight in the expand
 constexpr int kSmMaxCluster = 8;
 constexpr int kSmMaxHashBytes = 48 * 1024;            // hash table (key, first row, count) at most
 
@@ -222,6 +225,11 @@ __device__ __forceinline__ void tma_3d(uint32_t sdst, const CUtensorMap *map, in
         : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_cta() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+// Barrier of the consumer warps only (the producer warp runs its own loop).
+__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;\n" ::"n"(kSmThreads) : "memory"); }
+__device__ __forceinline__ void mbar_arrive1(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
 
 // The expand of the 8-column tiles nt0, nt0 + 16, ... (NB of them) of a
 // warp: B words and y words first, then the products, then y + delta in
@@ -266,7 +274,7 @@ __device__ __forceinline__ void expand_tiles(int nt0, int np, uint32_t sBa, cons
 }
 
 template <int R16>
-__global__ void __launch_bounds__(kSmThreads, 1)
+__global__ void __launch_bounds__(kStThreads, 1)
     sgmv_stream_kernel(const __grid_constant__ DeltaArgs p, const __grid_constant__ SmGeom g,
                       const __grid_constant__ SmMaps m) {
     constexpr int KS = R16 / 16;  // K steps of the expand (rank blocks of the shrink)
@@ -276,13 +284,14 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *recv_bar = reinterpret_cast<uint64_t *>(smem + g.off_bars);  // [2] partial h received
     uint64_t *full = recv_bar + 2;                                         // [D] stage landed
+    uint64_t *empty = full + 8;                                            // [D] stage released by the consumers
     int32_t *key = reinterpret_cast<int32_t *>(smem + g.off_key);
     int32_t *first = reinterpret_cast<int32_t *>(smem + g.off_first);
     int32_t *cnt = reinterpret_cast<int32_t *>(smem + g.off_cnt);
     int32_t *wsum = reinterpret_cast<int32_t *>(smem + g.off_scan);  // [kSmWarps]
     int32_t *wsum2 = wsum + 32;                                         // [kSmWarps]
     TileRec *tl = reinterpret_cast<TileRec *>(smem + g.off_tl);        // [tcap]
-    int32_t *rows2 = reinterpret_cast<int32_t *>(smem + g.off_rows);   // [2][kSmRT]: rows of tiles e (e & 1)
+    int32_t *rows_all = reinterpret_cast<int32_t *>(smem + g.off_rows);  // [tcap][kSmRT]: rows of tile e
     int32_t *ids_s = reinterpret_cast<int32_t *>(smem + g.off_ids);    // [512 RPT]: valid id or -1 per row
     float *recv = reinterpret_cast<float *>(smem + g.off_recv);        // [2][CL][16][R16]
     unsigned char *hbf = smem + g.off_hbf;                              // [16][R16 + 8] bf16
@@ -317,10 +326,13 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     if (tid == 0) {
         mbar_init(&recv_bar[0], 1);
         mbar_init(&recv_bar[1], 1);
-        for (int s2 = 0; s2 < g.D; ++s2) mbar_init(&full[s2], 1);
+        for (int s2 = 0; s2 < g.D; ++s2) {
+            mbar_init(&full[s2], 1);
+            mbar_init(&empty[s2], kSmWarps);
+        }
         fence_mbar_init();
     }
-    for (int s = tid; s < HS; s += kSmThreads) {
+    for (int s = tid; s < HS && tid < kSmThreads; s += kSmThreads) {
         key[s] = -1;
         first[s] = INT_MAX;
         cnt[s] = 0;
@@ -331,7 +343,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         if (!v) idr[k] = -1;
         rkr[k] = v && p.ranks ? __ldcg(p.ranks + idr[k]) : p.r_max;
         scr[k] = v && p.adapter_scale ? __ldcg(p.adapter_scale + idr[k]) : p.scale;
-        if (k < RPT) ids_s[tid * RPT + k] = idr[k];
+        if (k < RPT && tid < kSmThreads) ids_s[tid * RPT + k] = idr[k];
     }
     __syncthreads();
     cluster_arrive_relaxed();  // the barriers exist before any peer pushes into them
@@ -432,16 +444,12 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     const int nch = g.nK + g.nN[q];  // chunks per tile (>= D - 1)
     const int J = my_tiles * nch;
 
-    // Rows [lo, hi) of adapter a's group, in ascending row order, into dst.
+    // Rows [lo, hi) of adapter a's group, in ascending row order, into dst
+    // (consumer warps only).
     auto find_rows = [&](int a, int lo, int hi, int32_t *dst) {
         int idv[kSmMaxRPT];
         const int rb = tid * RPT;
-        if (RPT == 8) {
-            const int4 u0 = *reinterpret_cast<const int4 *>(ids_s + rb);
-            const int4 u1 = *reinterpret_cast<const int4 *>(ids_s + rb + 4);
-            idv[0] = u0.x; idv[1] = u0.y; idv[2] = u0.z; idv[3] = u0.w;
-            idv[4] = u1.x; idv[5] = u1.y; idv[6] = u1.z; idv[7] = u1.w;
-        } else if (RPT == 4) {
+        if (RPT == 4) {
             const int4 u0 = *reinterpret_cast<const int4 *>(ids_s + rb);
             idv[0] = u0.x; idv[1] = u0.y; idv[2] = u0.z; idv[3] = u0.w;
         } else if (RPT == 2) {
@@ -461,7 +469,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
             if (lane >= o) inc += t;
         }
         if (lane == 31) wsum2[warp] = inc;
-        __syncthreads();
+        consumers_sync();
         int b;
         {
             const int wv = lane < kSmWarps ? wsum2[lane] : 0;
@@ -483,36 +491,35 @@ __global__ void __launch_bounds__(kSmThreads, 1)
                 }
             }
         }
-        __syncthreads();
+        consumers_sync();
     };
 
     // The copies of chunk (e, c) into stage st: the weights (A or B boxes)
-    // and / or the activations (x or y rows), by lane 0 of every warp, all
-    // completing on full[st].  The call with the weights sets the stage's
-    // expected bytes (weights and activations).  Tile e's rows are in
-    // rows2[e & 1].
+    // and / or the activations (x or y rows), spread over the lanes of the
+    // producer warp, all completing on full[st].  The call with the weights
+    // sets the stage's expected bytes (weights and activations).
     auto issue = [&](int e, int c, int st, bool w, bool act) {
-        if (e >= my_tiles || lane != 0) return;
+        if (e >= my_tiles) return;
         const TileRec ti = tl[e];
         const uint32_t sb = smem_u32(stages) + (uint32_t)(st * g.SB);
         uint64_t *fb = &full[st];
         const int R = ti.hi - ti.lo;
-        const int32_t *rws = rows2 + (e & 1) * kSmRT;
+        const int32_t *rws = rows_all + e * kSmRT;
         const int wi = ti.r <= 16 ? 0 : (ti.r <= 32 ? 1 : 2);  // B box of 16 << wi ranks
         if (c < g.nK) {
             const int kb = k0 + c * g.kc;
             const int nA = ((ti.r + 15) >> 4) * g.natoms;  // 16-rank blocks x atoms
-            if (w && tid == 0) mbar_arrive_expect_tx(fb, (uint32_t)(nA * 2048 + R * g.kc * 2));
+            if (w && lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)(nA * 2048 + R * g.kc * 2));
             {
                 // A: box (columns 64 at .., ranks 16 pb ..) -> atom pb * natoms + at
                 if (w)
-                    for (int i = warp; i < nA; i += kSmWarps) {
+                    for (int i = lane; i < nA; i += 32) {
                         const int pb = i / g.natoms, at = i - pb * g.natoms;
                         tma_3d(sb + g.offA + (uint32_t)i * 2048u, &m.a, kb + at * 64, pb * 16, ti.a, fb);
                     }
                 // x rows
                 if (act)
-                    for (int i = warp; i < R; i += kSmWarps)
+                    for (int i = lane; i < R; i += 32)
                         bulk_g2s(stages + st * g.SB + i * g.xpitch,
                                  static_cast<const __nv_bfloat16 *>(p.x) + (int64_t)rws[i] * p.ldx + kb,
                                  (uint32_t)(g.kc * 2), fb);
@@ -522,16 +529,16 @@ __global__ void __launch_bounds__(kSmThreads, 1)
             const SliceDesc &sl = p.slices[ck.t];
             const int ncols = ck.ce - ck.cb;
             const int nbx = (ncols + 127) >> 7;
-            if (w && tid == 0) mbar_arrive_expect_tx(fb, (uint32_t)(nbx * (4096 << wi) + R * ncols * 2));
+            if (w && lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)(nbx * (4096 << wi) + R * ncols * 2));
             {
                 // B: box (ranks 0 .. 16 << wi, columns 128 bx ..) -> rows 128 bx ..
                 if (w)
-                    for (int bx = warp; bx < nbx; bx += kSmWarps)
+                    for (int bx = lane; bx < nbx; bx += 32)
                         tma_3d(sb + g.offB + (uint32_t)(bx * (4096 << wi)), &m.b[ck.t][wi], 0,
                                ck.cb - sl.col_begin + bx * 128, ti.a, fb);
                 // y rows
                 if (act)
-                    for (int i = warp; i < R; i += kSmWarps)
+                    for (int i = lane; i < R; i += 32)
                         bulk_g2s(stages + st * g.SB + i * g.ypitch,
                                  static_cast<const __nv_bfloat16 *>(p.y) + (int64_t)rws[i] * p.ldy + sl.y_col +
                                      (ck.cb - sl.col_begin),
@@ -540,20 +547,60 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         }
     };
 
-    // ---- prologue: tile 0's rows, the weights of the first D - 1 chunks
-    // (one group, before the wait), then their activations (one group each).
-    if (my_tiles > 0) {
-        const TileRec t0 = tl[0];
-        find_rows(t0.a, t0.lo, t0.hi, rows2);
-    }
-    for (int j = 0; j < D - 1; ++j) issue(j / nch, j % nch, j, true, false);
+    // ---- every tile's rows, found before the wait on the previous grid (the
+    // ids are fixed before it started); then the producer warp streams the
+    // chunks and the consumer warps compute them.
+    if (warp < kSmWarps)
+        for (int e = 0; e < my_tiles; ++e) {
+            const TileRec t0 = tl[e];
+            find_rows(t0.a, t0.lo, t0.hi, rows_all + e * kSmRT);
+        }
+    __syncthreads();
+    bool ok = true;
+    if (warp == kSmWarps) {
+        // ---- producer: the weights of the first D chunks (every stage is
+        // free) before the wait, then their activations, then each further
+        // chunk once the consumers have released its stage
+        const int npre = min(D, J);
+        int pe = 0, pc = 0;
+        for (int j = 0; j < npre; ++j) {
+            issue(pe, pc, j, true, false);
+            if (++pc == nch) {
+                pc = 0;
+                ++pe;
+            }
+        }
+        griddep_wait();
+        pe = 0;
+        pc = 0;
+        for (int j = 0; j < npre; ++j) {
+            issue(pe, pc, j, false, true);
+            if (++pc == nch) {
+                pc = 0;
+                ++pe;
+            }
+        }
+        int pst = npre % D, pu = npre / D;  // stage of chunk j and its use
+        for (int j = npre; j < J; ++j) {
+            if (lane == 0 && !mbar_wait(&empty[pst], (uint32_t)(pu - 1) & 1u)) ok = false;
+            __syncwarp();
+            issue(pe, pc, pst, true, true);
+            if (++pc == nch) {
+                pc = 0;
+                ++pe;
+            }
+            if (++pst == D) {
+                pst = 0;
+                ++pu;
+            }
+        }
+        cluster_wait_acquire();
+    } else {
     griddep_wait();
     if (p.trigger_after_wait) griddep_launch_dependents();
     if (bad_rank && blockIdx.x == 0 && tid == 0) raise_deverr(p.counts, LORA_DEVERR_RANK);
-    for (int j = 0; j < D - 1; ++j) issue(j / nch, j % nch, j, false, true);
     cluster_wait_acquire();
 
-    bool ok = true;
     const int g_ = lane >> 2, t4 = lane & 3;
     // tile state
     TileRec ti{};
@@ -562,26 +609,18 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     uint32_t hf[KS][4], bm0[KS], bm1[KS];
     int st = 0;                        // stage of chunk j
     uint32_t ph = 0;                   // phase parity of its barrier
-    int ie = (D - 1) / nch, ic = (D - 1) % nch, ist = D - 1;  // chunk j + D - 1 and its stage
-    if (ist == D) ist = 0;
     int e = 0, c = 0;                  // chunk j = (e, c)
     for (int j = 0; j < J; ++j) {
-        // chunk j has landed (one thread waits; the block barrier passes its
-        // view of the copies on), and every thread is done with chunk j - 1,
-        // whose stage the copies of chunk j + D - 1 now refill
+        // chunk j has landed (one thread waits; the consumer barrier passes
+        // its view of the copies on)
         if (tid == 0 && !mbar_wait(&full[st], ph)) ok = false;
-        fence_proxy_async_cta();  // this thread's accesses to the stages come before the copies issued next
-        __syncthreads();
+        consumers_sync();
         if (c == 0) {
             ti = tl[e];
             r = ti.r;
             R = ti.hi - ti.lo;
             r16a = (r + 15) & ~15;
             np = r16a / 16;
-            if (e + 1 < my_tiles) {
-                const TileRec tn = tl[e + 1];
-                find_rows(tn.a, tn.lo, tn.hi, rows2 + ((e + 1) & 1) * kSmRT);
-            }
             if (tid == 0) mbar_arrive_expect_tx(&recv_bar[e & 1], (uint32_t)(CL * 16 * r16a * 4));
 #pragma unroll
             for (int u = 0; u < 2; ++u)
@@ -590,13 +629,6 @@ __global__ void __launch_bounds__(kSmThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) acc[u][t][i] = 0.f;
         }
-        issue(ie, ic, ist, true, true);
-        if (++ic == nch) {
-            ic = 0;
-            ++ie;
-        }
-        if (++ist == D) ist = 0;
-
         unsigned char *sb = stages + st * g.SB;
         const int buf = e & 1;
         if (c < g.nK) {
@@ -639,7 +671,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
                 // floats: the fragment's rows 2t and 2t+1 fall in distinct
                 // banks), in this K stage, whose x and A every warp has read
                 float *red = reinterpret_cast<float *>(sb);
-                __syncthreads();
+                consumers_sync();
                 if (my_kq < kw) {
                     const uint32_t rw = smem_u32(red) + (uint32_t)warp * (16 * 20 * 4);
 #pragma unroll
@@ -653,7 +685,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
                         }
                     }
                 }
-                __syncthreads();
+                consumers_sync();
                 // CTA partial: the kw partials of each rank block summed in
                 // two levels (pairs kq, kq + 8 by all threads in place, then
                 // the eight sums in order), pushed to every CTA of the
@@ -674,7 +706,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
                                  "f"(__uint_as_float(x4.z) + __uint_as_float(y4.z)),
                                  "f"(__uint_as_float(x4.w) + __uint_as_float(y4.w))
                                  : "memory");
-                    __syncthreads();
+                    consumers_sync();
                 }
                 if (tid < nel4) {
                     const int row = tid / rq, col = (tid - row * rq) * 4;
@@ -699,7 +731,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
                 // bf16 (one thread waits for the partials; the next chunk's
                 // block barrier publishes h)
                 if (tid == 0 && !mbar_wait_cl(&recv_bar[buf], (uint32_t)(e >> 1) & 1u)) ok = false;
-                __syncthreads();
+                consumers_sync();
                 if (tid < nel4) {
                     const int row = tid / rq, col = (tid - row * rq) * 4;
                     float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -757,14 +789,14 @@ __global__ void __launch_bounds__(kSmThreads, 1)
             const uint32_t yr0 = smem_u32(sb) + g_ * g.ypitch + 4 * t4;  // row g_, column 2 t4
             const uint32_t yr1 = yr0 + 8 * g.ypitch;                     // row g_ + 8
             const bool row0 = g_ < R, row1 = g_ + 8 < R;
-            // warp w takes the 8-column tiles w, w + 16, ...: four at a time
-            // (in flight together) while four remain, then one at a time
+            // warp w takes the 8-column tiles w, w + 16, ...: two at a time
+            // (in flight together) while two remain, then one
             int nt = warp;
-            for (; nt + 3 * kSmWarps < nnt; nt += 4 * kSmWarps)
-                expand_tiles<KS, 4>(nt, np, sBa, boff, rsh, yr0, yr1, row0, row1, hf, bm0, bm1);
+            for (; nt + kSmWarps < nnt; nt += 2 * kSmWarps)
+                expand_tiles<KS, 2>(nt, np, sBa, boff, rsh, yr0, yr1, row0, row1, hf, bm0, bm1);
             for (; nt < nnt; nt += kSmWarps)
                 expand_tiles<KS, 1>(nt, np, sBa, boff, rsh, yr0, yr1, row0, row1, hf, bm0, bm1);
-            __syncthreads();
+            consumers_sync();
             // the rows leave by 16-byte stores: warp w takes row w / hv and
             // the 8-column pieces w % hv, w % hv + hv, ... (hv = 2 when R <= 8)
             {
@@ -772,7 +804,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
                 const int row = warp / hv, part = warp - row * hv;
                 if (row < R) {
                     __nv_bfloat16 *yrow =
-                        static_cast<__nv_bfloat16 *>(p.y) + (int64_t)rows2[buf * kSmRT + row] * p.ldy;
+                        static_cast<__nv_bfloat16 *>(p.y) + (int64_t)rows_all[e * kSmRT + row] * p.ldy;
                     const uint32_t src = smem_u32(sb) + row * g.ypitch;
                     const SliceDesc &sl = p.slices[ck.t];
                     const int go = sl.y_col - sl.col_begin;
@@ -781,6 +813,11 @@ __global__ void __launch_bounds__(kSmThreads, 1)
                 }
             }
         }
+        // release the stage: this thread's accesses to it come before the
+        // producer's next copies into it
+        fence_proxy_async_cta();
+        __syncwarp();
+        if (lane == 0) mbar_arrive1(&empty[st]);
         if (++st == D) {
             st = 0;
             ph ^= 1u;
@@ -790,12 +827,15 @@ __global__ void __launch_bounds__(kSmThreads, 1)
             ++e;
         }
     }
+    }
     // A wait that gave up may leave copies in flight: wait once more
     // (bounded) for the last use of every stage before the shared memory
     // goes away.
     if (__syncthreads_or(!ok)) {
-        if (tid == 0) raise_deverr(p.counts, LORA_DEVERR_WAIT);
-        for (int s2 = 0; s2 < D && s2 < J; ++s2) mbar_wait(&full[s2], (uint32_t)((J - 1 - s2) / D) & 1u);
+        if (tid == 0) {
+            raise_deverr(p.counts, LORA_DEVERR_WAIT);
+            for (int s2 = 0; s2 < D && s2 < J; ++s2) mbar_wait(&full[s2], (uint32_t)((J - 1 - s2) / D) & 1u);
+        }
     }
 }
 
@@ -817,7 +857,7 @@ static bool small_geometry(const DeltaArgs &p, int R16, int cl, int ncl, SmGeom 
     g = SmGeom{};
     g.CL = cl;
     g.KC = p.d_in / cl;
-    g.RPT = M <= kSmThreads ? 1 : (M <= 2 * kSmThreads ? 2 : (M <= 4 * kSmThreads ? 4 : 8));
+    g.RPT = M <= kSmThreads ? 1 : (M <= 2 * kSmThreads ? 2 : 4);
     const int nv = p.d_out_total / 8;
     int ncol0[kSmMaxCluster + 1];
     for (int qq = 0; qq <= cl; ++qq) ncol0[qq] = (int)((int64_t)nv * qq / cl) * 8;
@@ -835,13 +875,13 @@ static bool small_geometry(const DeltaArgs &p, int R16, int cl, int ncl, SmGeom 
         o = (o + bytes + 127) & ~size_t(127);
         return (int)at;
     };
-    g.off_bars = take(8 * (2 + 8));
+    g.off_bars = take(8 * (2 + 8 + 8));
     g.off_key = take((size_t)g.HS * 4);
     g.off_first = take((size_t)g.HS * 4);
     g.off_cnt = take((size_t)g.HS * 4);
     g.off_scan = take(64 * 4);
     g.off_tl = take((size_t)g.tcap * sizeof(TileRec));
-    g.off_rows = take(2 * kSmRT * 4);
+    g.off_rows = take((size_t)g.tcap * kSmRT * 4);
     g.off_ids = take((size_t)kSmThreads * g.RPT * 4);
     g.off_recv = take((size_t)2 * cl * 16 * R16 * 4);
     g.off_hbf = take((size_t)16 * (R16 + 8) * 2);
@@ -1053,7 +1093,7 @@ static cudaError_t launch_small_t(const DeltaArgs &p, const SmMaps &maps, int cl
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kSmThreads);
+    cfg.blockDim = dim3(kStThreads);
     cfg.dynamicSmemBytes = g.total;
     cfg.stream = stream;
     cfg.attrs = attr;

@@ -403,8 +403,8 @@ PIPE_CASES = [
     dict(M=512, d_in=4096, d_outs=[14336], n_pool=100, r_max=64, ranks=[8, 16, 32, 64], skip_frac=0.25),
     dict(M=512, d_in=14336, d_outs=[4096], n_pool=100, r_max=64, ranks=[8, 16, 32, 64], skip_frac=0.25,
          per_adapter_scale=True),
-    dict(M=4096, d_in=1024, d_outs=[1024], n_pool=300, r_max=16, run_len=3),
-    dict(M=3000, d_in=2048, d_outs=[2048], n_pool=4, r_max=16, run_len=1000),
+    dict(M=2048, d_in=1024, d_outs=[1024], n_pool=300, r_max=16, run_len=3),
+    dict(M=2000, d_in=2048, d_outs=[2048], n_pool=4, r_max=16, run_len=700),
     dict(M=1000, d_in=256, d_outs=[200], n_pool=50, r_max=16, ranks=[1, 3, 5, 8, 16], skip_frac=0.1),
     dict(M=777, d_in=1536, d_outs=[520, 264], n_pool=20, r_max=32, ranks=[8, 16, 24, 32], run_len=30,
          bad_frac=0.05),
