@@ -199,7 +199,11 @@ size_t lora_workspace_size(int32_t M, int32_t n_adapters, int32_t chunk_size);
  *              ("vLLM-Ascend LoRA" article, section 4.1: blocks below a row
  *              threshold use vector dot products; with chunking, every chunk
  *              of a long group counts as part of its group); <= 0 selects
- *              the library default.
+ *              the library default, 32 rows (on GB300, for batches of 8192
+ *              rows with every group of L rows, the CUDA-core kernel is ahead
+ *              for L <= 24, the tensor-core kernel for L = 32, 64, 128 and
+ *              256, the two even at 48).  Batches of at most 2048 rows do not
+ *              use the split: the streaming kernel takes them whole.
  * workspace    device buffer of >= lora_workspace_size(M, n_adapters,
  *              chunk_size) bytes, 256-byte aligned; owned by the caller and
  *              referenced by *batch until the batch is no longer used.

@@ -119,7 +119,10 @@ struct DeviceOnce {
 std::atomic<int64_t> &launch_counter();
 
 constexpr uint32_t kBatchMagic = 0x4C6F5241u;  // "LoRA"
-constexpr int kDefaultTcMinRows = 64;
+// Adapter groups of at least this many rows go to the tensor-core kernel
+// (measured crossover on GB300: the CUDA-core kernel is ahead for groups of
+// up to 24 rows, the tensor-core kernel from 32).
+constexpr int kDefaultTcMinRows = 32;
 // Batches of at most this many rows start the CUDA-core kernel before the
 // tensor-core kernel (see the dispatch in api.cu).
 constexpr int kCcFirstMaxRows = 256;

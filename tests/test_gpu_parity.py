@@ -418,3 +418,38 @@ def test_stream_kernel_pipeline(B, ci):
     assert B.lora_last_kernels() == B.KERNEL_STREAM
     _assert_delta(w, y)
     assert batch.counts()["device_error"] == 0
+
+
+# ------------------------------------------- split calls at full size
+
+@pytest.mark.parametrize("name", ["decode", "prefill", "prefill_chunk64", "mixed_serving"])
+def test_split_calls_full_size(B, name):
+    """lora_shrink then lora_expand on the full-size serving configurations:
+    h against the oracle's shrink, and the expand (fed the oracle's h, not the
+    GPU's) against the oracle's expand; rows outside every segment untouched."""
+    w = wl.serving_workloads()[name]()
+    d = to_dev(w)
+    batch = B.lora_prepare_batch(d["ids"], w.n_adapters, w.chunk_size)
+    act = active_rows(w)
+    guard = torch.full((w.M, w.r_max + 4), -777.0, device="cuda")
+    h = guard[:, :w.r_max]
+    B.lora_shrink(batch, d["x"], d["A"], h=h, ranks=d["ranks"])
+    torch.cuda.synchronize()
+    assert torch.all(guard[:, w.r_max:] == -777.0)
+    h_ref = oracle.shrink(w.x, w.ids, w.A, ranks=w.ranks)
+    hg = h.cpu().numpy().astype(np.float64)
+    err = np.abs(hg[act] - h_ref[act]).max() / np.abs(h_ref[act]).max()
+    assert err <= TOL[w.dtype], "shrink rel err %.3e" % err
+    assert np.all(hg[~act] == -777.0), "h rows outside segments written"
+    # the expand from the oracle's h (rounded to fp32), inactive rows zero
+    h_in = np.where(act[:, None], h_ref, 0.0).astype(np.float32)
+    y = d["y"].clone()
+    B.lora_expand(batch, torch.from_numpy(h_in).cuda(), d["B"], y, scale=w.scale,
+                  adapter_scale=d["adapter_scale"], ranks=d["ranks"])
+    y_ref = oracle.expand(h_in, w.ids, w.B, w.y, scale=w.scale, adapter_scale=w.adapter_scale,
+                          ranks=w.ranks)
+    yg = y.float().cpu().numpy().astype(np.float64)
+    e2 = rel_err(yg, y_ref, w.y.astype(np.float64), act)
+    assert e2 <= TOL[w.dtype], "expand rel err %.3e" % e2
+    assert np.array_equal(yg[~act], w.y[~act].astype(np.float64))
+    assert batch.counts()["device_error"] == 0
