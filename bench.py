@@ -419,6 +419,41 @@ class Bench:
             dist.barrier()
         return max_over_ranks(t0.elapsed_time(t1), world, dev)
 
+    def incremental_us(self, G, k_rows):
+        """Device time (us per step) of G steps that patch k_rows rows of a
+        kept batch (lora_batch_update) and then run the delta, against G steps
+        that rebuild the batch (lora_prepare_batch) and run the delta, and G
+        steps that run the delta on a kept batch whose ids did not change."""
+        torch, B, w = self.torch, self.B, self.w
+        gen = torch.Generator(device="cpu").manual_seed(5)
+        rows = [torch.randperm(w.M, generator=gen)[:k_rows].to(torch.int32).to(self.dev) for _ in range(G)]
+        new = [torch.randint(-1, w.n_adapters, (k_rows,), generator=gen).to(torch.int32).to(self.dev)
+               for _ in range(G)]
+        batches = [self.prepare(s) for s in self.sets]
+        with torch.cuda.stream(self.stream):
+            for i, b in enumerate(batches):  # the first update copies the ids into the batch
+                B.lora_batch_update(b, rows[0], new[0], stream=self.stream)
+                self.delta(b, self.sets[i])
+        self.stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream, capture_error_mode="thread_local"):
+            for i in range(G):
+                j = i % self.n_sets
+                B.lora_batch_update(batches[j], rows[i], new[i], stream=self.stream)
+                self.delta(batches[j], self.sets[j])
+        g_full, _ = self.graph(G)
+        out = {}
+        for name, gr in (("update_step_us", g), ("prepare_step_us", g_full)):
+            with torch.cuda.stream(self.stream):
+                gr.replay()
+            self.stream.synchronize()
+            out[name] = 1e3 * self.timed([gr], 1, self.dev) / G
+        out["rows_changed_per_step"] = k_rows
+        out["update_launches_per_step"] = 2
+        # ids unchanged: the kept batch needs neither update nor rebuild
+        out["kept_batch_step_us"] = self.delta_chain_us(G, self.path)
+        return out
+
     def delta_chain_us(self, G, path):
         """Average launch time (us) of lora_delta in a chain of G back-to-back
         calls on prepared batches of the rotating sets."""
@@ -598,6 +633,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     clocks = ClockSampler(vis.split(",")[local_rank].strip() if vis else str(local_rank))
     m = measure(b, args.workload, K, W, world, dev, args.graph_steps, clocks=clocks)
     e2e = e2e_measure(b, args.e2e_steps)
+    incremental = None
+    if args.path == 0 and w.M <= 2048 and world == 1:
+        # a decode step that keeps its grouping and patches the rows that
+        # changed (a few sequences join or leave), against the full rebuild
+        incremental = b.incremental_us(min(256, max(8, K)), max(1, w.M // 32))
     del b
     torch.cuda.empty_cache()
 
@@ -645,6 +685,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "clocks": m["clocks"],
         "wall_s_timed": m["wall_s_timed"],
     }
+    if incremental is not None:
+        line["incremental_grouping"] = incremental
     if others:
         line["other_workloads"] = others
     if world == 1 and not args.no_cpu_baseline:

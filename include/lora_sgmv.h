@@ -118,6 +118,7 @@ typedef int lora_status_t;
 
 #define LORA_DEVERR_RANK 1 /* an adapter's rank was outside [0, r_max] */
 #define LORA_DEVERR_WAIT 2 /* a bounded device wait gave up (result incomplete) */
+#define LORA_DEVERR_ROW 4  /* lora_batch_update named a row outside [0, M) (skipped) */
 
 /*
  * Segment metadata of one batch, built on the device by lora_prepare_batch
@@ -162,8 +163,14 @@ typedef struct lora_batch {
     int32_t max_segs;    /* capacity of the segment arrays */
     int32_t tc_min_rows; /* tensor-core row threshold used for the split */
     uint32_t magic;      /* set by lora_prepare_batch */
-    const int32_t *ids;  /* the ids the batch was built from (device, not owned;
-                            read again by the small-batch delta kernel) */
+    const int32_t *ids;  /* the ids the batch stands for (device; the caller's
+                            array until lora_batch_update, then ids_store);
+                            read again by the small-batch and streaming kernels */
+    int32_t *ids_store;  /* the batch's own copy of the ids (in the workspace),
+                            written by lora_batch_update */
+    int32_t order;       /* LORA_ORDER_* the batch was built with */
+    int32_t stale;       /* 1: ids changed since the segment metadata was built
+                            (lora_batch_update); lora_batch_refresh rebuilds it */
 } lora_batch_t;
 
 /* One output slice of the expand step: B pool and the y columns it writes
@@ -285,6 +292,37 @@ lora_status_t lora_prepare_batch_ordered(const int32_t *ids, int32_t M, int32_t 
 lora_status_t lora_prepare_batch_static(const int32_t *ids, int32_t M, int32_t n_adapters,
                                         int32_t chunk_size, int32_t tc_min_rows, lora_batch_t *batch,
                                         void *stream);
+
+/*
+ * Incremental update of a prepared batch: the grouping is kept across decode
+ * steps and patched when sequences join or leave ("vLLM-Ascend LoRA"
+ * article, sections 4.2 and 5.3: the index preparation is cached rather
+ * than rebuilt every step).
+ *
+ * lora_batch_update sets, for k < n, the adapter of row rows[k] to
+ * new_ids[k] (-1: the row leaves; an id: the row joins or switches), in the
+ * batch's own copy of the ids (ids_store, in the workspace; the first update
+ * copies the batch's ids there).  rows and new_ids are device int32[n];
+ * rows must lie in [0, M) (others are skipped and raise LORA_DEVERR_ROW in
+ * the counters, which report it until the metadata is rebuilt);
+ * when a row appears twice, the later entry wins.  No host
+ * synchronisation.  The segment metadata (sorted_token_ids, seg_indptr, ...)
+ * and the counters then describe the old ids (batch->stale = 1): the
+ * small-batch and streaming kernels, which group the rows themselves, use
+ * the patched ids directly, so a decode step needs no rebuild; every other
+ * path rebuilds the metadata into the workspace before it runs (each call,
+ * while the batch is stale), and lora_batch_refresh rebuilds it once and
+ * clears stale.  After lora_batch_refresh the batch equals the one
+ * lora_prepare_batch_ordered builds from the patched ids.  The update
+ * enqueues one kernel, which waits for the kernels ahead of it before it
+ * writes; the kernels of later calls on an updated batch read its ids only
+ * after their own wait on the kernels ahead (the ordering contract of
+ * lora_delta does not apply to them).
+ * Not in the pages' interface: an addition for serving loops.
+ */
+lora_status_t lora_batch_update(lora_batch_t *batch, const int32_t *rows, const int32_t *new_ids, int32_t n,
+                                void *stream);
+lora_status_t lora_batch_refresh(lora_batch_t *batch, void *stream);
 
 /*
  * Shrink: h[i, j] = sum_k x[i, k] * A[a, j, k] for j < r_a, and 0 for

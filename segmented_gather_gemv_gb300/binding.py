@@ -15,6 +15,8 @@ Calls (same names as the C ABI):
               ranks=None, y_cols=None, path=PATH_AUTO) -> y
   lora_delta(batch, x, A_pool, B_pools, y, scale=1.0, adapter_scale=None,
              ranks=None, y_cols=None, path=PATH_AUTO) -> y
+  lora_batch_update(batch, rows, new_ids) -> batch
+  lora_batch_refresh(batch) -> batch
 """
 from __future__ import annotations
 
@@ -38,7 +40,7 @@ LORA_ORDER_FIRST_APPEARANCE, LORA_ORDER_ASCENDING = 0, 1
 MAX_SLICES = 4
 COUNT_NAMES = ("num_segs", "num_active", "num_invalid", "num_small_segs",
                "num_tc_segs", "tc_rows", "device_error", "num_groups")
-DEVERR_RANK, DEVERR_WAIT = 1, 2
+DEVERR_RANK, DEVERR_WAIT, DEVERR_ROW = 1, 2, 4
 KERNEL_PREPARE, KERNEL_SMALL, KERNEL_CUDA_CORE, KERNEL_TENSOR, KERNEL_STREAM = 1, 2, 4, 8, 16
 KERNEL_NAMES = {KERNEL_PREPARE: "prepare_kernel", KERNEL_SMALL: "sgmv_small_kernel",
                 KERNEL_CUDA_CORE: "sgmv_cc_kernel", KERNEL_TENSOR: "sgmv_tc_kernel",
@@ -62,7 +64,8 @@ class _Batch(ctypes.Structure):
                 ("M", ctypes.c_int32), ("n_adapters", ctypes.c_int32),
                 ("chunk_size", ctypes.c_int32), ("max_segs", ctypes.c_int32),
                 ("tc_min_rows", ctypes.c_int32), ("magic", ctypes.c_uint32),
-                ("ids", ctypes.c_void_p)]
+                ("ids", ctypes.c_void_p), ("ids_store", ctypes.c_void_p),
+                ("order", ctypes.c_int32), ("stale", ctypes.c_int32)]
 
 
 class _BSlice(ctypes.Structure):
@@ -118,6 +121,10 @@ def lib() -> ctypes.CDLL:
             L.lora_launch_count.restype = ctypes.c_int64
             L.lora_last_kernels.restype = ctypes.c_int32
             L.lora_last_kernels.argtypes = []
+            L.lora_batch_update.restype = ctypes.c_int
+            L.lora_batch_update.argtypes = [ctypes.POINTER(_Batch), vp, vp, i32, vp]
+            L.lora_batch_refresh.restype = ctypes.c_int
+            L.lora_batch_refresh.argtypes = [ctypes.POINTER(_Batch), vp]
             L.lora_selftest_wait.restype = ctypes.c_int
             L.lora_selftest_wait.argtypes = [vp, vp]
             _lib = L
@@ -246,6 +253,26 @@ def lora_selftest_wait(counts: torch.Tensor, stream=None) -> None:
     if counts.dtype != torch.int32 or not counts.is_cuda or counts.numel() < len(COUNT_NAMES):
         raise ValueError("counts must be a CUDA int32 tensor of %d entries" % len(COUNT_NAMES))
     _check(lib().lora_selftest_wait(ctypes.c_void_p(counts.data_ptr()), ctypes.c_void_p(_stream(stream))))
+
+
+def lora_batch_update(batch: Batch, rows: torch.Tensor, new_ids: torch.Tensor, stream=None) -> Batch:
+    """Row rows[k] now carries adapter new_ids[k] (-1: none), on the device;
+    the batch's metadata is rebuilt lazily (lora_batch_refresh)."""
+    rows = rows.to(torch.int32).contiguous()
+    new_ids = new_ids.to(torch.int32).contiguous()
+    if rows.shape != new_ids.shape or rows.dim() != 1:
+        raise ValueError("rows and new_ids must be 1-D of the same length")
+    n = rows.numel()
+    _check(lib().lora_batch_update(ctypes.byref(batch.raw), _dev_ptr(rows, "rows") if n else None,
+                                   _dev_ptr(new_ids, "new_ids") if n else None, n, _stream(stream)))
+    batch._keep = (rows, new_ids)  # alive until the kernel that reads them has run
+    return batch
+
+
+def lora_batch_refresh(batch: Batch, stream=None) -> Batch:
+    """Rebuilds the metadata of a batch whose ids were updated."""
+    _check(lib().lora_batch_refresh(ctypes.byref(batch.raw), _stream(stream)))
+    return batch
 
 
 def lora_last_kernels() -> int:

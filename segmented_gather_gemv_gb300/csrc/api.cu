@@ -1,6 +1,7 @@
 // api.cu -- the extern "C" boundary of the library: argument checks,
 // workspace carving and kernel dispatch.  Declarations and the contract of
 // every entry point are in include/lora_sgmv.h.
+#include <climits>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -40,6 +41,35 @@ __global__ void selftest_wait_kernel(int32_t *counts) {
     __syncwarp();
     if (threadIdx.x == 0 && !mbar_wait(&bar, 0)) raise_deverr(counts, LORA_DEVERR_WAIT);
 }
+
+// lora_batch_update: for k < n in order, store[rows[k]] = new_ids[k].  The
+// warp takes 32 entries at a time; an entry whose row comes again later in
+// the same 32 is dropped, so the later entry wins.  The grid before may
+// still read the store: the writes wait for it.
+__global__ void batch_update_kernel(int32_t *__restrict__ store, int32_t M, const int32_t *__restrict__ rows,
+                                    const int32_t *__restrict__ new_ids, int32_t n, int32_t *counts) {
+    const int lane = threadIdx.x;
+    griddep_wait();
+    int bad = 0;
+    for (int base = 0; base < n; base += 32) {
+        const int k = base + lane;
+        const bool valid = k < n;
+        const int r = valid ? __ldg(rows + k) : INT_MIN + lane;  // distinct for the lanes past n
+        const int v = valid ? __ldg(new_ids + k) : 0;
+        const unsigned same = __match_any_sync(0xffffffffu, r);
+        const bool later = (same >> lane) > 1u;  // a later lane of this 32 has the same row
+        if (valid && !later) {
+            if (r >= 0 && r < M) store[r] = v;
+            else bad = 1;
+        }
+        __syncwarp();
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) raise_deverr(counts, LORA_DEVERR_ROW);
+}
+
+// Starts the kernels after it at once; launched without programmatic
+// serialization, it starts only after the kernel before it has finished.
+__global__ void order_kernel() { griddep_launch_dependents(); }
 
 namespace {
 
@@ -156,9 +186,28 @@ lora_status_t check_slices(const lora_batch_t *b, int32_t dtype, const lora_b_sl
 
 void fill_batch(const lora_batch_t *b, DeltaArgs &p) {
     p.ids = b->ids;
+    p.ids_after_wait = b->ids_store != nullptr && b->ids == b->ids_store ? 1 : 0;
     p.sorted = b->sorted_token_ids;
     p.tc_indptr = b->tc_indptr;
     p.counts = b->counts;
+}
+
+// Rebuilds a batch's segment metadata from its ids into its workspace.
+// prepare reads the ids before it waits on the grid before it, and an
+// update's kernel may be that grid: the ordering kernel (launched without
+// programmatic serialization, so it starts once the grid before it has
+// finished) goes first.
+cudaError_t refresh_metadata(const lora_batch_t *b, cudaStream_t stream) {
+    order_kernel<<<1, 32, 0, stream>>>();
+    cudaError_t oe = cudaGetLastError();
+    if (oe != cudaSuccess) return oe;
+    launch_counter().fetch_add(1, std::memory_order_relaxed);
+    const WsLayout L = ws_layout(b->M, b->n_adapters, b->chunk_size);
+    char *base = reinterpret_cast<char *>(b->seg_records) - L.rec;
+    lora_batch_t tmp{};
+    const int grid = tc_grid(b->M);
+    return launch_prepare(b->ids, b->M, b->n_adapters, b->chunk_size, b->tc_min_rows,
+                          b->order == LORA_ORDER_ASCENDING, grid <= kMaxShareGrid ? grid : 0, base, L, &tmp, stream);
 }
 
 // Launches the kernels of one call according to the path.
@@ -225,6 +274,14 @@ lora_status_t dispatch(const lora_batch_t *b, int32_t dtype, int mode, int32_t p
             }
             return LORA_OK;
         }
+    }
+    if (b->stale) {
+        // the ids changed since the metadata was built (lora_batch_update):
+        // rebuild it for the kernels below
+        e = refresh_metadata(b, stream);
+        if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "prepare launch failed: %s", cudaGetErrorString(e));
+        launch_counter().fetch_add(1, std::memory_order_relaxed);
+        g_last_kernels |= LORA_KERNEL_PREPARE;
     }
     if (path == LORA_PATH_TENSOR) {
         if (!tensor_ok || mode != kFused)
@@ -350,7 +407,57 @@ lora_status_t lora_prepare_batch_ordered(const int32_t *ids, int32_t M, int32_t 
     b.tc_min_rows = tc_min;
     b.magic = kBatchMagic;
     b.ids = ids;
+    b.ids_store = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + L.ids_store);
+    b.order = order;
+    b.stale = 0;
     *batch = b;
+    return LORA_OK;
+}
+
+lora_status_t lora_batch_update(lora_batch_t *batch, const int32_t *rows, const int32_t *new_ids, int32_t n,
+                                void *stream) {
+    g_err[0] = 0;
+    g_last_kernels = 0;
+    lora_status_t st;
+    if ((st = check_batch(batch))) return st;
+    if (n < 0) return fail(LORA_ERR_INVALID, "n %d < 0", n);
+    if (n > 0 && (!rows || !new_ids)) return fail(LORA_ERR_INVALID, "rows or new_ids is NULL");
+    if (n == 0 || batch->M == 0) return LORA_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (batch->ids != batch->ids_store)
+        e = cudaMemcpyAsync(batch->ids_store, batch->ids, (size_t)batch->M * 4, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess) {
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1);
+        cfg.blockDim = dim3(32);
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, batch_update_kernel, batch->ids_store, batch->M, rows, new_ids, n,
+                               batch->counts);
+    }
+    if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "update launch failed: %s", cudaGetErrorString(e));
+    launch_counter().fetch_add(1, std::memory_order_relaxed);
+    batch->ids = batch->ids_store;
+    batch->stale = 1;
+    return LORA_OK;
+}
+
+lora_status_t lora_batch_refresh(lora_batch_t *batch, void *stream) {
+    g_err[0] = 0;
+    g_last_kernels = 0;
+    lora_status_t st;
+    if ((st = check_batch(batch))) return st;
+    if (!batch->stale) return LORA_OK;
+    const cudaError_t e = refresh_metadata(batch, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "prepare launch failed: %s", cudaGetErrorString(e));
+    launch_counter().fetch_add(1, std::memory_order_relaxed);
+    g_last_kernels = LORA_KERNEL_PREPARE;
+    batch->stale = 0;
     return LORA_OK;
 }
 
@@ -424,7 +531,7 @@ lora_status_t lora_delta(const lora_batch_t *batch, int32_t dtype, const void *x
 
 const char *lora_last_error_string(void) { return g_err; }
 
-int32_t lora_abi_version(void) { return 100; }
+int32_t lora_abi_version(void) { return 200; }
 
 int64_t lora_launch_count(void) { return launch_counter().load(std::memory_order_relaxed); }
 

@@ -24,6 +24,7 @@ struct WsLayout {
     size_t first_pos, adapter_cnt, adapter_group;   // per adapter [n]
     size_t group_adapter, group_row, group_seg;      // per group [g_max]
     size_t warp_hist;                                // [32][g_max]
+    size_t ids_store;                                // [M]: the batch's own copy of the ids
     size_t total;
     int32_t max_segs, g_max;
 };
@@ -94,6 +95,7 @@ static inline WsLayout ws_layout(int32_t M, int32_t n, int32_t chunk) {
     L.group_row = take((size_t)gm + 1);
     L.group_seg = take((size_t)gm + 1);
     L.warp_hist = take((size_t)gm * 32);
+    L.ids_store = take(M > 0 ? (size_t)M : 1);
     L.total = o;
     return L;
 }
@@ -384,6 +386,8 @@ struct DeltaArgs {
     int32_t after_tc;          // 1: launched right after the tensor-core kernel, which waited on prepare
     int32_t after_cc;          // 1: tensor-core kernel launched right after the CUDA-core kernel, which waited on prepare
     int32_t trigger_after_wait;  // small-batch kernel: trigger the next grid only after its own wait
+    int32_t ids_after_wait;      // small-batch / streaming kernels: the ids may come from the grid
+                                 // before (lora_batch_update): read them only after the wait
     // CTA shares of the tensor-core row space computed by prepare for a grid
     // of tc_share_grid CTAs: boundary b = {first row of CTA b, its segment}
     const int2 *tc_share;

@@ -213,6 +213,8 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     // and this grid reads before its wait only what no grid of the stream
     // writes (see griddep_launch_dependents): the next grid may start at once.
     griddep_launch_dependents();
+    // ids written by the grid before (an updated batch): read after the wait
+    if (p.ids_after_wait) griddep_wait();
 
     // ---- phase 0: ids (one or two rows per thread), the adapters' ranks and
     // scales, and an empty hash table.  Everything read before the wait (ids,

@@ -311,6 +311,8 @@ __global__ void __launch_bounds__(kStThreads, 1)
     // batch metadata at its start: then this grid triggers only after its
     // wait on prepare.
     if (!p.trigger_after_wait) griddep_launch_dependents();
+    // ids written by the grid before (an updated batch): read after the wait
+    if (p.ids_after_wait) griddep_wait();
 
     // ---- phase 0: ids (rows tid * RPT .. tid * RPT + RPT - 1), the adapters'
     // ranks and scales, and an empty hash table.  Everything read before the

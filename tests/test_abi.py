@@ -71,4 +71,4 @@ def test_bad_arguments_rejected_before_any_cuda_call():
     st = L.lora_delta(ctypes.byref(raw), B.BF16, None, 0, 64, None, 0, 0, 16, None, 1, None,
                       ctypes.c_float(1.0), None, None, 0, 0, None)
     assert st == B.LORA_ERR_INVALID
-    assert L.lora_abi_version() == 100
+    assert L.lora_abi_version() == 200
