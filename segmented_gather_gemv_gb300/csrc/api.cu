@@ -45,10 +45,12 @@ __global__ void selftest_wait_kernel(int32_t *counts) {
 // lora_batch_update: for k < n in order, store[rows[k]] = new_ids[k].  The
 // warp takes 32 entries at a time; an entry whose row comes again later in
 // the same 32 is dropped, so the later entry wins.  The grid before may
-// still read the store: the writes wait for it.
+// still read the store: the writes wait for it.  The grid after may start at
+// once: it reads the ids only after its own wait, which covers this grid.
 __global__ void batch_update_kernel(int32_t *__restrict__ store, int32_t M, const int32_t *__restrict__ rows,
                                     const int32_t *__restrict__ new_ids, int32_t n, int32_t *counts) {
     const int lane = threadIdx.x;
+    griddep_launch_dependents();
     griddep_wait();
     int bad = 0;
     for (int base = 0; base < n; base += 32) {
