@@ -181,6 +181,10 @@ typedef struct lora_b_slice {
     int64_t stride_n;       /* elements between rows, >= r_max */
     int32_t d_out;          /* rows of this slice */
     int32_t y_col;          /* first y column written by this slice */
+    const void *A_pool;     /* lora_delta only: this slice's own A pool (a fused
+                               projection whose slices each have their A), laid
+                               out like the call's A_pool (same strides); NULL:
+                               the call's A_pool */
 } lora_b_slice_t;
 
 /*

@@ -218,7 +218,24 @@ def delta(x, ids, A_pool, B_pools, y_base, scale=1.0, adapter_scale=None,
 
     ``threads`` > 1 shares the token rows out over that many host threads
     (``oracle_delta_parallel``: the same per-row arithmetic, bit-identical
-    result); the number of threads used is then in ``delta.last_threads``."""
+    result); the number of threads used is then in ``delta.last_threads``.
+
+    ``A_pool`` may be a list with one pool per output slice (a fused
+    projection whose slices each have their own A): slice t's columns then
+    get s_id (x_i . A_t[id]^T) . B_t[id]^T, computed by this same per-token
+    routine on that slice alone (the slices write disjoint columns)."""
+    if isinstance(A_pool, (list, tuple)):
+        if not isinstance(B_pools, (list, tuple)):
+            B_pools = [B_pools]
+        assert len(A_pool) == len(B_pools) and not return_h
+        y = np.array(y_base, dtype=np.float64, copy=True)
+        col = 0
+        for A_t, B_t in zip(A_pool, B_pools):
+            d = B_t.shape[1]
+            y[:, col:col + d] = delta(x, ids, A_t, [B_t], y[:, col:col + d], scale=scale,
+                                      adapter_scale=adapter_scale, ranks=ranks, threads=threads)
+            col += d
+        return y
     lib = _load()
     if not isinstance(B_pools, (list, tuple)):
         B_pools = [B_pools]

@@ -71,7 +71,7 @@ class _Batch(ctypes.Structure):
 class _BSlice(ctypes.Structure):
     _fields_ = [("B_pool", ctypes.c_void_p), ("stride_adapter", ctypes.c_int64),
                 ("stride_n", ctypes.c_int64), ("d_out", ctypes.c_int32),
-                ("y_col", ctypes.c_int32)]
+                ("y_col", ctypes.c_int32), ("A_pool", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -388,16 +388,32 @@ def lora_expand(batch: Batch, h: torch.Tensor, B_pools, y: torch.Tensor, scale: 
     return y
 
 
-def lora_delta(batch: Batch, x: torch.Tensor, A_pool: torch.Tensor, B_pools, y: torch.Tensor,
+def lora_delta(batch: Batch, x: torch.Tensor, A_pool, B_pools, y: torch.Tensor,
                scale: float = 1.0, adapter_scale: Optional[torch.Tensor] = None,
                ranks: Optional[torch.Tensor] = None, y_cols: Optional[Sequence[int]] = None,
                path: int = PATH_AUTO, stream=None) -> torch.Tensor:
-    """y[i] += s_id * (x[i] . A_id^T) . B_id^T, fused (in place)."""
+    """y[i] += s_id * (x[i] . A_id^T) . B_id^T, fused (in place).
+
+    ``A_pool`` may be a list with one A pool per B pool (each slice of a fused
+    projection with its own A; the pools share shape and strides)."""
     _inner_contig(x, "x")
+    A_slices = None
+    if isinstance(A_pool, (list, tuple)):
+        A_slices = list(A_pool)
+        A_pool = A_slices[0]
+        for a in A_slices:
+            _inner_contig(a, "A_pool")
+            if a.shape != A_pool.shape or a.stride() != A_pool.stride():
+                raise ValueError("per-slice A pools must share shape and strides")
     _inner_contig(A_pool, "A_pool")
     _inner_contig(y, "y")
     n, r_max, d_in = A_pool.shape
     arr, ns = _slices(B_pools, y, y_cols, r_max, x.dtype)
+    if A_slices is not None:
+        if len(A_slices) != ns:
+            raise ValueError("one A pool per B pool")
+        for t, a in enumerate(A_slices):
+            arr[t].A_pool = _dev_ptr(a, "A_pool", x.dtype)
     rp, sp = _ranks_scale(ranks, adapter_scale)
     _check(lib().lora_delta(ctypes.byref(batch.raw), _dtype_code(x), _dev_ptr(x, "x"), _ld(x), d_in,
                             _dev_ptr(A_pool, "A_pool", x.dtype), _ld(A_pool), _ld(A_pool, 1),

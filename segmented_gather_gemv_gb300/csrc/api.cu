@@ -171,6 +171,7 @@ lora_status_t check_slices(const lora_batch_t *b, int32_t dtype, const lora_b_sl
             if (s.y_col < o.y_col + o.d_out && o.y_col < s.y_col + s.d_out)
                 return fail(LORA_ERR_INVALID, "slices %d and %d write overlapping y columns", u, t);
         }
+        p.slices[t].A = s.A_pool;
         p.slices[t].B = s.B_pool;
         p.slices[t].stride_adapter = s.stride_adapter;
         p.slices[t].stride_n = s.stride_n;
@@ -213,8 +214,8 @@ cudaError_t refresh_metadata(const lora_batch_t *b, cudaStream_t stream) {
 }
 
 // Launches the kernels of one call according to the path.
-lora_status_t dispatch(const lora_batch_t *b, int32_t dtype, int mode, int32_t path, int d_in, DeltaArgs &p,
-                       cudaStream_t stream) {
+lora_status_t dispatch_one(const lora_batch_t *b, int32_t dtype, int mode, int32_t path, int d_in, DeltaArgs &p,
+                           cudaStream_t stream) {
     g_last_kernels = 0;
     fill_batch(b, p);
     if (b->M == 0) return LORA_OK;
@@ -356,6 +357,53 @@ lora_status_t dispatch(const lora_batch_t *b, int32_t dtype, int mode, int32_t p
         }
     }
     if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+    return LORA_OK;
+}
+
+// A fused call whose slices have their own A pools: the streaming kernel
+// stacks the slices' rank blocks into one shrink where they fit (at most 64
+// stacked ranks); otherwise every slice runs as a call of its own.
+lora_status_t dispatch(const lora_batch_t *b, int32_t dtype, int mode, int32_t path, int d_in, DeltaArgs &p,
+                       cudaStream_t stream) {
+    bool per_slice_a = false;
+    for (int t = 0; t < p.n_slices; ++t) {
+        if (!p.slices[t].A) p.slices[t].A = p.A;
+        if (p.slices[t].A != p.A) per_slice_a = true;
+    }
+    if (!per_slice_a || mode != kFused) return dispatch_one(b, dtype, mode, path, d_in, p, stream);
+    const int rs = p.r_max <= 16 ? 16 : (p.r_max <= 32 ? 32 : 64);
+    if (dtype == LORA_BF16 && (path == LORA_PATH_AUTO || path == LORA_PATH_CUDA_CORE) && p.n_slices * rs <= 64 &&
+        (p.r_max == 16 || p.r_max == 32 || p.r_max == 64) && b->M > 0) {
+        g_last_kernels = 0;
+        fill_batch(b, p);
+        p.desc = reinterpret_cast<const SegDesc *>(b->seg_records);
+        p.max_list = b->max_segs;
+        p.M_rows = b->M;
+        p.n_adapters = b->n_adapters;
+        p.stacked = 1;
+        p.max_len = 0x7fffffff;
+        cudaError_t e = cudaSuccess;
+        if (try_launch_stream(p, sm_count(), stream, &e)) {
+            if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+            launch_counter().fetch_add(1, std::memory_order_relaxed);
+            g_last_kernels = LORA_KERNEL_STREAM;
+            return LORA_OK;
+        }
+        p.stacked = 0;
+    }
+    int32_t bits = 0;
+    for (int t = 0; t < p.n_slices; ++t) {
+        DeltaArgs q = p;
+        q.A = p.slices[t].A;
+        q.slices[0] = p.slices[t];
+        q.slices[0].col_begin = 0;
+        q.n_slices = 1;
+        q.d_out_total = p.slices[t].d_out;
+        const lora_status_t st = dispatch_one(b, dtype, mode, path, d_in, q, stream);
+        if (st != LORA_OK) return st;
+        bits |= g_last_kernels;
+    }
+    g_last_kernels = bits;
     return LORA_OK;
 }
 
@@ -518,6 +566,8 @@ lora_status_t lora_delta(const lora_batch_t *batch, int32_t dtype, const void *x
     if ((st = check_x_a(batch, dtype, x, ldx, d_in, A_pool, a_stride_adapter, a_stride_r, r_max))) return st;
     DeltaArgs p{};
     if ((st = check_slices(batch, dtype, slices, n_slices, r_max, y, ldy, p))) return st;
+    for (int t = 0; t < n_slices; ++t)
+        if (!aligned16(slices[t].A_pool)) return fail(LORA_ERR_UNSUPPORTED, "slice %d: A_pool not 16-byte aligned", t);
     p.x = x;
     p.ldx = ldx;
     p.d_in = d_in;

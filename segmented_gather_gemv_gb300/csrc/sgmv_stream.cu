@@ -91,7 +91,7 @@ constexpr int kSmRT = 16;                             // rows per tile: one 16-r
 constexpr int kSmMaxCluster = 8;
 constexpr int kSmMaxHashBytes = 48 * 1024;            // hash table (key, first row, count) at most
 
-constexpr int kSmMaxNChunks = 16;                     // N chunks per CTA at most
+constexpr int kSmMaxNChunks = 12;                     // N chunks per CTA at most
 
 // One N chunk of a CTA: output slice t, columns [cb, ce) of the
 // concatenated output (within slice t).
@@ -109,6 +109,8 @@ struct SmGeom {
     int xpitch, offA;    // bytes per x row in a K stage (kc * 2 + 16); A atoms in a K stage
     int ypitch, offB;    // bytes per y row in an N stage; B planes in an N stage
     int ncp;             // rows per B plane (a multiple of 128, >= the widest N chunk)
+    int stacked;         // 1: every slice has its own A; their rank blocks are stacked in one shrink
+    int rs, nrb_s;       // ranks per slice block when stacked (16, 32 or 64) and its 16-rank blocks
     int HS;              // hash slots (power of two, >= 2 distinct adapters)
     int tcap;            // tile records per CTA
     uint32_t ncl_magic;  // ceil(2^32 / clusters): x / clusters = umulhi(x, magic) for x < 2^16
@@ -123,7 +125,7 @@ struct SmGeom {
 // boxes, wi = 0, 1, 2 (no swizzle, 64-byte and 128-byte swizzle), for the
 // widths up to r_max.
 struct SmMaps {
-    CUtensorMap a;
+    CUtensorMap a[LORA_MAX_SLICES];  // per output slice (all the call's A pool unless stacked)
     CUtensorMap b[LORA_MAX_SLICES][3];
 };
 
@@ -510,14 +512,18 @@ __global__ void __launch_bounds__(kStThreads, 1)
         const int wi = ti.r <= 16 ? 0 : (ti.r <= 32 ? 1 : 2);  // B box of 16 << wi ranks
         if (c < g.nK) {
             const int kb = k0 + c * g.kc;
-            const int nA = ((ti.r + 15) >> 4) * g.natoms;  // 16-rank blocks x atoms
+            const int nbl = ((ti.r + 15) >> 4) * g.natoms;         // 16-rank blocks x atoms of one slice
+            const int nA = (g.stacked ? p.n_slices : 1) * nbl;
             if (w && lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)(nA * 2048 + R * g.kc * 2));
             {
-                // A: box (columns 64 at .., ranks 16 pb ..) -> atom pb * natoms + at
+                // A: box (columns 64 at .., ranks 16 pb ..) of slice t's pool
+                // -> atom (t nrb_s + pb) natoms + at (stacked), pb natoms + at
                 if (w)
                     for (int i = lane; i < nA; i += 32) {
-                        const int pb = i / g.natoms, at = i - pb * g.natoms;
-                        tma_3d(sb + g.offA + (uint32_t)i * 2048u, &m.a, kb + at * 64, pb * 16, ti.a, fb);
+                        const int t = i / nbl, rem = i - t * nbl;
+                        const int pb = rem / g.natoms, at = rem - pb * g.natoms;
+                        tma_3d(sb + g.offA + (uint32_t)(((t * g.nrb_s + pb) * g.natoms + at) * 2048), &m.a[t],
+                               kb + at * 64, pb * 16, ti.a, fb);
                     }
                 // x rows
                 if (act)
@@ -606,7 +612,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
     const int g_ = lane >> 2, t4 = lane & 3;
     // tile state
     TileRec ti{};
-    int r = 0, R = 0, r16a = 16, np = 1;
+    int r = 0, R = 0, r16a = 16, np = 1, npe = 1;
     float acc[2][2][4];
     uint32_t hf[KS][4], bm0[KS], bm1[KS];
     int st = 0;                        // stage of chunk j
@@ -621,8 +627,11 @@ __global__ void __launch_bounds__(kStThreads, 1)
             ti = tl[e];
             r = ti.r;
             R = ti.hi - ti.lo;
-            r16a = (r + 15) & ~15;
-            np = r16a / 16;
+            // rank blocks of the shrink (all slices' when stacked) and K
+            // steps of the expand
+            np = g.stacked ? p.n_slices * g.nrb_s : (r + 15) >> 4;
+            r16a = np * 16;
+            npe = (r + 15) >> 4;
             if (tid == 0) mbar_arrive_expect_tx(&recv_bar[e & 1], (uint32_t)(CL * 16 * r16a * 4));
 #pragma unroll
             for (int u = 0; u < 2; ++u)
@@ -687,6 +696,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
                         }
                     }
                 }
+                fence_proxy_async_cta();  // writes into the stage come before the producer's next copies
                 consumers_sync();
                 // CTA partial: the kw partials of each rank block summed in
                 // two levels (pairs kq, kq + 8 by all threads in place, then
@@ -708,6 +718,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
                                  "f"(__uint_as_float(x4.z) + __uint_as_float(y4.z)),
                                  "f"(__uint_as_float(x4.w) + __uint_as_float(y4.w))
                                  : "memory");
+                    fence_proxy_async_cta();
                     consumers_sync();
                 }
                 if (tid < nel4) {
@@ -743,10 +754,11 @@ __global__ void __launch_bounds__(kStThreads, 1)
                             add4(s4, *reinterpret_cast<const float4 *>(rv + ((size_t)pr * 16 + row) * R16 + col));
                     const bool rok = row < R;
                     const float sc = ti.sc;
-                    const float h0 = rok && col + 0 < r ? s4.x * sc : 0.f;
-                    const float h1 = rok && col + 1 < r ? s4.y * sc : 0.f;
-                    const float h2 = rok && col + 2 < r ? s4.z * sc : 0.f;
-                    const float h3 = rok && col + 3 < r ? s4.w * sc : 0.f;
+                    const int cin = g.stacked ? (col & (g.rs - 1)) : col;  // rank within its slice
+                    const float h0 = rok && cin + 0 < r ? s4.x * sc : 0.f;
+                    const float h1 = rok && cin + 1 < r ? s4.y * sc : 0.f;
+                    const float h2 = rok && cin + 2 < r ? s4.z * sc : 0.f;
+                    const float h3 = rok && cin + 3 < r ? s4.w * sc : 0.f;
                     *reinterpret_cast<uint2 *>(hbf + row * hpitch + col * 2) =
                         make_uint2(bf16x2_bits(h0, h1), bf16x2_bits(h2, h3));
                 }
@@ -757,11 +769,13 @@ __global__ void __launch_bounds__(kStThreads, 1)
             // h and B: slots 2t, 2t+1 hold ranks 4t, 4t+1 and slots 2t+8,
             // 2t+9 hold ranks 4t+2, 4t+3, so a thread's two B words (and two
             // h words) are eight contiguous bytes: one 64-bit load.
-            if (c == g.nK) {
-                const uint32_t hb = smem_u32(hbf) + g_ * hpitch + 8 * t4;
+            const NChunk ck = nck[c - g.nK];
+            if (c == g.nK || g.stacked) {
+                // h of this chunk's slice: its block of columns when stacked
+                const uint32_t hb = smem_u32(hbf) + g_ * hpitch + 8 * t4 + (g.stacked ? ck.t * g.rs * 2 : 0);
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
-                    if (ks < np) {
+                    if (ks < npe) {
                         const uint2 lo2 = lds64(hb + ks * 32);
                         const uint2 hi2 = lds64(hb + 8 * hpitch + ks * 32);
                         hf[ks][0] = lo2.x;
@@ -774,7 +788,6 @@ __global__ void __launch_bounds__(kStThreads, 1)
                     bm1[ks] = (kk + 3 < r ? 0xFFFF0000u : 0u) | (kk + 2 < r ? 0x0000FFFFu : 0u);
                 }
             }
-            const NChunk ck = nck[c - g.nK];
             const int nnt = (ck.ce - ck.cb) >> 3;
             // B fragment of K step ks, 8-column tile nt: row n = 8 nt + g_
             // (2w bytes, w = 16 << wi ranks), 16-byte chunk 2 ks + t4 / 2
@@ -795,9 +808,10 @@ __global__ void __launch_bounds__(kStThreads, 1)
             // (in flight together) while two remain, then one
             int nt = warp;
             for (; nt + kSmWarps < nnt; nt += 2 * kSmWarps)
-                expand_tiles<KS, 2>(nt, np, sBa, boff, rsh, yr0, yr1, row0, row1, hf, bm0, bm1);
+                expand_tiles<KS, 2>(nt, npe, sBa, boff, rsh, yr0, yr1, row0, row1, hf, bm0, bm1);
             for (; nt < nnt; nt += kSmWarps)
-                expand_tiles<KS, 1>(nt, np, sBa, boff, rsh, yr0, yr1, row0, row1, hf, bm0, bm1);
+                expand_tiles<KS, 1>(nt, npe, sBa, boff, rsh, yr0, yr1, row0, row1, hf, bm0, bm1);
+            fence_proxy_async_cta();  // the y + delta writes come before the producer's next copies
             consumers_sync();
             // the rows leave by 16-byte stores: warp w takes row w / hv and
             // the 8-column pieces w % hv, w % hv + hv, ... (hv = 2 when R <= 8)
@@ -815,9 +829,8 @@ __global__ void __launch_bounds__(kStThreads, 1)
                 }
             }
         }
-        // release the stage: this thread's accesses to it come before the
-        // producer's next copies into it
-        fence_proxy_async_cta();
+        // release the stage (its writes were fenced where they happened;
+        // the reads are ordered by the barrier)
         __syncwarp();
         if (lane == 0) mbar_arrive1(&empty[st]);
         if (++st == D) {
@@ -859,6 +872,10 @@ static bool small_geometry(const DeltaArgs &p, int R16, int cl, int ncl, SmGeom 
     g = SmGeom{};
     g.CL = cl;
     g.KC = p.d_in / cl;
+    g.stacked = p.stacked ? 1 : 0;
+    g.rs = p.r_max <= 16 ? 16 : (p.r_max <= 32 ? 32 : 64);
+    g.nrb_s = g.rs / 16;
+    if (g.stacked && p.n_slices * g.rs > R16) return false;
     g.RPT = M <= kSmThreads ? 1 : (M <= 2 * kSmThreads ? 2 : 4);
     const int nv = p.d_out_total / 8;
     int ncol0[kSmMaxCluster + 1];
@@ -1053,9 +1070,12 @@ bool small_maps(const DeltaArgs &p, SmMaps &m) {
     // B boxes of 16, 32 or 64 ranks, none wider than the pool: pools padded
     // to one of those widths
     if (p.r_max != 16 && p.r_max != 32 && p.r_max != 64) return false;
-    if (!encode_3d(&m.a, p.A, (uint64_t)p.d_in, (uint64_t)p.r_max, (uint64_t)p.n_adapters,
-                   (uint64_t)p.a_stride_r * 2, (uint64_t)p.a_stride_adapter * 2, 64, 16, 2))
-        return false;
+    for (int t = 0; t < (p.stacked ? p.n_slices : 1); ++t) {
+        const void *A = p.stacked && p.slices[t].A ? p.slices[t].A : p.A;
+        if (!encode_3d(&m.a[t], A, (uint64_t)p.d_in, (uint64_t)p.r_max, (uint64_t)p.n_adapters,
+                       (uint64_t)p.a_stride_r * 2, (uint64_t)p.a_stride_adapter * 2, 64, 16, 2))
+            return false;
+    }
     for (int t = 0; t < p.n_slices; ++t) {
         const SliceDesc &sl = p.slices[t];
         for (int wi = 0; wi < 3 && (16 << wi) <= p.r_max; ++wi)
@@ -1149,7 +1169,9 @@ bool try_launch_stream(const DeltaArgs &p, int sms, cudaStream_t stream, cudaErr
     if (p.r_max > 64 || p.ids == nullptr || p.M_rows < 1 || p.M_rows > kSmMaxRows) return false;
     SmMaps maps;
     if (!small_maps(p, maps)) return false;
-    const int R16 = small_r16(p.r_max);
+    const int rs = p.r_max <= 16 ? 16 : (p.r_max <= 32 ? 32 : 64);
+    if (p.stacked && p.n_slices * rs > 64) return false;
+    const int R16 = p.stacked ? small_r16(p.n_slices * rs) : small_r16(p.r_max);
     const int cl0 = small_cluster_size(p.d_in, p.d_out_total);
     // the preferred cluster size first, then larger ones, then smaller ones
     int order[8], no = 0;

@@ -453,3 +453,46 @@ def test_split_calls_full_size(B, name):
     assert e2 <= TOL[w.dtype], "expand rel err %.3e" % e2
     assert np.array_equal(yg[~act], w.y[~act].astype(np.float64))
     assert batch.counts()["device_error"] == 0
+
+
+# ------------------------------------------------- per-slice A pools
+
+# (workload kwargs, path, kernel): the stacked shrink on the streaming kernel
+# (QKV with r 16: 48 stacked ranks; two slices of r 32; a decode-sized batch),
+# and one pass per slice where the stacked ranks exceed 64 (decode batch with
+# r 32 on the small-batch kernel, rank 64) or the batch exceeds the streaming
+# kernel's limit
+PER_SLICE_A_CASES = [
+    (dict(M=700, d_in=1024, d_outs=[1024, 256, 256], n_pool=40, r_max=16, run_len=20,
+          ranks=[8, 16], per_adapter_scale=True, skip_frac=0.1), 0, "sgmv_stream_kernel"),
+    (dict(M=1200, d_in=512, d_outs=[384, 128], n_pool=30, r_max=32, ranks=[8, 24, 32]), 1, "sgmv_stream_kernel"),
+    (dict(M=200, d_in=1024, d_outs=[512, 256, 256], n_pool=20, r_max=16), 0, "sgmv_stream_kernel"),
+    (dict(M=200, d_in=1024, d_outs=[512, 256, 256], n_pool=20, r_max=32), 0, "sgmv_small_kernel"),
+    (dict(M=600, d_in=512, d_outs=[256, 128], n_pool=10, r_max=64, ranks=[8, 64], run_len=40), 0, None),
+    (dict(M=5000, d_in=256, d_outs=[256, 128, 128], n_pool=60, r_max=16, run_len=50), 0, None),
+]
+
+
+@pytest.mark.parametrize("ci", range(len(PER_SLICE_A_CASES)))
+def test_per_slice_a(B, ci):
+    kw, path, kernel = PER_SLICE_A_CASES[ci]
+    w = wl.random_batch(seed=980 + ci, dtype="bf16", **kw)
+    rng = np.random.default_rng(981 + ci)
+    A_pools = [w.A] + [wl.round_bf16((rng.standard_normal(w.A.shape) / np.sqrt(w.A.shape[2])).astype(np.float32))
+                       for _ in w.B[1:]]
+    d = to_dev(w)
+    A_dev = [torch.from_numpy(a).to(device="cuda", dtype=torch.bfloat16) for a in A_pools]
+    batch = B.lora_prepare_batch(d["ids"], w.n_adapters, w.chunk_size)
+    y = d["y"].clone()
+    B.lora_delta(batch, d["x"], A_dev, d["B"], y, scale=w.scale, adapter_scale=d["adapter_scale"],
+                 ranks=d["ranks"], path=path)
+    if kernel is not None:
+        assert B.KERNEL_NAMES.get(B.lora_last_kernels()) == kernel
+    torch.cuda.synchronize()
+    yg = y.float().cpu().numpy().astype(np.float64)
+    ref = oracle.delta(w.x, w.ids, A_pools, w.B, w.y, scale=w.scale, adapter_scale=w.adapter_scale,
+                       ranks=w.ranks)
+    act = active_rows(w)
+    assert rel_err(yg, ref, w.y.astype(np.float64), act) <= TOL["bf16"]
+    assert np.array_equal(yg[~act], w.y[~act].astype(np.float64))
+    assert batch.counts()["device_error"] == 0

@@ -330,3 +330,52 @@ def test_parallel_delta_is_bit_identical(case):
                       ranks=w.ranks, threads=4)
     assert np.array_equal(y1, y4)
     assert oracle.delta.last_threads >= 1
+
+
+# ---- per-slice A (a fused projection whose slices each have their own A)
+
+def _brute_delta_per_slice_a(w, A_pools):
+    x = w.x.astype(np.float64)
+    y = w.y.astype(np.float64).copy()
+    col = 0
+    for A_t, B in zip(A_pools, w.B):
+        for a in range(w.n_adapters):
+            rows = np.nonzero(w.ids == a)[0]
+            if rows.size == 0:
+                continue
+            r = w.r_max if w.ranks is None else int(w.ranks[a])
+            s = w.scale if w.adapter_scale is None else float(w.adapter_scale[a])
+            H = x[rows] @ A_t[a, :r, :].astype(np.float64).T
+            y[np.ix_(rows, np.arange(col, col + B.shape[1]))] += s * (H @ B[a, :, :r].astype(np.float64).T)
+        col += B.shape[1]
+    return y
+
+
+@pytest.mark.parametrize("case", [
+    dict(M=40, d_in=32, d_outs=[24, 8, 16], n_pool=6, r_max=8, skip_frac=0.2),
+    dict(M=29, d_in=48, d_outs=[16, 16], n_pool=4, r_max=16, ranks=[4, 8, 16], per_adapter_scale=True),
+])
+def test_per_slice_a_brute_force(case):
+    w = wl.random_batch(seed=11, dtype="f32", **case)
+    rng = np.random.default_rng(12)
+    A_pools = [w.A] + [rng.standard_normal(w.A.shape).astype(np.float32) for _ in w.B[1:]]
+    y = oracle.delta(w.x, w.ids, A_pools, w.B, w.y, scale=w.scale, adapter_scale=w.adapter_scale,
+                     ranks=w.ranks)
+    assert _rel_err(y, _brute_delta_per_slice_a(w, A_pools), w.y) < 1e-12
+    # a slice's A pool changes only that slice's columns
+    A2 = list(A_pools)
+    A2[-1] = A2[-1] * 2
+    y2 = oracle.delta(w.x, w.ids, A2, w.B, w.y, scale=w.scale, adapter_scale=w.adapter_scale,
+                      ranks=w.ranks)
+    last = sum(w.d_outs[:-1])
+    assert np.array_equal(y2[:, :last], y[:, :last])
+    act = (w.ids >= 0) & (w.ids < w.n_adapters)
+    assert np.allclose(y2[act, last:] - w.y[act, last:], 2 * (y[act, last:] - w.y[act, last:]), rtol=1e-12, atol=1e-12)
+
+
+def test_per_slice_a_equal_pools_is_the_shared_a():
+    w = wl.random_batch(seed=13, M=33, d_in=40, d_outs=[24, 8], n_pool=5, r_max=8, dtype="f32",
+                        skip_frac=0.1)
+    shared = oracle.delta(w.x, w.ids, w.A, w.B, w.y, scale=w.scale)
+    per = oracle.delta(w.x, w.ids, [w.A, w.A], w.B, w.y, scale=w.scale)
+    assert np.array_equal(shared, per)
