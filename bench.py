@@ -94,6 +94,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
     ap.add_argument("--extra-steps", type=int, default=500)
+    ap.add_argument("--b-layout", choices=["rank_contiguous", "rank_major"], default="rank_contiguous",
+                    help="B pools [n][d_out][r_max] or [n][r_max][d_out] (main workload only)")
     return ap.parse_args(argv)
 
 
@@ -331,7 +333,7 @@ def run_reference(args, rank: int, world: int):
 class Bench:
     """Input sets, graphs and timings of one workload on one GPU."""
 
-    def __init__(self, w: wl.Workload, args, dev, stream, path: int):
+    def __init__(self, w: wl.Workload, args, dev, stream, path: int, rank_major: bool = False):
         import torch
         from segmented_gather_gemv_gb300 import binding as B
         self.torch, self.B = torch, B
@@ -344,7 +346,11 @@ class Bench:
         x0 = torch.from_numpy(w.x).to(dev, self.tdt)
         y0 = torch.from_numpy(w.y).to(dev, self.tdt)
         A0 = torch.from_numpy(w.A).to(dev, self.tdt)
+        # rank-major B pools, (n, r_max, d_out): an adapter reads only its rank's rows
+        self.rank_major = rank_major
         B0 = [torch.from_numpy(b).to(dev, self.tdt) for b in w.B]
+        if rank_major:
+            B0 = [b.transpose(1, 2).contiguous() for b in B0]
         ids0 = torch.from_numpy(w.ids).to(dev)
         self.ranks = None if w.ranks is None else torch.from_numpy(w.ranks).to(dev)
         self.ascale = None if w.adapter_scale is None else torch.from_numpy(w.adapter_scale).to(dev)
@@ -363,7 +369,7 @@ class Bench:
                                          workspace=s["ws"], stream=self.stream)
 
     def delta(self, batch, s, path=None):
-        self.B.lora_delta(batch, s["x"], s["A"], s["B"], s["y"], scale=self.w.scale,
+        self.B.lora_delta(batch, s["x"], s["A"], s["B"], s["y"], scale=self.w.scale, b_rank_major=self.rank_major,
                           adapter_scale=self.ascale, ranks=self.ranks,
                           path=self.path if path is None else path, stream=self.stream)
 
@@ -627,7 +633,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     W = max(3, args.warmup)
     w = factory(replica_seed(rank))
     stream = torch.cuda.Stream(device=dev)
-    b = Bench(w, args, dev, stream, args.path)
+    b = Bench(w, args, dev, stream, args.path, rank_major=args.b_layout == "rank_major")
 
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     clocks = ClockSampler(vis.split(",")[local_rank].strip() if vis else str(local_rank))
@@ -664,6 +670,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             "workload": w.name, "tokens_per_step": w.M, "active_rows": ab["active_rows"],
             "touched_adapters": ab["touched_adapters"], "num_segs": m["counts"]["num_segs"],
             "chunk_size": w.chunk_size, "path": ["auto", "cuda_core", "tensor"][args.path],
+            "b_layout": args.b_layout,
             "l2": "inputs rotate over %d sets (%.0f MB > %d MB L2)"
                   % (m["n_sets"], m["n_sets"] * b_set_bytes(w) / 1e6, L2_BYTES // 2**20),
             "timing": ("CUDA graphs of %d steps (kernels chained by programmatic dependent launch), "

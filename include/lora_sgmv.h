@@ -176,15 +176,28 @@ typedef struct lora_batch {
 /* One output slice of the expand step: B pool and the y columns it writes
  * (a fused projection such as QKV keeps one B pool per slice). */
 typedef struct lora_b_slice {
-    const void *B_pool;     /* device, [n_adapters][d_out][>= r_max] */
-    int64_t stride_adapter; /* elements between adapters, >= d_out * stride_n */
-    int64_t stride_n;       /* elements between rows, >= r_max */
+    const void *B_pool;     /* device; element (adapter a, output n, rank k) at
+                               a * stride_adapter + n * stride_n + k * stride_r */
+    int64_t stride_adapter; /* elements between adapters */
+    int64_t stride_n;       /* elements between outputs: >= r_max when stride_r <= 1
+                               ([n_adapters][d_out][>= r_max], rank-contiguous rows);
+                               1 when rank-major */
     int32_t d_out;          /* rows of this slice */
     int32_t y_col;          /* first y column written by this slice */
     const void *A_pool;     /* lora_delta only: this slice's own A pool (a fused
                                projection whose slices each have their A), laid
                                out like the call's A_pool (same strides); NULL:
                                the call's A_pool */
+    int64_t stride_r;       /* elements between ranks: 0 or 1 (rank-contiguous rows,
+                               the default), or >= d_out with stride_n = 1: the
+                               rank-major layout [n_adapters][>= r_max][d_out], in
+                               which an adapter of rank r reads r whole rows and
+                               no padding ("vLLM-Ascend LoRA" article, section
+                               4.2: adapter-major, rank-secondary weight blocks).
+                               All slices of a call share one layout; rank-major
+                               pools run on the streaming kernel only (bf16
+                               lora_delta, batches it takes), other calls return
+                               LORA_ERR_UNSUPPORTED. */
 } lora_b_slice_t;
 
 /*

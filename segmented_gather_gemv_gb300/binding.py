@@ -71,7 +71,7 @@ class _Batch(ctypes.Structure):
 class _BSlice(ctypes.Structure):
     _fields_ = [("B_pool", ctypes.c_void_p), ("stride_adapter", ctypes.c_int64),
                 ("stride_n", ctypes.c_int64), ("d_out", ctypes.c_int32),
-                ("y_col", ctypes.c_int32), ("A_pool", ctypes.c_void_p)]
+                ("y_col", ctypes.c_int32), ("A_pool", ctypes.c_void_p), ("stride_r", ctypes.c_int64)]
 
 
 _lock = threading.Lock()
@@ -327,7 +327,7 @@ def lora_prepare_batch_static(ids: torch.Tensor, n_adapters: int, chunk_size: in
     return Batch(raw, None, ids)
 
 
-def _slices(B_pools, y: torch.Tensor, y_cols, r_max: int, dtype):
+def _slices(B_pools, y: torch.Tensor, y_cols, r_max: int, dtype, rank_major: bool = False):
     if isinstance(B_pools, torch.Tensor):
         B_pools = [B_pools]
     B_pools = list(B_pools)
@@ -337,14 +337,21 @@ def _slices(B_pools, y: torch.Tensor, y_cols, r_max: int, dtype):
     col = 0
     for t, B in enumerate(B_pools):
         if B.dim() != 3 or B.dtype != dtype:
-            raise ValueError("B pool %d must be (n, d_out, r_max) of the input dtype" % t)
+            raise ValueError("B pool %d must be (n, %s) of the input dtype"
+                             % (t, "r_max, d_out" if rank_major else "d_out, r_max"))
         _inner_contig(B, "B pool")
         arr[t].B_pool = _dev_ptr(B, "B pool")
         arr[t].stride_adapter = _ld(B)
-        arr[t].stride_n = _ld(B, 1)
-        arr[t].d_out = B.shape[1]
+        d_out = B.shape[2] if rank_major else B.shape[1]
+        if rank_major:  # (n, r_max, d_out): rank rows of d_out outputs
+            arr[t].stride_n = 1
+            arr[t].stride_r = _ld(B, 1)
+        else:
+            arr[t].stride_n = _ld(B, 1)
+            arr[t].stride_r = 0
+        arr[t].d_out = d_out
         arr[t].y_col = int(y_cols[t]) if y_cols is not None else col
-        col += B.shape[1]
+        col += d_out
     return arr, len(B_pools)
 
 
@@ -391,11 +398,12 @@ def lora_expand(batch: Batch, h: torch.Tensor, B_pools, y: torch.Tensor, scale: 
 def lora_delta(batch: Batch, x: torch.Tensor, A_pool, B_pools, y: torch.Tensor,
                scale: float = 1.0, adapter_scale: Optional[torch.Tensor] = None,
                ranks: Optional[torch.Tensor] = None, y_cols: Optional[Sequence[int]] = None,
-               path: int = PATH_AUTO, stream=None) -> torch.Tensor:
+               path: int = PATH_AUTO, stream=None, b_rank_major: bool = False) -> torch.Tensor:
     """y[i] += s_id * (x[i] . A_id^T) . B_id^T, fused (in place).
 
     ``A_pool`` may be a list with one A pool per B pool (each slice of a fused
-    projection with its own A; the pools share shape and strides)."""
+    projection with its own A; the pools share shape and strides).  With
+    ``b_rank_major`` the B pools are (n, r_max, d_out): rank-major."""
     _inner_contig(x, "x")
     A_slices = None
     if isinstance(A_pool, (list, tuple)):
@@ -408,7 +416,7 @@ def lora_delta(batch: Batch, x: torch.Tensor, A_pool, B_pools, y: torch.Tensor,
     _inner_contig(A_pool, "A_pool")
     _inner_contig(y, "y")
     n, r_max, d_in = A_pool.shape
-    arr, ns = _slices(B_pools, y, y_cols, r_max, x.dtype)
+    arr, ns = _slices(B_pools, y, y_cols, r_max, x.dtype, rank_major=b_rank_major)
     if A_slices is not None:
         if len(A_slices) != ns:
             raise ValueError("one A pool per B pool")

@@ -161,9 +161,21 @@ lora_status_t check_slices(const lora_batch_t *b, int32_t dtype, const lora_b_sl
         if (b->M > 0 && !s.B_pool) return fail(LORA_ERR_INVALID, "slice %d: B_pool is NULL", t);
         if (!aligned16(s.B_pool)) return fail(LORA_ERR_UNSUPPORTED, "slice %d: B_pool not 16-byte aligned", t);
         if (s.d_out < 1 || s.d_out % V) return fail(LORA_ERR_UNSUPPORTED, "slice %d: d_out %d not a multiple of %d", t, s.d_out, V);
-        if (s.stride_n < r_max || (s.stride_n * es) % 16) return fail(LORA_ERR_UNSUPPORTED, "slice %d: stride_n invalid", t);
-        if (s.stride_adapter < (int64_t)s.d_out * s.stride_n || (s.stride_adapter * es) % 16)
-            return fail(LORA_ERR_UNSUPPORTED, "slice %d: stride_adapter invalid", t);
+        const bool rank_major = s.stride_r > 1;
+        if (t > 0 && rank_major != (p.b_rank_major != 0))
+            return fail(LORA_ERR_UNSUPPORTED, "slices %d and 0 have different B layouts", t);
+        p.b_rank_major = rank_major ? 1 : 0;
+        if (rank_major) {
+            if (s.stride_n != 1 || s.stride_r < s.d_out || (s.stride_r * es) % 16)
+                return fail(LORA_ERR_UNSUPPORTED, "slice %d: rank-major B needs stride_n 1 and stride_r >= d_out", t);
+            if (s.stride_adapter < (int64_t)r_max * s.stride_r || (s.stride_adapter * es) % 16)
+                return fail(LORA_ERR_UNSUPPORTED, "slice %d: stride_adapter invalid", t);
+        } else {
+            if (s.stride_n < r_max || (s.stride_n * es) % 16)
+                return fail(LORA_ERR_UNSUPPORTED, "slice %d: stride_n invalid", t);
+            if (s.stride_adapter < (int64_t)s.d_out * s.stride_n || (s.stride_adapter * es) % 16)
+                return fail(LORA_ERR_UNSUPPORTED, "slice %d: stride_adapter invalid", t);
+        }
         if (s.y_col < 0 || s.y_col % V || (int64_t)s.y_col + s.d_out > ldy)
             return fail(LORA_ERR_UNSUPPORTED, "slice %d: y_col %d invalid", t, s.y_col);
         for (int u = 0; u < t; ++u) {
@@ -175,6 +187,7 @@ lora_status_t check_slices(const lora_batch_t *b, int32_t dtype, const lora_b_sl
         p.slices[t].B = s.B_pool;
         p.slices[t].stride_adapter = s.stride_adapter;
         p.slices[t].stride_n = s.stride_n;
+        p.slices[t].stride_r = rank_major ? s.stride_r : 1;
         p.slices[t].d_out = s.d_out;
         p.slices[t].y_col = s.y_col;
         p.slices[t].col_begin = col;
@@ -236,6 +249,19 @@ lora_status_t dispatch_one(const lora_batch_t *b, int32_t dtype, int mode, int32
     // tensor-core grid of one CTA per 64 rows that takes the long groups).
     // With kStreamSplitTc set, LORA_PATH_AUTO gives the long groups to the
     // tensor-core kernel instead.
+    if (p.b_rank_major) {
+        // rank-major B pools: the streaming kernel only
+        if (mode == kFused && dtype == LORA_BF16 && (path == LORA_PATH_AUTO || path == LORA_PATH_CUDA_CORE) &&
+            try_launch_stream(p, sms, stream, &e)) {
+            if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+            launch_counter().fetch_add(1, std::memory_order_relaxed);
+            g_last_kernels = LORA_KERNEL_STREAM;
+            return LORA_OK;
+        }
+        return fail(LORA_ERR_UNSUPPORTED,
+                    "rank-major B pools run on the streaming kernel only (bf16 lora_delta, at most 2048 rows, "
+                    "r_max 16, 32 or 64)");
+    }
     if (mode == kFused && dtype == LORA_BF16 && (path == LORA_PATH_AUTO || path == LORA_PATH_CUDA_CORE)) {
         if (b->M <= kSmallAutoRows) {
             if (try_launch_small(p, sms, stream, &e)) {

@@ -360,7 +360,7 @@ __device__ __forceinline__ void raise_deverr(int32_t *counts, int bit) {
 struct SliceDesc {
     const void *A;  // this slice's A pool (the call's A pool when it has none of its own)
     const void *B;
-    int64_t stride_adapter, stride_n;
+    int64_t stride_adapter, stride_n, stride_r;  // stride_r 1: rank-contiguous rows; > 1: rank-major
     int32_t d_out, y_col, col_begin;  // col_begin: first column in the concatenated N range
 };
 
@@ -388,6 +388,7 @@ struct DeltaArgs {
     int32_t after_cc;          // 1: tensor-core kernel launched right after the CUDA-core kernel, which waited on prepare
     int32_t trigger_after_wait;  // small-batch kernel: trigger the next grid only after its own wait
     int32_t stacked;             // streaming kernel: per-slice A pools, their rank blocks stacked in one shrink
+    int32_t b_rank_major;        // B pools laid out [n][r][d_out] (streaming kernel only)
     int32_t ids_after_wait;      // small-batch / streaming kernels: the ids may come from the grid
                                  // before (lora_batch_update): read them only after the wait
     // CTA shares of the tensor-core row space computed by prepare for a grid

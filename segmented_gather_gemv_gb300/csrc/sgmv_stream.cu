@@ -236,17 +236,35 @@ __device__ __forceinline__ void mbar_arrive1(uint64_t *bar) {
 // The expand of the 8-column tiles nt0, nt0 + 16, ... (NB of them) of a
 // warp: B words and y words first, then the products, then y + delta in
 // fp32, rounded once, back into the y rows of the stage.
-template <int KS, int NB>
+__device__ __forceinline__ uint2 ldsm_x2_trans(uint32_t addr) {
+    uint2 r;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];\n" : "=r"(r.x), "=r"(r.y) : "r"(addr));
+    return r;
+}
+// RM false: B rows of 2w bytes (one output column each), the thread's eight
+// bytes of K step ks at boff[ks] (rsh = log2 of the row bytes).  RM true:
+// rank-major B in 64-column atoms of w rank rows x 128 bytes (128-byte
+// swizzle), read by ldmatrix.trans: lane l < 16 addresses rank row 16 ks + l
+// (sBa = the atoms' base + l * 128, boff[ks] = 16 ks * 128, rsh = log2 of an
+// atom's bytes), chunk (column tile & 7) ^ (l & 7).
+template <int KS, int NB, bool RM>
 __device__ __forceinline__ void expand_tiles(int nt0, int np, uint32_t sBa, const uint32_t (&boff)[KS], uint32_t rsh, uint32_t yr0,
                                              uint32_t yr1, bool row0, bool row1, const uint32_t (&hf)[KS][4],
-                                             const uint32_t (&bm0)[KS], const uint32_t (&bm1)[KS]) {
+                                             const uint32_t (&bm0)[KS], const uint32_t (&bm1)[KS], uint32_t lsw) {
     uint2 bw[NB][KS];
 #pragma unroll
-    for (int b = 0; b < NB; ++b)
+    for (int b = 0; b < NB; ++b) {
+        const int nt = nt0 + b * 16;
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks)
-            bw[b][ks] = ks < np ? lds64(sBa + boff[ks] + ((uint32_t)(nt0 + b * 16) << (rsh + 3)))
-                                : make_uint2(0u, 0u);
+        for (int ks = 0; ks < KS; ++ks) {
+            if (RM)
+                bw[b][ks] = ks < np ? ldsm_x2_trans(sBa + boff[ks] + ((uint32_t)(nt >> 3) << rsh) +
+                                                   ((((uint32_t)nt & 7u) ^ lsw) << 4))
+                                    : make_uint2(0u, 0u);
+            else
+                bw[b][ks] = ks < np ? lds64(sBa + boff[ks] + ((uint32_t)nt << (rsh + 3))) : make_uint2(0u, 0u);
+        }
+    }
     uint32_t y0[NB], y1[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
@@ -536,14 +554,22 @@ __global__ void __launch_bounds__(kStThreads, 1)
             const NChunk ck = nck[c - g.nK];
             const SliceDesc &sl = p.slices[ck.t];
             const int ncols = ck.ce - ck.cb;
-            const int nbx = (ncols + 127) >> 7;
-            if (w && lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)(nbx * (4096 << wi) + R * ncols * 2));
+            // B boxes of 128 columns x (16 << wi) ranks (rank-contiguous
+            // rows), or 64 columns x (16 << wi) rank rows (rank-major)
+            const int cw = p.b_rank_major ? 64 : 128;
+            const int nbx = (ncols + cw - 1) / cw;
+            const uint32_t bb = (uint32_t)cw * (32u << wi);  // bytes per box
+            if (w && lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)(nbx * bb + R * ncols * 2));
             {
-                // B: box (ranks 0 .. 16 << wi, columns 128 bx ..) -> rows 128 bx ..
                 if (w)
-                    for (int bx = lane; bx < nbx; bx += 32)
-                        tma_3d(sb + g.offB + (uint32_t)(bx * (4096 << wi)), &m.b[ck.t][wi], 0,
-                               ck.cb - sl.col_begin + bx * 128, ti.a, fb);
+                    for (int bx = lane; bx < nbx; bx += 32) {
+                        if (p.b_rank_major)
+                            tma_3d(sb + g.offB + (uint32_t)bx * bb, &m.b[ck.t][wi], ck.cb - sl.col_begin + bx * cw, 0,
+                                   ti.a, fb);
+                        else
+                            tma_3d(sb + g.offB + (uint32_t)bx * bb, &m.b[ck.t][wi], 0, ck.cb - sl.col_begin + bx * cw,
+                                   ti.a, fb);
+                    }
                 // y rows
                 if (act)
                     for (int i = lane; i < R; i += 32)
@@ -775,17 +801,32 @@ __global__ void __launch_bounds__(kStThreads, 1)
                 const uint32_t hb = smem_u32(hbf) + g_ * hpitch + 8 * t4 + (g.stacked ? ck.t * g.rs * 2 : 0);
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
-                    if (ks < npe) {
-                        const uint2 lo2 = lds64(hb + ks * 32);
-                        const uint2 hi2 = lds64(hb + 8 * hpitch + ks * 32);
-                        hf[ks][0] = lo2.x;
-                        hf[ks][1] = hi2.x;
-                        hf[ks][2] = lo2.y;
-                        hf[ks][3] = hi2.y;
+                    if (p.b_rank_major) {
+                        // natural K order (ldmatrix.trans gives B in it):
+                        // slots 2t, 2t + 1 and 2t + 8, 2t + 9
+                        const uint32_t hn = hb - 8 * t4 + 4 * t4 + ks * 32;
+                        if (ks < npe) {
+                            hf[ks][0] = lds32(hn);
+                            hf[ks][1] = lds32(hn + 8 * hpitch);
+                            hf[ks][2] = lds32(hn + 16);
+                            hf[ks][3] = lds32(hn + 8 * hpitch + 16);
+                        }
+                        const int kk = ks * 16 + 2 * t4;
+                        bm0[ks] = (kk + 1 < r ? 0xFFFF0000u : 0u) | (kk < r ? 0x0000FFFFu : 0u);
+                        bm1[ks] = (kk + 9 < r ? 0xFFFF0000u : 0u) | (kk + 8 < r ? 0x0000FFFFu : 0u);
+                    } else {
+                        if (ks < npe) {
+                            const uint2 lo2 = lds64(hb + ks * 32);
+                            const uint2 hi2 = lds64(hb + 8 * hpitch + ks * 32);
+                            hf[ks][0] = lo2.x;
+                            hf[ks][1] = hi2.x;
+                            hf[ks][2] = lo2.y;
+                            hf[ks][3] = hi2.y;
+                        }
+                        const int kk = ks * 16 + 4 * t4;
+                        bm0[ks] = (kk + 1 < r ? 0xFFFF0000u : 0u) | (kk < r ? 0x0000FFFFu : 0u);
+                        bm1[ks] = (kk + 3 < r ? 0xFFFF0000u : 0u) | (kk + 2 < r ? 0x0000FFFFu : 0u);
                     }
-                    const int kk = ks * 16 + 4 * t4;
-                    bm0[ks] = (kk + 1 < r ? 0xFFFF0000u : 0u) | (kk < r ? 0x0000FFFFu : 0u);
-                    bm1[ks] = (kk + 3 < r ? 0xFFFF0000u : 0u) | (kk + 2 < r ? 0x0000FFFFu : 0u);
                 }
             }
             const int nnt = (ck.ce - ck.cb) >> 3;
@@ -795,22 +836,40 @@ __global__ void __launch_bounds__(kStThreads, 1)
             // 8 (t4 % 2) .. + 8: ranks 16 ks + 4 t4 ..; the eight rows of a
             // fragment fall in distinct bank groups
             const int wi = r <= 16 ? 0 : (r <= 32 ? 1 : 2);
-            const uint32_t rsh = 5u + (uint32_t)wi;  // log2 bytes per B row
-            const int swz = wi == 2 ? g_ : (wi == 1 ? (g_ >> 1) & 3 : 0);
+            uint32_t rsh, sBa, lsw = 0;
             uint32_t boff[KS];
+            if (p.b_rank_major) {
+                // atoms of 64 columns x (16 << wi) rank rows of 128 bytes
+                const uint32_t l = (uint32_t)(lane & 15);
+                rsh = 11u + (uint32_t)wi;  // log2 bytes per atom
+                sBa = smem_u32(sb) + g.offB + l * 128u;
+                lsw = l & 7u;
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) boff[ks] = ((((2 * ks + (t4 >> 1)) ^ swz) << 4) + (t4 & 1) * 8);
-            const uint32_t sBa = smem_u32(sb) + g.offB + ((uint32_t)g_ << rsh);
+                for (int ks = 0; ks < KS; ++ks) boff[ks] = (uint32_t)ks * 16u * 128u;
+            } else {
+                rsh = 5u + (uint32_t)wi;  // log2 bytes per B row
+                const int swz = wi == 2 ? g_ : (wi == 1 ? (g_ >> 1) & 3 : 0);
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) boff[ks] = ((((2 * ks + (t4 >> 1)) ^ swz) << 4) + (t4 & 1) * 8);
+                sBa = smem_u32(sb) + g.offB + ((uint32_t)g_ << rsh);
+            }
             const uint32_t yr0 = smem_u32(sb) + g_ * g.ypitch + 4 * t4;  // row g_, column 2 t4
             const uint32_t yr1 = yr0 + 8 * g.ypitch;                     // row g_ + 8
             const bool row0 = g_ < R, row1 = g_ + 8 < R;
             // warp w takes the 8-column tiles w, w + 16, ...: two at a time
             // (in flight together) while two remain, then one
             int nt = warp;
-            for (; nt + kSmWarps < nnt; nt += 2 * kSmWarps)
-                expand_tiles<KS, 2>(nt, npe, sBa, boff, rsh, yr0, yr1, row0, row1, hf, bm0, bm1);
-            for (; nt < nnt; nt += kSmWarps)
-                expand_tiles<KS, 1>(nt, npe, sBa, boff, rsh, yr0, yr1, row0, row1, hf, bm0, bm1);
+            if (p.b_rank_major) {
+                for (; nt + kSmWarps < nnt; nt += 2 * kSmWarps)
+                    expand_tiles<KS, 2, true>(nt, npe, sBa, boff, rsh, yr0, yr1, row0, row1, hf, bm0, bm1, lsw);
+                for (; nt < nnt; nt += kSmWarps)
+                    expand_tiles<KS, 1, true>(nt, npe, sBa, boff, rsh, yr0, yr1, row0, row1, hf, bm0, bm1, lsw);
+            } else {
+                for (; nt + kSmWarps < nnt; nt += 2 * kSmWarps)
+                    expand_tiles<KS, 2, false>(nt, npe, sBa, boff, rsh, yr0, yr1, row0, row1, hf, bm0, bm1, lsw);
+                for (; nt < nnt; nt += kSmWarps)
+                    expand_tiles<KS, 1, false>(nt, npe, sBa, boff, rsh, yr0, yr1, row0, row1, hf, bm0, bm1, lsw);
+            }
             fence_proxy_async_cta();  // the y + delta writes come before the producer's next copies
             consumers_sync();
             // the rows leave by 16-byte stores: warp w takes row w / hv and
@@ -1052,10 +1111,13 @@ bool encode_3d(CUtensorMap *out, const void *base, uint64_t d0, uint64_t d1, uin
     const cuuint64_t dims[3] = {d0, d1, d2};
     const cuuint64_t strides[2] = {s1, s2};
     const cuuint32_t box[3] = {b0, b1, 1}, elem[3] = {1, 1, 1};
+    // No L2 promotion for boxes of narrow rows (a few ranks of a padded B
+    // row): promotion would fetch the padding around every row.
+    const CUtensorMapL2promotion promo = b0 * 2 >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_NONE;
     if (fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, elem,
            CU_TENSOR_MAP_INTERLEAVE_NONE,
            swz == 2 ? CU_TENSOR_MAP_SWIZZLE_128B : (swz == 1 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE),
-           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+           promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return false;
     const int i = cache.n < 16 ? cache.n++ : (cache.next++ & 15);
     cache.key[i] = k;
@@ -1078,10 +1140,15 @@ bool small_maps(const DeltaArgs &p, SmMaps &m) {
     }
     for (int t = 0; t < p.n_slices; ++t) {
         const SliceDesc &sl = p.slices[t];
-        for (int wi = 0; wi < 3 && (16 << wi) <= p.r_max; ++wi)
-            if (!encode_3d(&m.b[t][wi], sl.B, (uint64_t)p.r_max, (uint64_t)sl.d_out, (uint64_t)p.n_adapters,
-                           (uint64_t)sl.stride_n * 2, (uint64_t)sl.stride_adapter * 2, 16u << wi, 128, wi))
-                return false;
+        for (int wi = 0; wi < 3 && (16 << wi) <= p.r_max; ++wi) {
+            const bool ok =
+                p.b_rank_major
+                    ? encode_3d(&m.b[t][wi], sl.B, (uint64_t)sl.d_out, (uint64_t)p.r_max, (uint64_t)p.n_adapters,
+                                (uint64_t)sl.stride_r * 2, (uint64_t)sl.stride_adapter * 2, 64, 16u << wi, 2)
+                    : encode_3d(&m.b[t][wi], sl.B, (uint64_t)p.r_max, (uint64_t)sl.d_out, (uint64_t)p.n_adapters,
+                                (uint64_t)sl.stride_n * 2, (uint64_t)sl.stride_adapter * 2, 16u << wi, 128, wi);
+            if (!ok) return false;
+        }
     }
     return true;
 }

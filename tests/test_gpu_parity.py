@@ -496,3 +496,37 @@ def test_per_slice_a(B, ci):
     assert rel_err(yg, ref, w.y.astype(np.float64), act) <= TOL["bf16"]
     assert np.array_equal(yg[~act], w.y[~act].astype(np.float64))
     assert batch.counts()["device_error"] == 0
+
+
+# ----------------------------------------- rank-major B pools [n][r][d_out]
+
+RANK_MAJOR_CASES = [
+    dict(M=512, d_in=4096, d_outs=[14336], n_pool=100, r_max=64, ranks=[8, 16, 32, 64], skip_frac=0.25,
+         per_adapter_scale=True),
+    dict(M=300, d_in=1024, d_outs=[1024, 256, 256], n_pool=30, r_max=32, ranks=[8, 24, 32], run_len=12),
+    dict(M=100, d_in=512, d_outs=[520], n_pool=8, r_max=16, ranks=[3, 16]),
+]
+
+
+@pytest.mark.parametrize("ci", range(len(RANK_MAJOR_CASES)))
+def test_rank_major_b(B, ci):
+    w = wl.random_batch(seed=990 + ci, dtype="bf16", pad_value=float("nan"), **RANK_MAJOR_CASES[ci])
+    d = to_dev(w)
+    Bt = [b.transpose(1, 2).contiguous() for b in d["B"]]  # (n, r_max, d_out)
+    batch = B.lora_prepare_batch(d["ids"], w.n_adapters, 0)
+    y = d["y"].clone()
+    B.lora_delta(batch, d["x"], d["A"], Bt, y, scale=w.scale, adapter_scale=d["adapter_scale"],
+                 ranks=d["ranks"], b_rank_major=True)
+    assert B.lora_last_kernels() == B.KERNEL_STREAM
+    torch.cuda.synchronize()
+    _assert_delta(w, y.float().cpu().numpy().astype(np.float64))
+
+
+def test_rank_major_b_unsupported_elsewhere(B):
+    w = wl.random_batch(seed=995, M=3000, d_in=256, d_outs=[128], n_pool=8, r_max=16, dtype="bf16")
+    d = to_dev(w)
+    batch = B.lora_prepare_batch(d["ids"], w.n_adapters, 0)
+    with pytest.raises(B.LoraError) as e:
+        B.lora_delta(batch, d["x"], d["A"], [b.transpose(1, 2).contiguous() for b in d["B"]], d["y"],
+                     b_rank_major=True)
+    assert e.value.status == B.LORA_ERR_UNSUPPORTED
