@@ -637,7 +637,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     clocks = ClockSampler(vis.split(",")[local_rank].strip() if vis else str(local_rank))
-    m = measure(b, args.workload, K, W, world, dev, args.graph_steps, clocks=clocks)
+    m = measure(b, args.workload + ("+rank_major" if b.rank_major else ""), K, W, world, dev, args.graph_steps,
+                clocks=clocks)
     e2e = e2e_measure(b, args.e2e_steps)
     incremental = None
     if args.path == 0 and w.M <= 2048 and world == 1:
@@ -653,9 +654,14 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             if name == args.workload:
                 continue
             wo = fac(replica_seed(rank))
-            bo = Bench(wo, args, dev, stream, 0)
-            mo = measure(bo, name, args.extra_steps, W, world, dev, args.graph_steps, kernel_events=False)
+            # the padded mixed-rank pools in the rank-major layout, which reads
+            # only each adapter's rank rows
+            rm = name.startswith("mixed_rank")
+            bo = Bench(wo, args, dev, stream, 0, rank_major=rm)
+            mo = measure(bo, name + ("+rank_major" if rm else ""), args.extra_steps, W, world, dev,
+                         args.graph_steps, kernel_events=False)
             others[name] = summary(mo)
+            others[name]["b_layout"] = "rank_major" if rm else "rank_contiguous"
             del bo
             torch.cuda.empty_cache()
 
