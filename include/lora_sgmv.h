@@ -285,9 +285,9 @@ lora_status_t lora_prepare_batch_ordered(const int32_t *ids, int32_t M, int32_t 
  *
  * Arguments and result are those of lora_prepare_batch, without workspace
  * and workspace_bytes.  The batch needs lora_workspace_size(M, n_adapters,
- * chunk_size) <= LORA_STATIC_WORKSPACE_BYTES (4 MiB: about 4 bytes per
+ * chunk_size) <= LORA_STATIC_WORKSPACE_BYTES (4 MiB: about 8 bytes per
  * row plus a fixed part that grows with n_adapters, so for example up to
- * about 710000 rows with 4096 adapters unchunked, 420000 with 64-row
+ * about 355000 rows with 4096 adapters unchunked, 264000 with 64-row
  * chunks); a larger batch returns
  * LORA_ERR_WORKSPACE and launches nothing.  The call allocates no memory:
  * no cudaMalloc, no cudaFree, no allocating library routine.
