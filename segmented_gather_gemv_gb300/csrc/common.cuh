@@ -125,9 +125,6 @@ constexpr uint32_t kBatchMagic = 0x4C6F5241u;  // "LoRA"
 // (measured crossover on GB300: the CUDA-core kernel is ahead for groups of
 // up to 24 rows, the tensor-core kernel from 32).
 constexpr int kDefaultTcMinRows = 32;
-// Batches of at most this many rows start the CUDA-core kernel before the
-// tensor-core kernel (see the dispatch in api.cu).
-constexpr int kCcFirstMaxRows = 256;
 // Batches of at most this many rows run whole on the single-pass small-batch
 // kernel under LORA_PATH_AUTO; larger ones that the streaming kernel takes
 // run on it (see the dispatch in api.cu).
@@ -222,6 +219,11 @@ __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+// Brings a tensor map (a kernel parameter) into the copy unit's descriptor
+// cache ahead of its first copy.
+__device__ __forceinline__ void prefetch_tensormap(const void *map) {
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
 
 // mbarrier helpers (shared::cta barriers, transaction-count based).
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
@@ -377,14 +379,14 @@ struct DeltaArgs {
     const int32_t *ids;      // the batch's ids (the small-batch kernel groups rows from them)
     const int32_t *sorted;   // sorted_token_ids
     const SegDesc *desc;     // all segment descriptors (len 0 past the last)
-    const int4 *recs;        // records {start, len, adapter, s} (tensor-core list)
+    // small-segment list {start, len, adapter, s} (counts[LORA_COUNT_SMALL_SEGS]
+    // of them): with it, the CUDA-core kernel walks these segments only
+    const int4 *small_list;
     const int32_t *tc_indptr;
     int32_t *counts;
-    int32_t count_index;     // which counter holds the number of records in recs
     int32_t max_list;        // host-side capacity of desc / recs
     int32_t min_len, max_len;  // the CUDA-core kernel takes segments with min_len <= len < max_len
     int32_t split_tc;          // 1: segments >= max_len with a tensor-core rank go to the tensor-core kernel
-    int32_t after_tc;          // 1: launched right after the tensor-core kernel, which waited on prepare
     int32_t after_cc;          // 1: tensor-core kernel launched right after the CUDA-core kernel, which waited on prepare
     int32_t trigger_after_wait;  // small-batch kernel: trigger the next grid only after its own wait
     int32_t stacked;             // streaming kernel: per-slice A pools, their rank blocks stacked in one shrink

@@ -153,12 +153,7 @@ __global__ void __launch_bounds__(kCcThreads, 1)
     const uint32_t cid = cluster_id_x(), ncl = nclusters_x();
     const int RT = g.RT, HP = g.HP, SB = g.stage_bytes;
 
-    // Launched right after the tensor-core kernel, which triggers only after
-    // its own wait: the batch metadata is final and the two kernels write
-    // disjoint rows, so this grid works at once and waits for its
-    // predecessor only before it exits (its completion then implies the
-    // predecessor's).  Otherwise it waits first.
-    if (!p.after_tc) griddep_wait();
+    griddep_wait();
     griddep_launch_dependents();
 
     const int kv_total = p.d_in / V;
@@ -195,7 +190,12 @@ __global__ void __launch_bounds__(kCcThreads, 1)
     const bool may_plan = p.ranks != nullptr && p.counts != nullptr && p.n_adapters <= kCcThreads;
     int4 pd = make_int4(0, 0, 0, 0);  // this thread's descriptor head {start, len, adapter, flags}
     int32_t *p_rank = reinterpret_cast<int32_t *>(ring);  // scratch in the (still unused) ring
-    if (tid < 32) desc_s[tid] = reinterpret_cast<const int32_t *>(p.desc + cid)[tid];  // round-robin's first
+    // With a small-segment list (every adapter at the pool's rank, one the
+    // tensor cores take) the segments of this kernel are exactly that list:
+    // the round robin walks it instead of every descriptor.
+    const bool by_list = p.split_tc && p.small_list != nullptr;
+    const int n_list = by_list ? min(__ldcg(p.counts + LORA_COUNT_SMALL_SEGS), p.max_list) : 0;
+    if (tid < 32 && !by_list) desc_s[tid] = reinterpret_cast<const int32_t *>(p.desc + cid)[tid];  // round-robin's first
     if (may_plan) {
         if (tid < min(p.max_list, kPlanMaxSegs)) pd = *reinterpret_cast<const int4 *>(p.desc + tid);
         if (tid < p.n_adapters) p_rank[tid] = p.ranks[tid];
@@ -286,11 +286,16 @@ __global__ void __launch_bounds__(kCcThreads, 1)
             te = tb + 1;
         } else {
             li = (int)cid + e * (int)ncl;
-            if (li >= p.max_list) break;
+            if (by_list) {
+                if (li >= n_list) break;
+                li = __ldcg(&p.small_list[li].w);
+            } else if (li >= p.max_list) {
+                break;
+            }
             tb = 0;
             te = 0x7fffffff;
         }
-        if (n_plan >= 0 || e > 0) {
+        if (n_plan >= 0 || e > 0 || by_list) {
             __syncthreads();  // the previous segment is done with desc_s / rows_s
             if (tid < 32) desc_s[tid] = reinterpret_cast<const int32_t *>(p.desc + li)[tid];
             __syncthreads();
@@ -725,7 +730,6 @@ __global__ void __launch_bounds__(kCcThreads, 1)
             gjob += (uint32_t)total;
         }
     }
-    if (p.after_tc) griddep_wait();
 }
 
 // ---------------------------------------------------------------------------

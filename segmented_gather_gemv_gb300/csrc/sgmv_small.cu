@@ -26,20 +26,23 @@
 //   - the N slice q of d_out for the expand (B rows and y rows of that slice),
 // so every byte of x, A, B and y of a tile is read once.
 //
-// Data movement.  A rows and the gathered x and y rows arrive by 16-byte
-// cp.async from every thread (a few per thread: the copy unit takes them
-// faster than one bulk copy per 2 KB row piece); the CTA's B rows are one
-// contiguous block per output slice and arrive by one bulk copy each.  The
-// weights (A and B) depend only on the adapter, so they are requested before
-// the kernel waits on the previous grid in the stream (programmatic
-// dependent launch); x and y are requested after that wait.  y + delta
-// leaves by 16-byte stores.
+// Data movement.  A rows and the gathered y rows arrive by 16-byte cp.async
+// from every thread (a few per thread: the copy unit takes them faster than
+// one bulk copy per 2 KB row piece); the CTA's B rows are one contiguous
+// block per output slice and arrive by one bulk copy each.  x never enters
+// shared memory: each lane loads its shrink fragments straight into
+// registers (8 bytes per row and K step).  The weights (A and B) depend only
+// on the adapter, so they are requested before the kernel waits on the
+// previous grid in the stream (programmatic dependent launch); x and y are
+// requested after that wait.  y + delta leaves by 16-byte stores.  One
+// shared-memory region serves three purposes in turn: the hash table of the
+// grouping, a tile's A rows, and the warps' partial h.
 //
 // Compute.  Shrink: warp-level bf16 tensor-core tiles (16 x 8 x 16, fp32
-// accumulators in registers; operands by ldmatrix from rows padded by 16
-// bytes, so the eight rows of a fragment fall in eight bank groups).  The
-// warps split the K steps (and, for ranks above 16, the 16-column rank
-// blocks); their partials are summed in warp order.  The CTA's partial h is
+// accumulators in registers; A fragments by 8-byte loads from rows whose
+// pitch puts the rows of a half-warp's loads in distinct banks).  The warps
+// split the K steps and each takes every 16-column rank block of its steps;
+// their partials are summed in warp order.  The CTA's partial h is
 // pushed to every CTA of the cluster (st.async, completing on the receiver's
 // mbarrier: no cluster barrier per tile), and each CTA sums the CL partials
 // in rank order, so every CTA holds the same h.  h is scaled once, masked to
@@ -63,6 +66,7 @@ constexpr int kSmWarps = kSmThreads / 32;
 constexpr int kSmMaxRows = 1024;  // rows a batch may have for this kernel (two per thread)
 constexpr int kSmRT = 16;         // rows per tile: one 16-row MMA tile
 constexpr int kSmNtBatch = 4;     // 8-column tiles a warp keeps in flight in the expand
+constexpr int kSmXB = 8;          // K steps of x a warp holds in registers at once
 
 // The CTA's columns [n0, n1) by output slice t: columns [cb, ce) (ce <= cb:
 // the slice has none of them), y column = column + go, B rows at byte off of
@@ -79,14 +83,13 @@ struct SmGeom {
     int CL;              // CTAs per cluster
     int KC;              // shrink columns per CTA
     int NCmax;           // expand columns per CTA (at most)
-    int xpitch, ypitch;  // bytes per shared row of x / A and of y
+    int apitch, ypitch;  // bytes per shared row of A and of y
     int HS;              // hash slots (power of two, >= 2 M)
     int tcap;            // tile records per CTA
     uint32_t ncl_magic;  // ceil(2^32 / clusters): x / clusters = umulhi(x, magic) for x < 2^16
     int ncol0[kSmMaxCluster + 1];  // first expand column of cluster rank q (multiples of 8)
     PieceTab pt[kSmMaxCluster];    // the slices of each cluster rank's columns
-    int off_bars, off_key, off_first, off_cnt, off_scan, off_tl, off_rows, off_red, off_recv, off_hbf, off_A, off_x,
-        off_y, off_B, total;
+    int off_bars, off_scan, off_tl, off_rows, off_recv, off_hbf, off_A, off_y, off_B, total;
 };
 
 // One tile of this cluster: adapter, rank, first and last row (exclusive)
@@ -97,11 +100,6 @@ struct TileRec {
     int pad[3];
 };
 
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -157,9 +155,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
     return v;
 }
-__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[4], uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n" : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
-}
 __device__ __forceinline__ void sts32(uint32_t a, uint32_t v) {
     asm volatile("st.shared.u32 [%0], %1;\n" ::"r"(a), "r"(v) : "memory");
 }
@@ -186,21 +181,24 @@ template <int R16>
 __global__ void __launch_bounds__(kSmThreads, 1)
     sgmv_small_kernel(const __grid_constant__ DeltaArgs p, const __grid_constant__ SmGeom g) {
     constexpr int KS = R16 / 16;  // K steps of the expand (rank blocks of the shrink)
+    constexpr int NT = kSmThreads, NW = kSmWarps;
+    constexpr int RP = R16 + 4;   // floats per row of a warp's partial h
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bar_b = reinterpret_cast<uint64_t *>(smem + g.off_bars);  // B block landed
     uint64_t *recv_bar = bar_b + 1;                                      // [2] partial h received
-    int32_t *key = reinterpret_cast<int32_t *>(smem + g.off_key);
-    int32_t *first = reinterpret_cast<int32_t *>(smem + g.off_first);
-    int32_t *cnt = reinterpret_cast<int32_t *>(smem + g.off_cnt);
-    int32_t *wsum = reinterpret_cast<int32_t *>(smem + g.off_scan);  // [kSmWarps]
-    int32_t *wsum2 = wsum + 32;                                         // [kSmWarps]
+    // Region A holds the hash table while the rows are grouped, the A rows of
+    // a tile during its shrink, and then the warps' partial h.
+    int32_t *key = reinterpret_cast<int32_t *>(smem + g.off_A);
+    int32_t *first = key + g.HS;
+    int32_t *cnt = first + g.HS;
+    int32_t *wsum = reinterpret_cast<int32_t *>(smem + g.off_scan);  // [NW]
+    int32_t *wsum2 = wsum + 32;                                         // [NW]
     TileRec *tl = reinterpret_cast<TileRec *>(smem + g.off_tl);        // [tcap]
     int32_t *rows_s = reinterpret_cast<int32_t *>(smem + g.off_rows);  // [kSmRT]
     const PieceTab *pt = &g.pt[cluster_ctarank()];  // launch parameters
-    float *red = reinterpret_cast<float *>(smem + g.off_red);          // [warps][16][20]
     float *recv = reinterpret_cast<float *>(smem + g.off_recv);        // [2][CL][16][R16]
     unsigned char *hbf = smem + g.off_hbf;                              // [16][R16 + 8] bf16
-    unsigned char *sA = smem + g.off_A, *sX = smem + g.off_x, *sY = smem + g.off_y, *sB = smem + g.off_B;
+    unsigned char *sA = smem + g.off_A, *sY = smem + g.off_y, *sB = smem + g.off_B;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int CL = g.CL;
@@ -220,7 +218,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     // scales, and an empty hash table.  Everything read before the wait (ids,
     // ranks, scales and later the weights) is fixed before the previous grid
     // in the stream started (header contract).
-    const int RPT = M > kSmThreads ? 2 : 1;
+    const int RPT = M > NT ? 2 : 1;
     int idr[2], rkr[2];
     float scr[2];
 #pragma unroll
@@ -234,7 +232,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         mbar_init(&recv_bar[1], 1);
         fence_mbar_init();
     }
-    for (int s = tid; s < HS; s += kSmThreads) {
+    for (int s = tid; s < HS; s += NT) {
         key[s] = -1;
         first[s] = INT_MAX;
         cnt[s] = 0;
@@ -293,15 +291,15 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     int base, total;
     {
         // warp totals, scanned across the warps by shuffles
-        const int wv = lane < kSmWarps ? wsum[lane] : 0;
+        const int wv = lane < NW ? wsum[lane] : 0;
         int ws = wv;
 #pragma unroll
-        for (int o = 1; o < kSmWarps; o <<= 1) {
+        for (int o = 1; o < NW; o <<= 1) {
             const int t = __shfl_up_sync(0xffffffffu, ws, o);
             if (lane >= o) ws += t;
         }
         base = __shfl_sync(0xffffffffu, ws - wv, warp);
-        total = __shfl_sync(0xffffffffu, ws, kSmWarps - 1);
+        total = __shfl_sync(0xffffffffu, ws, NW - 1);
     }
     const int T = total >> 16;  // tiles of the batch
     {
@@ -330,6 +328,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
             }
         }
     }
+    // (the barrier also ends every read of the hash table: region A is free)
     const int bad_rank = __syncthreads_or(bad);
     const int my_tiles =
         (int)cid < T ? min((int)__umulhi((uint32_t)(T - 1 - (int)cid), g.ncl_magic) + 1, g.tcap) : 0;
@@ -338,15 +337,17 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     const int n0 = g.ncol0[q], n1 = g.ncol0[q + 1];
     const int ncols = n1 - n0;
     const int kc8 = g.KC / 8;
+    const int nks = g.KC >> 4;  // 16-column K steps of the shrink
+    const int g_ = lane >> 2, t4 = lane & 3;
 
     // The weights of a tile: A rows [0, r) of the K slice (cp.async, one
-    // group: warp w takes rows w, w + 16, ..., its lanes the 16-byte pieces),
+    // group: warp w takes rows w, w + NW, ..., its lanes the 16-byte pieces),
     // B rows of the N slice (one bulk copy per output slice, on bar_b).
     auto request_weights = [&](const TileRec &ti) {
         const __nv_bfloat16 *Aa = static_cast<const __nv_bfloat16 *>(p.A) + (int64_t)ti.a * p.a_stride_adapter + k0;
-        for (int jr = warp; jr < ti.r; jr += kSmWarps) {
+        for (int jr = warp; jr < ti.r; jr += NW) {
             const __nv_bfloat16 *src = Aa + (int64_t)jr * p.a_stride_r;
-            unsigned char *dst = sA + jr * g.xpitch;
+            unsigned char *dst = sA + jr * g.apitch;
             for (int cc = lane; cc < kc8; cc += 32) cp_async16_full(dst + cc * 16, src + cc * 8);
         }
         cp_async_commit();
@@ -374,10 +375,10 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         __syncthreads();
         int b;
         {
-            const int wv = lane < kSmWarps ? wsum2[lane] : 0;
+            const int wv = lane < NW ? wsum2[lane] : 0;
             int ws = wv;
 #pragma unroll
-            for (int o = 1; o < kSmWarps; o <<= 1) {
+            for (int o = 1; o < NW; o <<= 1) {
                 const int t = __shfl_up_sync(0xffffffffu, ws, o);
                 if (lane >= o) ws += t;
             }
@@ -390,20 +391,12 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         if (RPT > 1 && idr[1] == a && p1 >= lo && p1 < hi) rows_s[p1 - lo] = tid * RPT + 1;
         __syncthreads();
     };
-    // x rows (K slice) and y rows (N slice) of the tile, one cp.async group
-    // each: warp w takes row w (R <= 16 rows), its lanes the 16-byte pieces.
-    auto request_acts = [&](int R) {
-        if (warp < R) {
-            const int row = rows_s[warp];
-            const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(p.x) + (int64_t)row * p.ldx + k0;
-            unsigned char *dst = sX + warp * g.xpitch;
-            for (int cc = lane; cc < kc8; cc += 32) cp_async16_full(dst + cc * 16, src + cc * 8);
-        }
-        cp_async_commit();
-        if (warp < R) {
-            const int row = rows_s[warp];
-            const __nv_bfloat16 *yrow = static_cast<const __nv_bfloat16 *>(p.y) + (int64_t)row * p.ldy;
-            unsigned char *dst = sY + warp * g.ypitch;
+    // y rows (N slice) of the tile, one cp.async group: warp w takes rows w,
+    // w + NW, ..., its lanes the 16-byte pieces.
+    auto request_y = [&](int R) {
+        for (int row = warp; row < R; row += NW) {
+            const __nv_bfloat16 *yrow = static_cast<const __nv_bfloat16 *>(p.y) + (int64_t)rows_s[row] * p.ldy;
+            unsigned char *dst = sY + row * g.ypitch;
             for (int t = 0; t < p.n_slices; ++t) {
                 const int ce = pt->ce[t], go = pt->go[t];
                 for (int col = pt->cb[t] + lane * 8; col < ce; col += 256)
@@ -411,6 +404,27 @@ __global__ void __launch_bounds__(kSmThreads, 1)
             }
         }
         cp_async_commit();
+    };
+    // x goes straight from global memory into the shrink's B fragments.  The
+    // MMA's K slots are permuted inside each 16-column step, the same way for
+    // A and x: slots 2t, 2t+1, 2t+8, 2t+9 of lane t take columns 4t .. 4t+3,
+    // so a lane's x fragment of one row and step is 8 contiguous bytes (and a
+    // warp's load covers 8 rows x 32 bytes).  Lane (g, t) takes rows g and
+    // g + 8 of the tile; warp w takes K steps w, w + NW, ...
+    const __nv_bfloat16 *xbase = static_cast<const __nv_bfloat16 *>(p.x) + k0 + 4 * t4;
+    const __nv_bfloat16 *x0 = nullptr, *x1 = nullptr;
+    uint2 xa[kSmXB], xb[kSmXB];
+    auto x_rows = [&](int R) {
+        x0 = g_ < R ? xbase + (int64_t)rows_s[g_] * p.ldx : nullptr;
+        x1 = g_ + 8 < R ? xbase + (int64_t)rows_s[g_ + 8] * p.ldx : nullptr;
+    };
+    auto load_x = [&](int kb) {
+#pragma unroll
+        for (int j = 0; j < kSmXB; ++j) {
+            const int ks = kb + j * NW;
+            xa[j] = (x0 && ks < nks) ? __ldcg(reinterpret_cast<const uint2 *>(x0 + ks * 16)) : make_uint2(0u, 0u);
+            xb[j] = (x1 && ks < nks) ? __ldcg(reinterpret_cast<const uint2 *>(x1 + ks * 16)) : make_uint2(0u, 0u);
+        }
     };
 
     TileRec ti{};
@@ -421,18 +435,23 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     }
     griddep_wait();
     if (bad_rank && blockIdx.x == 0 && tid == 0) raise_deverr(p.counts, LORA_DEVERR_RANK);
-    if (my_tiles > 0) request_acts(ti.hi - ti.lo);
+    if (my_tiles > 0) {
+        x_rows(ti.hi - ti.lo);
+        load_x(warp);
+        request_y(ti.hi - ti.lo);
+    }
     cluster_wait_acquire();
 
     bool ok = true;
-    const int g_ = lane >> 2, t4 = lane & 3;
     for (int e = 0; e < my_tiles; ++e) {
         if (e > 0) {
             // the previous tile is done with every buffer
             ti = tl[e];
             request_weights(ti);
             find_rows(ti.a, ti.lo, ti.hi);
-            request_acts(ti.hi - ti.lo);
+            x_rows(ti.hi - ti.lo);
+            load_x(warp);
+            request_y(ti.hi - ti.lo);
         }
         const int r = ti.r, R = ti.hi - ti.lo;
         const int r16a = (r + 15) & ~15;
@@ -442,93 +461,75 @@ __global__ void __launch_bounds__(kSmThreads, 1)
 
         // ---- shrink: h^T = A . x^T on warp-level tensor-core tiles (M = the
         // 16 ranks of a rank block, N = 8 rows, K = 16 columns of d_in): a
-        // tile of at most 8 rows takes one product per K step.  Warp w takes
-        // rank block w % np and the K steps w / np, w / np + kw, ...
-        cp_async_wait<1>();  // A and x of this thread
+        // tile of at most 8 rows takes one product per K step and rank block.
+        cp_async_wait<1>();  // A of this thread
         __syncthreads();
-        const int kw = kSmWarps / np;
-        const int my_pb = warp % np, my_kq = warp / np;
         const bool two = R > 8;  // a second 8-row tile
-        if (my_kq < kw) {
-            float acc[2][2][4];  // [row tile][accumulator set][fragment]
+        float acc[KS][2][4];     // [rank block][row tile][fragment]
+#pragma unroll
+        for (int pb = 0; pb < KS; ++pb)
 #pragma unroll
             for (int u = 0; u < 2; ++u)
 #pragma unroll
-                for (int t = 0; t < 2; ++t)
+                for (int i = 0; i < 4; ++i) acc[pb][u][i] = 0.f;
+        // A fragment of rank g (+ 8) of block pb: the 8 bytes of the lane's
+        // four permuted columns
+        const uint32_t ab = smem_u32(sA) + g_ * g.apitch + 8 * t4;
+        for (int kb = warp; kb < nks; kb += NW * kSmXB) {
+            if (kb != warp) load_x(kb);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) acc[u][t][i] = 0.f;
-            const int nks = g.KC >> 4;
-            // A operand: ranks of the block (lane & 15), K half lane >> 4;
-            // B operand: x rows (lane & 7) (+ 8 for lanes 16-31), K half (lane >> 3) & 1
-            const uint32_t ab = smem_u32(sA) + (my_pb * 16 + (lane & 15)) * g.xpitch + (lane >> 4) * 16;
-            const uint32_t xb = smem_u32(sX) + ((lane & 7) + ((lane >> 4) << 3)) * g.xpitch + ((lane >> 3) & 1) * 16;
-            int u = 0;
-#pragma unroll 4
-            for (int ks = my_kq; ks < nks; ks += kw) {
-                uint32_t af[4], xf[4];
-                ldsm_x4(af, ab + ks * 32);
-                if (two) ldsm_x4(xf, xb + ks * 32);
-                else ldsm_x2(xf, xb + ks * 32);
-                if (u == 0) {
-                    mma_bf16_16816(acc[0][0], af, xf[0], xf[1]);
-                    if (two) mma_bf16_16816(acc[1][0], af, xf[2], xf[3]);
-                } else {
-                    mma_bf16_16816(acc[0][1], af, xf[0], xf[1]);
-                    if (two) mma_bf16_16816(acc[1][1], af, xf[2], xf[3]);
+            for (int j = 0; j < kSmXB; ++j) {
+                const int ks = kb + j * NW;
+                if (ks < nks) {
+#pragma unroll
+                    for (int pb = 0; pb < KS; ++pb) {
+                        if (pb < np) {
+                            const uint32_t a = ab + pb * 16 * g.apitch + ks * 32;
+                            const uint2 lo = lds64(a), hi = lds64(a + 8 * g.apitch);
+                            const uint32_t af[4] = {lo.x, hi.x, lo.y, hi.y};
+                            mma_bf16_16816(acc[pb][0], af, xa[j].x, xa[j].y);
+                            if (two) mma_bf16_16816(acc[pb][1], af, xb[j].x, xb[j].y);
+                        }
+                    }
                 }
-                u ^= 1;
             }
-            // warp partial -> red[warp][row][rank in block] (row pitch 20 floats:
-            // the fragment's rows 2t and 2t+1 fall in distinct banks)
-            const uint32_t rw = smem_u32(red) + (uint32_t)warp * (16 * 20 * 4);
+        }
+        __syncthreads();  // every warp is done with the A rows: the region takes the partials
+        // warp partial -> red[warp][row][rank] (row pitch R16 + 4 floats: the
+        // fragment's rows 2t and 2t+1 fall in distinct banks).  Rows of a
+        // missing second 8-row tile hold leftovers; h masks them.
+        {
+            const uint32_t rw = smem_u32(sA) + (uint32_t)warp * (16 * RP * 4);
 #pragma unroll
-            for (int rt = 0; rt < 2; ++rt) {
-                if (rt == 0 || two) {
-                    const uint32_t a0 = rw + ((rt * 8 + 2 * t4) * 20 + g_) * 4;
-                    sts32(a0, __float_as_uint(acc[rt][0][0] + acc[rt][1][0]));
-                    sts32(a0 + 20 * 4, __float_as_uint(acc[rt][0][1] + acc[rt][1][1]));
-                    sts32(a0 + 8 * 4, __float_as_uint(acc[rt][0][2] + acc[rt][1][2]));
-                    sts32(a0 + 28 * 4, __float_as_uint(acc[rt][0][3] + acc[rt][1][3]));
+            for (int pb = 0; pb < KS; ++pb) {
+#pragma unroll
+                for (int rt = 0; rt < 2; ++rt) {
+                    if (pb < np && (rt == 0 || two)) {
+                        const uint32_t a0 = rw + ((rt * 8 + 2 * t4) * RP + pb * 16 + g_) * 4;
+                        sts32(a0, __float_as_uint(acc[pb][rt][0]));
+                        sts32(a0 + RP * 4, __float_as_uint(acc[pb][rt][1]));
+                        sts32(a0 + 8 * 4, __float_as_uint(acc[pb][rt][2]));
+                        sts32(a0 + (RP + 8) * 4, __float_as_uint(acc[pb][rt][3]));
+                    }
                 }
             }
         }
         __syncthreads();
-        // CTA partial: the kw partials of each rank block summed in two
-        // levels (pairs kq, kq + 8 by all threads in place, then the eight
-        // sums in order), pushed to every CTA of the cluster: slot q of their
-        // receive buffer.  Rows of a missing second 8-row tile hold leftovers;
-        // h masks them.
+        // CTA partial: the NW warp partials summed in warp order, pushed to
+        // every CTA of the cluster: slot q of their receive buffer.
         const int nel4 = 4 * r16a;  // float4 entries of a 16 x r16a block
         const int rq = r16a / 4;    // float4 entries per row
         float *rv = recv + (size_t)buf * CL * 16 * R16;
-        const uint32_t redb = smem_u32(red);
-        if (kw > 8) {
-            // kw == 16 (np == 1): warp partials kq and kq + 8
-            const int e4 = tid & 63, part = tid >> 6;  // 64 float4 x 8 parts
-            const uint32_t a = redb + ((uint32_t)part * 320 + (e4 >> 2) * 20 + (e4 & 3) * 4) * 4;
-            const uint4 x4 = lds128(a), y4 = lds128(a + 8 * 320 * 4);
-            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(a),
-                         "f"(__uint_as_float(x4.x) + __uint_as_float(y4.x)),
-                         "f"(__uint_as_float(x4.y) + __uint_as_float(y4.y)),
-                         "f"(__uint_as_float(x4.z) + __uint_as_float(y4.z)),
-                         "f"(__uint_as_float(x4.w) + __uint_as_float(y4.w))
-                         : "memory");
-            __syncthreads();
-        }
         if (tid < nel4) {
             const int row = tid / rq, col = (tid - row * rq) * 4;
-            const int pb = col >> 4, cl = col & 15;
-            const int kn = kw > 8 ? 8 : kw;
-            uint4 pv[8];
-#pragma unroll
-            for (int kq = 0; kq < 8; ++kq)
-                pv[kq] = kq < kn ? lds128(redb + ((uint32_t)(kq * np + pb) * 320 + row * 20 + cl) * 4)
-                                 : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t a = smem_u32(sA) + (uint32_t)(row * RP + col) * 4;
             float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int kq = 0; kq < 8; ++kq)
-                add4(s4, make_float4(__uint_as_float(pv[kq].x), __uint_as_float(pv[kq].y), __uint_as_float(pv[kq].z),
-                                     __uint_as_float(pv[kq].w)));
+            for (int w = 0; w < NW; ++w) {
+                const uint4 pv = lds128(a + (uint32_t)w * (16 * RP * 4));
+                add4(s4, make_float4(__uint_as_float(pv.x), __uint_as_float(pv.y), __uint_as_float(pv.z),
+                                     __uint_as_float(pv.w)));
+            }
             const uint32_t la = smem_u32(rv + ((size_t)q * 16 + row) * R16 + col);
             const uint32_t lb = smem_u32(&recv_bar[buf]);
             for (int pr = 0; pr < CL; ++pr) st_async_f4(map_to_rank(la, pr), s4, map_to_rank(lb, pr));
@@ -554,7 +555,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
                 make_uint2(bf16x2_bits(h0, h1), bf16x2_bits(h2, h3));
         }
         cp_async_wait<0>();  // y of this thread
-        if (tid == kSmThreads - 1 && !mbar_wait(bar_b, (uint32_t)e & 1u)) ok = false;
+        if (tid == NT - 1 && !mbar_wait(bar_b, (uint32_t)e & 1u)) ok = false;
         __syncthreads();
 
         // ---- expand: warp w takes 8-column tiles w * 4 .. w * 4 + 3, then
@@ -590,7 +591,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         const uint32_t yr0 = smem_u32(sY) + g_ * g.ypitch + 4 * t4;  // row g_, column 2 t4
         const uint32_t yr1 = yr0 + 8 * g.ypitch;                     // row g_ + 8
         const bool row0 = g_ < R, row1 = g_ + 8 < R;
-        for (int nt0 = warp * kSmNtBatch; nt0 < nnt; nt0 += kSmWarps * kSmNtBatch) {
+        for (int nt0 = warp * kSmNtBatch; nt0 < nnt; nt0 += NW * kSmNtBatch) {
             // addresses of the four tiles' B rows (the slice that holds each)
             uint32_t ba[kSmNtBatch];
 #pragma unroll
@@ -646,12 +647,13 @@ __global__ void __launch_bounds__(kSmThreads, 1)
             }
         }
         __syncthreads();
-        // the rows leave by 16-byte stores: warp w takes row w / hv and the
-        // 8-column pieces w % hv, w % hv + hv, ... (hv = 2 when R <= 8)
+        // the rows leave by 16-byte stores: unit u = (row u / hv, 8-column
+        // pieces u % hv, u % hv + hv, ...) goes to warp u % NW (hv = 2 when
+        // the rows are at most half the warps)
         {
-            const int hv = R > 8 ? 1 : 2;
-            const int row = warp / hv, part = warp - row * hv;
-            if (row < R) {
+            const int hv = 2 * R <= NW ? 2 : 1;
+            for (int u = warp; u < R * hv; u += NW) {
+                const int row = u / hv, part = u - row * hv;
                 __nv_bfloat16 *yrow = static_cast<__nv_bfloat16 *>(p.y) + (int64_t)rows_s[row] * p.ldy;
                 const uint32_t src = smem_u32(sY) + row * g.ypitch;
                 for (int t = 0; t < p.n_slices; ++t) {
@@ -718,7 +720,10 @@ static bool small_geometry(const DeltaArgs &p, int R16, int cl, int ncl, SmGeom 
         }
     }
     g.ncl_magic = (uint32_t)((0x100000000ull + (uint64_t)ncl - 1) / (uint64_t)ncl);
-    g.xpitch = g.KC * 2 + 16;
+    // A row pitch: (pitch / 4) = 8 mod 32 words, so the 8-byte fragment
+    // reads of rows g = 0..3 by lanes t = 0..3 (one half-warp) fall in
+    // distinct banks; a multiple of 16 bytes for the 16-byte copies
+    g.apitch = g.KC * 2 + 4 * (((8 - g.KC / 2) % 32 + 32) % 32);
     g.ypitch = g.NCmax * 2 + 16;
     size_t o = 0;
     auto take = [&](size_t bytes) {
@@ -727,17 +732,14 @@ static bool small_geometry(const DeltaArgs &p, int R16, int cl, int ncl, SmGeom 
         return (int)at;
     };
     g.off_bars = take(8 * 4);
-    g.off_key = take((size_t)g.HS * 4);
-    g.off_first = take((size_t)g.HS * 4);
-    g.off_cnt = take((size_t)g.HS * 4);
     g.off_scan = take(64 * 4);
     g.off_tl = take((size_t)g.tcap * sizeof(TileRec));
     g.off_rows = take(kSmRT * 4);
-    g.off_red = take((size_t)kSmWarps * 16 * 20 * 4);
     g.off_recv = take((size_t)2 * cl * 16 * R16 * 4);
     g.off_hbf = take((size_t)16 * (R16 + 8) * 2);
-    g.off_A = take((size_t)R16 * g.xpitch);
-    g.off_x = take((size_t)kSmRT * g.xpitch);
+    // region A: the hash table (key, first, count), the A rows, the warps'
+    // partial h, one after the other
+    g.off_A = take(std::max({(size_t)R16 * g.apitch, (size_t)3 * g.HS * 4, (size_t)kSmWarps * 16 * (R16 + 4) * 4}));
     g.off_y = take((size_t)kSmRT * g.ypitch);
     // + 32 bytes: the expand's B fragment reads cover 16 rank columns and may
     // reach past a short last B row (those values are masked to zero)

@@ -331,6 +331,17 @@ __global__ void __launch_bounds__(kStThreads, 1)
     // batch metadata at its start: then this grid triggers only after its
     // wait on prepare.
     if (!p.trigger_after_wait) griddep_launch_dependents();
+    if (warp == kSmWarps) {
+        // the producer's tensor maps, one per lane: A per stacked slice, B
+        // per slice and box width
+        const CUtensorMap *mp = nullptr;
+        if (lane < (g.stacked ? p.n_slices : 1)) mp = &m.a[lane];
+        else if (lane >= 4 && lane < 4 + 3 * p.n_slices) {
+            const int t = (lane - 4) / 3, wi = (lane - 4) - 3 * t;
+            if ((16 << wi) <= p.r_max) mp = &m.b[t][wi];
+        }
+        if (mp) prefetch_tensormap(mp);
+    }
     // ids written by the grid before (an updated batch): read after the wait
     if (p.ids_after_wait) griddep_wait();
 

@@ -10,7 +10,7 @@
 // moved to a nearby boundary between adapters (prepare computes the shares
 // for this grid), so every CTA moves about the same amount of x and y
 // whatever the segment lengths.  The grid has one CTA per 64 batch rows, at
-// most one per SM.  A share is cut into tiles of up to 128 rows; a tile may
+// most one per SM, and leaves one SM free.  A share is cut into tiles of up to 128 rows; a tile may
 // span several segments (pieces, see Tile below), so a share never costs two
 // passes.
 //
@@ -424,6 +424,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+    if (warp == 0) {
+        // the tensor maps of the TMA copies, one per lane: x, y per slice, A
+        const CUtensorMap *mp = nullptr;
+        if (m.use && lane < 3) mp = lane == 0 ? &m.x64 : lane == 1 ? &m.x32 : &m.x8;
+        else if (m.use && lane < 3 + 3 * p.n_slices) {
+            const int t = (lane - 3) / 3, k = (lane - 3) - 3 * t;
+            mp = k == 0 ? &m.y64[t] : k == 1 ? &m.y32[t] : &m.y8[t];
+        } else if (m.use_ab && lane >= 16 && lane < 19 && (8 << (lane - 16)) <= m.a_box_max)
+            mp = lane == 16 ? &m.a8 : lane == 17 ? &m.a16 : &m.a32;
+        if (mp) prefetch_tensormap(mp);
+    }
     if (tid == 0) {
         for (int s = 0; s < kMaxNS; ++s) {
             // TMA path: the two issuers' expect_tx and the 64 helper threads;
