@@ -585,28 +585,88 @@ def measure(b: Bench, key: str, K: int, W: int, world: int, dev, graph_steps: in
 
 
 def e2e_measure(b: Bench, steps: int) -> dict:
-    """The public API from pinned host buffers, copies inside the region."""
+    """The public API from pinned host buffers, copies inside the timed region.
+
+    Every step copies its inputs in (x, y, ids), runs prepare + delta and
+    copies its result (y) out.  The steps run as a serving loop runs them:
+    captured in a CUDA graph, device buffer sets in rotation, the input copies
+    of later steps (x and ids on one stream, y on another) and the output copy
+    of the step before beside a step's kernels.  A buffer set is refilled only
+    after the output copy of its previous step has finished."""
     torch, w = b.torch, b.w
     x_h = torch.from_numpy(w.x).to(b.tdt).pin_memory()
     y_h = torch.from_numpy(w.y).to(b.tdt).pin_memory()
     ids_h = torch.from_numpy(w.ids).pin_memory()
     y_out = torch.empty_like(y_h).pin_memory()
-    s0 = b.sets[0]
-    with torch.cuda.stream(b.stream):
-        for i in range(3 + steps):
-            if i == 3:
-                b.stream.synchronize()
-                e_a = torch.cuda.Event(enable_timing=True)
-                e_b = torch.cuda.Event(enable_timing=True)
-                e_a.record(b.stream)
-            s0["x"].copy_(x_h, non_blocking=True)
-            s0["y"].copy_(y_h, non_blocking=True)
-            s0["ids"].copy_(ids_h, non_blocking=True)
-            b.step(s0)
-            y_out.copy_(s0["y"], non_blocking=True)
-        e_b.record(b.stream)
+    nb = min(3, len(b.sets))
+    comp = b.stream
+    s_x, s_y, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_x = [torch.cuda.Event() for _ in range(nb)]
+    ev_y = [torch.cuda.Event() for _ in range(nb)]
+    ev_c = [torch.cuda.Event() for _ in range(nb)]
+    ev_o = [torch.cuda.Event() for _ in range(nb)]
+    G = max(1, min(16, steps))
+    reps = max(1, (steps + G - 1) // G)
+
+    def one(i):
+        k = i % nb
+        s = b.sets[k]
+        with torch.cuda.stream(s_x):
+            if i >= nb:
+                s_x.wait_event(ev_o[k])
+            s["x"].copy_(x_h, non_blocking=True)
+            s["ids"].copy_(ids_h, non_blocking=True)
+            ev_x[k].record(s_x)
+        with torch.cuda.stream(s_y):
+            if i >= nb:
+                s_y.wait_event(ev_o[k])
+            s["y"].copy_(y_h, non_blocking=True)
+            ev_y[k].record(s_y)
+        comp.wait_event(ev_x[k])
+        comp.wait_event(ev_y[k])
+        b.step(s)
+        ev_c[k].record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_c[k])
+            y_out.copy_(s["y"], non_blocking=True)
+            ev_o[k].record(s_out)
+
+    # eager warm-up (also builds the batches' host state), then the graph
+    with torch.cuda.stream(comp):
+        for i in range(nb):
+            root = torch.cuda.Event()
+            root.record(comp)
+            for st in (s_x, s_y, s_out):
+                st.wait_event(root)
+            one(i)
+            tail = torch.cuda.Event()
+            tail.record(s_out)
+            comp.wait_event(tail)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=comp):
+        root = torch.cuda.Event()
+        root.record(comp)
+        for st in (s_x, s_y, s_out):
+            st.wait_event(root)
+        for i in range(G):
+            one(i)
+        for st in (s_x, s_y, s_out):
+            j = torch.cuda.Event()
+            j.record(st)
+            comp.wait_event(j)
+    with torch.cuda.stream(comp):
+        g.replay()
+    comp.synchronize()
+    e_a = torch.cuda.Event(enable_timing=True)
+    e_b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(comp):
+        e_a.record(comp)
+        for _ in range(reps):
+            g.replay()
+        e_b.record(comp)
     e_b.synchronize()
-    e2e_ms = e_a.elapsed_time(e_b) / steps
+    e2e_ms = e_a.elapsed_time(e_b) / (reps * G)
     h2d = (x_h.numel() + y_h.numel()) * b.es + ids_h.numel() * 4
     d2h = y_out.numel() * b.es
     return {"value": w.M / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
