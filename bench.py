@@ -460,6 +460,50 @@ class Bench:
         out["kept_batch_step_us"] = self.delta_chain_us(G, self.path)
         return out
 
+    def split_calls_us(self, G):
+        """Device time (us per call) of lora_shrink and of lora_expand, each in
+        a chain of G back-to-back calls on prepared batches: the two halves of
+        the fused delta, with h in global memory between them."""
+        torch, B, w = self.torch, self.B, self.w
+        batches = [self.prepare(s) for s in self.sets]
+        hs = [torch.zeros((w.M, w.r_max), dtype=torch.float32, device=self.dev) for _ in range(min(self.n_sets, 4))]
+
+        def shrink(i):
+            s = self.sets[i % self.n_sets]
+            B.lora_shrink(batches[i % self.n_sets], s["x"], s["A"], h=hs[i % len(hs)], ranks=self.ranks,
+                          path=self.path, stream=self.stream)
+
+        def expand(i):
+            s = self.sets[i % self.n_sets]
+            B.lora_expand(batches[i % self.n_sets], hs[i % len(hs)], s["B"], s["y"], scale=w.scale,
+                          adapter_scale=self.ascale, ranks=self.ranks, path=self.path, stream=self.stream)
+
+        out = {}
+        for name, fn in (("shrink", shrink), ("expand", expand)):
+            with torch.cuda.stream(self.stream):
+                for i in range(3):
+                    fn(i)
+            self.stream.synchronize()
+            used = B.lora_last_kernels()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream, capture_error_mode="thread_local"):
+                for i in range(G):
+                    fn(i)
+            with torch.cuda.stream(self.stream):
+                g.replay()
+            self.stream.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(self.stream):
+                self.delay()
+                e0.record(self.stream)
+                g.replay()
+                e1.record(self.stream)
+            e1.synchronize()
+            out[name + "_us"] = 1e3 * e0.elapsed_time(e1) / G
+            out[name + "_kernels"] = [n for bit, n in sorted(B.KERNEL_NAMES.items()) if used & bit]
+        return out
+
     def delta_chain_us(self, G, path):
         """Average launch time (us) of lora_delta in a chain of G back-to-back
         calls on prepared batches of the rotating sets."""
@@ -705,6 +749,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         # a decode step that keeps its grouping and patches the rows that
         # changed (a few sequences join or leave), against the full rebuild
         incremental = b.incremental_us(min(256, max(8, K)), max(1, w.M // 32))
+    split_calls = None
+    if world == 1 and not b.rank_major:
+        # the same batch through lora_shrink then lora_expand (h in global memory)
+        split_calls = b.split_calls_us(min(64, max(8, K)))
     del b
     torch.cuda.empty_cache()
 
@@ -760,6 +808,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     }
     if incremental is not None:
         line["incremental_grouping"] = incremental
+    if split_calls is not None:
+        line["split_calls"] = split_calls
     if others:
         line["other_workloads"] = others
     if world == 1 and not args.no_cpu_baseline:

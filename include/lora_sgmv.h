@@ -94,7 +94,8 @@ typedef int lora_status_t;
 #define LORA_PATH_CUDA_CORE 1 /* no tcgen05 kernel: the small-batch or streaming kernel where they
                                  take the batch, else the small-segment kernel (clusters of CTAs,
                                  warp-level bf16 tensor-core tiles; fp32: CUDA-core FMAs) */
-#define LORA_PATH_TENSOR 2    /* every segment on the tcgen05 kernel (bf16 only) */
+#define LORA_PATH_TENSOR 2    /* every segment on the tcgen05 kernel (bf16 only; lora_delta,
+                                 lora_shrink and lora_expand) */
 
 /* Largest supported sizes. */
 #define LORA_MAX_TOKENS (1 << 24)

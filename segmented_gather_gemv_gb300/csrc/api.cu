@@ -315,8 +315,7 @@ lora_status_t dispatch_one(const lora_batch_t *b, int32_t dtype, int mode, int32
         g_last_kernels |= LORA_KERNEL_PREPARE;
     }
     if (path == LORA_PATH_TENSOR) {
-        if (!tensor_ok || mode != kFused)
-            return fail(LORA_ERR_UNSUPPORTED, "the tensor-core path computes the fused bf16 delta only");
+        if (!tensor_ok) return fail(LORA_ERR_UNSUPPORTED, "the tensor-core path computes bf16 only");
         if (p.r_max > kTcMaxRankCommon && !p.ranks)
             return fail(LORA_ERR_UNSUPPORTED, "the tensor-core path takes ranks up to %d", kTcMaxRankCommon);
         // every segment: the row space is the sorted rows themselves
@@ -333,7 +332,7 @@ lora_status_t dispatch_one(const lora_batch_t *b, int32_t dtype, int mode, int32
             g_last_kernels |= LORA_KERNEL_TENSOR;
         }
     } else {
-        const bool split = path == LORA_PATH_AUTO && tensor_ok && mode == kFused;
+        const bool split = path == LORA_PATH_AUTO && tensor_ok;
         p.min_len = 0;
         p.max_len = split ? b->tc_min_rows : 0x7fffffff;
         p.split_tc = split ? 1 : 0;

@@ -32,6 +32,11 @@
 // Ranks are masked exactly: A rows / B columns past an adapter's rank are
 // never read, H columns past it are zero, so padding never reaches y.
 //
+// Split calls (one instantiation per mode): a shrink runs the x jobs only and
+// the epilogue writes each row's D1 columns to h in global memory (fp32,
+// unscaled, zero past the rank); an expand runs the y jobs only, with H
+// built from h in global memory (scaled, rounded to bf16) instead of D1.
+//
 // Data movement.  The kernel streams x once and y twice (read, write); the
 // adapter weights are small and stay in L2.  All staging goes through ONE
 // ring of stages, filled in program order: a tile's nkb "x jobs" (x rows of
@@ -411,6 +416,9 @@ __device__ __forceinline__ float exact_output(uint32_t yword, int e, const unsig
     return yv + dsum;
 }
 
+// MODE: kFused, kShrink (x jobs only; h out, unscaled) or kExpand (h in;
+// y jobs only).
+template <int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
     sgmv_tc_kernel(const __grid_constant__ DeltaArgs p, const __grid_constant__ TcMaps m) {
     extern __shared__ unsigned char smem_raw[];
@@ -427,8 +435,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 0) {
         // the tensor maps of the TMA copies, one per lane: x, y per slice, A
         const CUtensorMap *mp = nullptr;
-        if (m.use && lane < 3) mp = lane == 0 ? &m.x64 : lane == 1 ? &m.x32 : &m.x8;
-        else if (m.use && lane < 3 + 3 * p.n_slices) {
+        if (m.use && MODE != kExpand && lane < 3) mp = lane == 0 ? &m.x64 : lane == 1 ? &m.x32 : &m.x8;
+        else if (m.use && MODE != kShrink && lane >= 3 && lane < 3 + 3 * p.n_slices) {
             const int t = (lane - 3) / 3, k = (lane - 3) - 3 * t;
             mp = k == 0 ? &m.y64[t] : k == 1 ? &m.y32[t] : &m.y8[t];
         } else if (m.use_ab && lane >= 16 && lane < 19 && (8 << (lane - 16)) <= m.a_box_max)
@@ -531,7 +539,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int nkb = (p.d_in + kBK - 1) / kBK;
     // Every CTA walks the K blocks and the n-tiles from its own starting
     // point, so that the CTAs do not all hit the same column block at once.
-    const int kb_rot = (int)(((uint32_t)blockIdx.x * 2654435761u) >> 7) % nkb;
+    const int kb_rot = nkb > 0 ? (int)(((uint32_t)blockIdx.x * 2654435761u) >> 7) % nkb : 0;
     const int nt_rot = (int)(((uint32_t)blockIdx.x * 2246822519u) >> 7) % (n_nt > 0 ? n_nt : 1);
     const __nv_bfloat16 *yg = static_cast<const __nv_bfloat16 *>(p.y);
     bool ok = true;
@@ -894,8 +902,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mbar_arrive_n(&empty[s], kEpiWarps - 1);
                     umma_commit(&empty[s]);
                 }
-                umma_commit(d1f);
-                // H of this tile is ready once the epilogue has written it.
+                if (MODE != kExpand) umma_commit(d1f);
+                // H of this tile is ready once the epilogue has written it
+                // (shrink only: the epilogue has read D1)
                 if (!wait1(hr, tiles & 1, ok, abort)) goto role_done;
                 tc_fence_after();
                 for (int nt = 0; nt < n_nt; ++nt, ++job, ++ts) {
@@ -919,7 +928,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                              smem_desc(bb + kc * 2 * kBChunk, kBChunk, 128, kLayoutNone), id2, 1);
                     umma_commit(&tf[sd]);
                 }
-                umma_commit(he);
+                if (MODE != kShrink) umma_commit(he);
                 ++tiles;
             }
         }
@@ -939,6 +948,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // with the tensor-core path forced they are an error.
             if (p.tc_only && ew == 0 && lane < t.np && sel(t.rk, lane) == 0 && sel(t.rank, lane) != 0)
                 raise_deverr(p.counts, LORA_DEVERR_RANK);
+            if (MODE == kShrink && p.tc_only && chalf == 0 && row < t.n && sel(t.rank, t.piece_of(row)) == 0) {
+                // every segment is this kernel's: h rows of rank-0 adapters are zero
+                float *hrow = p.h + (int64_t)tile_token(p, t, row) * p.ldh;
+                for (int j = 0; j < p.r_max; ++j) hrow[j] = 0.f;
+            }
             if (t.K == 0) continue;
             job += nkb;  // the x stages of this tile are the MMA's
             const int K16 = (t.K + 15) & ~15;
@@ -948,12 +962,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int my_tok = row < t.n ? tile_token(p, t, row) : 0;
             const int k_lo = live ? sel(t.kofs, pq) : 0, k_hi = live ? sel(t.kofs, pq) + sel(t.rk, pq) : 0;
             const float sc = live ? (p.adapter_scale ? p.adapter_scale[sel(t.a, pq)] : p.scale) : 0.f;
-            if (chalf == 0) {
-                // ---- D1 -> scale -> bf16 H (columns of other pieces are zero)
-                if (!wait_warp(d1f, tiles & 1, ok, abort)) goto role_done;
-                tc_fence_after();
+            if (chalf == 0 && MODE == kExpand) {
+                // ---- h (global, fp32) -> scale -> bf16 H (columns of other pieces are zero)
                 if (tiles > 0)
                     if (!wait_warp(he, (tiles - 1) & 1, ok, abort)) goto role_done;  // previous expand done with H
+                const float *hrow = p.h + (int64_t)my_tok * p.ldh;
+                for (int c8 = 0; c8 < kTcMaxRank / 8; ++c8) {
+                    if (8 * c8 >= K16) break;
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 8 * c8 + 2 * e;
+                        const float f0 = j >= k_lo && j < k_hi ? hrow[j - k_lo] * sc : 0.f;
+                        const float f1 = j + 1 >= k_lo && j + 1 < k_hi ? hrow[j + 1 - k_lo] * sc : 0.f;
+                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(f0, f1);
+                        w[e] = *reinterpret_cast<const uint32_t *>(&h2);
+                    }
+                    *reinterpret_cast<uint4 *>(H + c8 * kHChunk + row * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(hr);
+            } else if (chalf == 0) {
+                // ---- D1 -> scale -> bf16 H (columns of other pieces are
+                // zero), or (shrink) D1 -> h in global memory, unscaled, zero
+                // past the rank
+                if (!wait_warp(d1f, tiles & 1, ok, abort)) goto role_done;
+                tc_fence_after();
+                if (tiles > 0 && MODE != kShrink)
+                    if (!wait_warp(he, (tiles - 1) & 1, ok, abort)) goto role_done;  // previous expand done with H
+                float *hout = MODE == kShrink && live ? p.h + (int64_t)my_tok * p.ldh : nullptr;
                 for (int c16 = 0; c16 < kTcMaxRank / 16; ++c16) {
                     if (16 * c16 >= K16) break;
                     uint32_t v[16], u[3][16];
@@ -965,6 +1004,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int e = 0; e < 16; ++e)
                         v[e] = __float_as_uint((__uint_as_float(v[e]) + __uint_as_float(u[0][e])) +
                                                (__uint_as_float(u[1][e]) + __uint_as_float(u[2][e])));
+                    if (MODE == kShrink) {
+                        if (hout) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const int j = 16 * c16 + e - k_lo;
+                                if (j >= 0 && j < k_hi - k_lo) hout[j] = __uint_as_float(v[e]);
+                            }
+                        }
+                        continue;
+                    }
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         const int c8 = 2 * c16 + half;
@@ -980,6 +1029,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         *reinterpret_cast<uint4 *>(H + c8 * kHChunk + row * 16) = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
+                if (hout)
+                    for (int j = k_hi - k_lo; j < p.r_max; ++j) hout[j] = 0.f;
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
@@ -1137,10 +1188,11 @@ bool encode_rows(EncodeTiledFn fn, CUtensorMap *map, const void *base, int64_t c
 }  // namespace
 
 cudaError_t launch_tc(const DeltaArgs &p, int mode, int sms, cudaStream_t stream) {
-    if (mode != kFused) return cudaErrorNotSupported;
-    static DeviceOnce once;
-    cudaError_t e = once.run([] {
-        return cudaFuncSetAttribute(sgmv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+    if (mode != kFused && mode != kShrink && mode != kExpand) return cudaErrorNotSupported;
+    static DeviceOnce once[3];
+    auto kern = mode == kShrink ? sgmv_tc_kernel<kShrink> : mode == kExpand ? sgmv_tc_kernel<kExpand> : sgmv_tc_kernel<kFused>;
+    cudaError_t e = once[mode].run([&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
     });
     if (e != cudaSuccess) return e;
     // Tensor maps for the TMA copies of contiguous row groups; without them
@@ -1149,12 +1201,13 @@ cudaError_t launch_tc(const DeltaArgs &p, int mode, int sms, cudaStream_t stream
     TcMaps maps;
     memset(&maps, 0, sizeof(maps));
     EncodeTiledFn fn = encode_fn();
+    // (shrink: x and A only; expand: y and B only)
     bool use = fn != nullptr;
-    if (use)
+    if (use && mode != kExpand)
         use = encode_rows(fn, &maps.x64, p.x, p.d_in, p.M_rows, p.ldx, 64) &&
               encode_rows(fn, &maps.x32, p.x, p.d_in, p.M_rows, p.ldx, 32) &&
               encode_rows(fn, &maps.x8, p.x, p.d_in, p.M_rows, p.ldx, 8);
-    for (int t = 0; use && t < p.n_slices; ++t) {
+    for (int t = 0; use && mode != kShrink && t < p.n_slices; ++t) {
         const void *yb = static_cast<const __nv_bfloat16 *>(p.y) + p.slices[t].y_col;
         use = encode_rows(fn, &maps.y64[t], yb, p.slices[t].d_out, p.M_rows, p.ldy, 64) &&
               encode_rows(fn, &maps.y32[t], yb, p.slices[t].d_out, p.M_rows, p.ldy, 32) &&
@@ -1164,7 +1217,7 @@ cudaError_t launch_tc(const DeltaArgs &p, int mode, int sms, cudaStream_t stream
     // A and B pools as 3-D maps (rank rows / columns past r_pad read zeros)
     bool use_ab = use;
     maps.r_pad = (p.r_max + 7) & ~7;
-    if (use_ab) {
+    if (use_ab && mode != kExpand) {
         const cuuint64_t dims[3] = {(cuuint64_t)p.d_in, (cuuint64_t)p.r_max, (cuuint64_t)p.n_adapters};
         const cuuint64_t strides[2] = {(cuuint64_t)(p.a_stride_r * 2), (cuuint64_t)(p.a_stride_adapter * 2)};
         const cuuint32_t box[3] = {64, 8, 1}, elem[3] = {1, 1, 1};
@@ -1183,7 +1236,7 @@ cudaError_t launch_tc(const DeltaArgs &p, int mode, int sms, cudaStream_t stream
             maps.a_box_max = 16 << w;
         }
     }
-    for (int t = 0; use_ab && t < p.n_slices; ++t) {
+    for (int t = 0; use_ab && mode != kShrink && t < p.n_slices; ++t) {
         const SliceDesc &S = p.slices[t];
         const cuuint64_t dims[3] = {(cuuint64_t)p.r_max, (cuuint64_t)S.d_out, (cuuint64_t)p.n_adapters};
         const cuuint64_t strides[2] = {(cuuint64_t)(S.stride_n * 2), (cuuint64_t)(S.stride_adapter * 2)};
@@ -1203,7 +1256,7 @@ cudaError_t launch_tc(const DeltaArgs &p, int mode, int sms, cudaStream_t stream
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, sgmv_tc_kernel, p, maps);
+    return cudaLaunchKernelEx(&cfg, kern, p, maps);
 }
 
 }  // namespace lora

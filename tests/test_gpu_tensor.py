@@ -152,3 +152,62 @@ def test_auto_split_back_to_back_calls(B, M):
     assert rel_err(yg, base + 2.0 * (once - base), base, act) <= 2 * TOL[w.dtype]
     assert np.array_equal(yg[~act], base[~act])
     assert batch.counts()["tc_rows"] > 0
+
+
+# ------------------------------- split calls (lora_shrink / lora_expand)
+
+def _shrink_expand(B, w, path, tc_min=0, seed=0):
+    """lora_shrink into a guarded h, then lora_expand of a seeded h (not the
+    GPU's); both against the oracle's shrink and expand."""
+    import oracle
+    d = to_dev(w)
+    batch = B.lora_prepare_batch(d["ids"], w.n_adapters, w.chunk_size, tc_min_rows=tc_min)
+    act = active_rows(w)
+    guard = torch.full((w.M, w.r_max + 4), -777.0, device="cuda")
+    h = guard[:, :w.r_max]
+    B.lora_shrink(batch, d["x"], d["A"], h=h, ranks=d["ranks"], path=path)
+    torch.cuda.synchronize()
+    kernels = B.lora_last_kernels()
+    assert torch.all(guard[:, w.r_max:] == -777.0), "h written past r_max"
+    hg = h.cpu().numpy().astype(np.float64)
+    assert np.all(hg[~act] == -777.0), "h rows outside segments written"
+    h_ref = oracle.shrink(w.x, w.ids, w.A, ranks=w.ranks)
+    err = np.abs(hg[act] - h_ref[act]).max() / np.abs(h_ref[act]).max()
+    assert err <= TOL[w.dtype], "shrink rel err %.3e" % err
+    rng = np.random.default_rng(seed)
+    h_in = rng.standard_normal((w.M, w.r_max)).astype(np.float32)
+    y = d["y"].clone()
+    B.lora_expand(batch, torch.from_numpy(h_in).cuda(), d["B"], y, scale=w.scale,
+                  adapter_scale=d["adapter_scale"], ranks=d["ranks"], path=path)
+    torch.cuda.synchronize()
+    y_ref = oracle.expand(h_in, w.ids, w.B, w.y, scale=w.scale, adapter_scale=w.adapter_scale, ranks=w.ranks)
+    yg = y.float().cpu().numpy().astype(np.float64)
+    e2 = rel_err(yg, y_ref, w.y.astype(np.float64), act)
+    assert e2 <= TOL[w.dtype], "expand rel err %.3e" % e2
+    assert np.array_equal(yg[~act], w.y[~act].astype(np.float64)), "inactive rows changed"
+    assert batch.counts()["device_error"] == 0
+    return kernels, B.lora_last_kernels()
+
+
+@pytest.mark.parametrize("ci", range(len(TC_CASES)))
+def test_tensor_shrink_expand_forced(B, ci):
+    w = wl.random_batch(seed=450 + ci, dtype="bf16", **TC_CASES[ci])
+    k_s, k_e = _shrink_expand(B, w, B.PATH_TENSOR, seed=451 + ci)
+    assert k_s == B.KERNEL_TENSOR and k_e == B.KERNEL_TENSOR
+
+
+@pytest.mark.parametrize("n_decode", [0, 60])
+def test_shrink_expand_auto_split(B, n_decode):
+    # long groups on the tensor-core kernel, the rest on the small-segment kernel
+    w = wl.mixed_serving(n_prefill_seq=3, prefill_rows=2600, len_lo=300, len_hi=1200, n_decode=n_decode,
+                         n_pool=16, r=16, d_in=1024, d_outs=(512, 256, 256))
+    k_s, k_e = _shrink_expand(B, w, B.PATH_AUTO, seed=470 + n_decode)
+    assert k_s & B.KERNEL_TENSOR and k_e & B.KERNEL_TENSOR
+
+
+def test_tensor_shrink_rank_zero_rows(B):
+    # with every segment forced onto the tensor-core kernel, rows of rank-0
+    # adapters get zero h (they are in segments); mixed with rank-16 groups
+    w = wl.random_batch(seed=480, M=300, d_in=512, d_outs=[256], n_pool=4, r_max=16, run_len=60,
+                        ranks=[0, 16], dtype="bf16")
+    _shrink_expand(B, w, B.PATH_TENSOR, seed=481)
