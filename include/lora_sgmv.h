@@ -347,6 +347,12 @@ lora_status_t lora_batch_refresh(lora_batch_t *batch, void *stream);
  * r_a <= j < r_max, for every row i in a segment (unscaled; "vLLM-Ascend
  * LoRA" article, section 3.2: first project d_in down to r).  Rows in no
  * segment keep their h contents.  h: device fp32 [M][ldh], ldh >= r_max.
+ * Kernels (bf16): under LORA_PATH_AUTO the segments of groups with at least
+ * tc_min_rows rows and a tensor-core rank (a multiple of 8, at most 32) run
+ * on the tcgen05 kernel (x jobs only, h written from its fp32 accumulator),
+ * the others on the small-segment kernel, side by side; LORA_PATH_TENSOR puts
+ * every segment on the tcgen05 kernel, LORA_PATH_CUDA_CORE (and fp32) every
+ * segment on the small-segment kernel.
  */
 lora_status_t lora_shrink(const lora_batch_t *batch, int32_t dtype,
                           const void *x, int64_t ldx, int32_t d_in,
@@ -360,6 +366,9 @@ lora_status_t lora_shrink(const lora_batch_t *batch, int32_t dtype,
  * for every row i in a segment and every slice t ("vLLM-Ascend LoRA"
  * article, section 3.3: delta = (tmp * scale) . B^T added into out).
  * slices: host array of n_slices (1..LORA_MAX_SLICES) descriptors.
+ * Kernels as for lora_shrink (the tcgen05 kernel runs y jobs only).  On the
+ * tcgen05 kernel s_a * h is rounded once to bf16 for the tensor cores, as in
+ * lora_delta; y + delta is formed in fp32 and rounded to y's type once.
  */
 lora_status_t lora_expand(const lora_batch_t *batch, int32_t dtype,
                           const float *h, int64_t ldh, int32_t r_max,
