@@ -120,8 +120,8 @@ def test_auto_split_rank64_long_segments_use_cuda_cores(B):
 
 @pytest.mark.parametrize("n_decode", [0, 60, 106])
 def test_auto_split_small_batch_both_kernels(B, n_decode):
-    # batches of at most 256 rows start the CUDA-core kernel first; here the
-    # tensor-core kernel after it has long segments to do as well
+    # the CUDA-core kernel starts first; here the tensor-core kernel after it
+    # has long segments to do as well
     w = wl.mixed_serving(n_prefill_seq=2, prefill_rows=150, len_lo=64, len_hi=100, n_decode=n_decode,
                          n_pool=16, r=16, d_in=1024, d_outs=(512, 256, 256))
     assert w.M <= 256
