@@ -1049,12 +1049,16 @@ static bool small_geometry(const DeltaArgs &p, int R16, int cl, int ncl, SmGeom 
 }
 
 // Cluster size by the larger of d_in and d_out: a CTA's K and N slices stay
-// at most about 2048 columns.
+// at most about 4096 columns, in clusters of at least two above 1024.  Fewer,
+// wider CTAs per tile measured faster than the 2048-column slices of the
+// single-pass kernel: mixed serving (4096 -> 6144) 54.4 -> 50.9 us per launch
+// in clusters of 2 instead of 4 (59.5 in clusters of 1), mixed rank (4096 ->
+// 14336) 49.7 -> 41.8 us in clusters of 4 instead of 8.
 static int small_cluster_size(int d_in, int d_out) {
     const int d = d_in > d_out ? d_in : d_out;
     if (d < 1024) return 1;
-    if (d < 2048) return 2;
-    if (d <= 8192) return 4;
+    if (d <= 8192) return 2;
+    if (d <= 16384) return 4;
     return 8;
 }
 
