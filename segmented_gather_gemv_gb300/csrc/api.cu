@@ -326,7 +326,12 @@ lora_status_t dispatch_one(const lora_batch_t *b, int32_t dtype, int mode, int32
         p.tc_count_index = LORA_COUNT_SEGS;
         p.tc_rows_index = LORA_COUNT_ACTIVE;
         p.tc_only = 1;
-        e = launch_tc(p, mode, tc_grid(b->M), stream);
+        const int g = tc_grid(b->M);
+        // prepare's shares, which the kernel takes when every segment is on
+        // the tensor-core list
+        p.tc_share = share_table(b->counts);
+        p.tc_share_grid = g <= kMaxShareGrid ? g : -1;
+        e = launch_tc(p, mode, g, stream);
         if (e == cudaSuccess) {
             launch_counter().fetch_add(1, std::memory_order_relaxed);
             g_last_kernels |= LORA_KERNEL_TENSOR;

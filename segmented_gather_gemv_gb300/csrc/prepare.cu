@@ -51,36 +51,87 @@ struct PrepArgs {
     int32_t hs, off_hash, off_gtab;
 };
 
-// Shares of the tensor-core row space for a grid of `grid` CTAs, by the rule
-// the tensor-core kernel applies itself when it has no table: the share end
-// e = rows * b / grid moves to the boundary between two adapters when one
-// lies within half a share (chunks of one adapter do not count).  Written for
-// every batch, zeros when it has no such row.  `tcl` / `tcp` are the
-// tensor-core records and their row prefix (nseg of them).
-__device__ void write_shares(const int4 *tcl, const int32_t *tcp, int nseg, int rows, int grid, int2 *shares) {
-    const int half = grid > 0 ? (int)(rows / (2 * (int64_t)grid)) : 0;
-    auto seg_of = [&](int r) {  // largest i < nseg with tcp[i] <= r
-        int lo = 0, hi = nseg - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (tcp[mid] <= r) lo = mid;
-            else hi = mid - 1;
-        }
-        return lo;
-    };
-    for (int b = threadIdx.x; grid > 0 && b <= grid; b += blockDim.x) {
-        int e = (int)((int64_t)rows * b / grid), sg = 0;
-        if (nseg > 0 && rows > 0) {
-            if (nseg >= 2 && e > 0 && e < rows) {
-                const int i = seg_of(e);
-                const int lo = tcp[i], hi = tcp[i + 1], a = tcl[i].z;
-                if (e - lo <= half && i > 0 && tcl[i - 1].z != a) e = lo;
-                else if (hi - e <= half && i + 1 < nseg && tcl[i + 1].z != a) e = hi;
-            }
-            sg = e < rows ? seg_of(e) : nseg;
-        }
-        shares[b] = make_int2(e, sg);
+// Shares of the tensor-core row space for a grid of `grid` CTAs: boundary b
+// (b <= grid) = {first row of CTA b, the segment holding it}; zeros when the
+// batch has no such row.  `tcl` / `tcp` are the tensor-core records and their
+// row prefix (nseg of them).  The share end e = rows * b / grid moves to the
+// boundary between two adapter groups (runs of records of one adapter: the
+// chunks of a chunked group) when one lies within half a share, so that a
+// tile holds rows of two adapters only where the groups are short.  The
+// boundaries come from a table of the groups' first rows (up to
+// kShareGroups groups); with more groups each end looks only at the
+// boundaries of its own record, which is exact for unchunked batches.
+// plan_shares builds the shares in shared memory (every thread of the block
+// calls it; it reads only the block's own records, so it may run before the
+// wait on the previous grid); store_shares writes them to the workspace.
+constexpr int kShareGroups = 256;
+struct ShareTable {
+    int2 b[kMaxShareGrid + 1];
+    int gstart[kShareGroups + 1];  // first row of group g; [ng] = rows
+    int ng;                        // groups in gstart, 0 when they do not fit
+};
+
+// largest i < n with v[i] <= r (v ascending, v[0] <= r)
+__device__ __forceinline__ int last_le(const int32_t *v, int n, int r) {
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (v[mid] <= r) lo = mid;
+        else hi = mid - 1;
     }
+    return lo;
+}
+
+__device__ void plan_shares(const int4 *tcl, const int32_t *tcp, int nseg, int rows, int grid, ShareTable &T) {
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const bool any = nseg > 0 && rows > 0 && grid > 0;
+    __syncthreads();  // the records and tcp[nseg] are complete
+    if (tid < 32) {
+        // the groups' first rows: a group starts at every record whose
+        // adapter differs from the one before
+        const int lane = tid;
+        int ng = 0;
+        for (int base = 0; any && base < nseg && ng <= kShareGroups; base += 32) {
+            const int i = base + lane;
+            const bool head = i < nseg && (i == 0 || tcl[i - 1].z != tcl[i].z);
+            const unsigned bal = __ballot_sync(0xffffffffu, head);
+            const int k = ng + __popc(bal & ((1u << lane) - 1u));
+            if (head && k < kShareGroups) T.gstart[k] = tcp[i];
+            ng += __popc(bal);
+        }
+        if (lane == 0) {
+            T.ng = ng <= kShareGroups ? ng : 0;
+            if (ng <= kShareGroups) T.gstart[ng] = rows;
+        }
+    }
+    __syncthreads();
+    const int half = grid > 0 ? (int)(rows / (2 * (int64_t)grid)) : 0;
+    const int ng = T.ng;
+    for (int b = tid; grid > 0 && b <= grid; b += nthr) {
+        int e = (int)((int64_t)rows * b / grid), sg = 0;
+        if (any) {
+            if (nseg >= 2 && e > 0 && e < rows) {
+                if (ng > 0) {
+                    const int g = last_le(T.gstart, ng, e);
+                    const int lo = T.gstart[g], hi = T.gstart[g + 1];
+                    if (e - lo <= half && g > 0) e = lo;
+                    else if (hi - e <= half && g + 1 < ng) e = hi;
+                } else {
+                    const int i = last_le(tcp, nseg, e);
+                    const int lo = tcp[i], hi = tcp[i + 1], a = tcl[i].z;
+                    if (e - lo <= half && i > 0 && tcl[i - 1].z != a) e = lo;
+                    else if (hi - e <= half && i + 1 < nseg && tcl[i + 1].z != a) e = hi;
+                }
+            }
+            sg = e < rows ? last_le(tcp, nseg, e) : nseg;
+        }
+        T.b[b] = make_int2(e, sg);
+    }
+}
+
+// Each thread writes the boundaries it computed in plan_shares.
+__device__ __forceinline__ void store_shares(const ShareTable &T, int grid, int2 *shares) {
+    for (int b = threadIdx.x; grid > 0 && b <= grid; b += blockDim.x) shares[b] = T.b[b];
 }
 
 // Block-wide exclusive scan of one value per thread.  `ws` is shared scratch
@@ -114,10 +165,11 @@ __device__ __forceinline__ int block_excl_scan(int v, int *total, int *ws) {
     return res;
 }
 
-__global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
+__global__ void __launch_bounds__(1024, 1) prepare_kernel(const __grid_constant__ PrepArgs p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ int scan_ws[33];
     __shared__ int s_invalid;
+    __shared__ ShareTable s_shares;
 
     // Phases 1-3 read only the ids and write only shared memory; when every
     // table of theirs is in shared memory they run before the wait on the
@@ -482,6 +534,7 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
         }
     }
 
+    plan_shares(o_tc, o_tcptr, n_tc, tc_rows, p.share_grid, s_shares);
     if (stage) {
         // copy the staged outputs (descriptors as 16-byte pieces)
         __syncthreads();
@@ -494,8 +547,7 @@ __global__ void prepare_kernel(const __grid_constant__ PrepArgs p) {
         for (int k = tid; k < n16; k += nthr) dst[k] = src[k];
     }
 
-    __syncthreads();  // the tensor-core list (shared or global) is complete
-    write_shares(o_tc, o_tcptr, n_tc, tc_rows, p.share_grid, p.shares);
+    store_shares(s_shares, p.share_grid, p.shares);
 
     // Phase 6: counters.
     if (tid == 0) {
@@ -535,6 +587,7 @@ __global__ void __launch_bounds__(kPrepSmallThreads, 1) prepare_small_kernel(con
     constexpr int NW = kPrepSmallThreads / 32;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ unsigned long long wsum[NW];
+    __shared__ ShareTable s_shares;
     // The next grid may start at once (see griddep_launch_dependents): this
     // grid writes global memory only after its wait.
     griddep_launch_dependents();
@@ -703,7 +756,9 @@ __global__ void __launch_bounds__(kPrepSmallThreads, 1) prepare_small_kernel(con
     }
     __syncthreads();
 
-    // 6. after the previous grid: the copy, the shares, the counters
+    // 6. the shares (computed before the wait), then after the previous grid:
+    // the copy, the shares, the counters
+    plan_shares(o_tc, o_tcptr, n_tc, tc_rows, p.share_grid, s_shares);
     griddep_wait();
     {
         const int4 *src = reinterpret_cast<const int4 *>(stg);
@@ -711,7 +766,7 @@ __global__ void __launch_bounds__(kPrepSmallThreads, 1) prepare_small_kernel(con
         const int n16 = int(O.total / 16);
         for (int k = tid; k < n16; k += kPrepSmallThreads) dst[k] = src[k];
     }
-    write_shares(o_tc, o_tcptr, n_tc, tc_rows, p.share_grid, p.shares);
+    store_shares(s_shares, p.share_grid, p.shares);
     if (tid == 0) {
         p.counts[LORA_COUNT_SEGS] = S;
         p.counts[LORA_COUNT_ACTIVE] = ACT;

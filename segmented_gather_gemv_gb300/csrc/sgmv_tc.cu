@@ -473,15 +473,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             n == k ? (uint16_t)0x3F80 : (uint16_t)0;
         fence_proxy_async_smem();
     }
+    bool planned = false;
     if (warp == kMmaWarp && p.tc_share != nullptr && p.tc_share_grid == (int)gridDim.x) {
-        // the shares prepare computed for this grid (the same rule as below)
-        if (lane == 0) {
-            const int2 s0 = p.tc_share[blockIdx.x], s1 = p.tc_share[blockIdx.x + 1];
+        // the shares prepare computed for this grid over its tensor-core
+        // list; a call that routes every segment here (tc_only) takes them
+        // when that list holds every segment (the two row spaces are then
+        // the same)
+        const int2 s0 = p.tc_share[blockIdx.x], s1 = p.tc_share[blockIdx.x + 1];
+        planned = !p.tc_only || p.counts[LORA_COUNT_TC_SEGS] == p.counts[LORA_COUNT_SEGS];
+        if (planned && lane == 0) {
             range[0] = s0.x;
             range[1] = max(s0.x, s1.x);
             range[2] = s0.x < s1.x ? s0.y : 0;
         }
-    } else if (warp == kMmaWarp) {
+    }
+    if (warp == kMmaWarp && !planned) {
         // This CTA's row range: an equal share of the row space.
         const int nseg = min(p.counts[p.tc_count_index], p.max_list);
         const int Mrows = nseg > 0 ? p.counts[p.tc_rows_index] : 0;
@@ -490,7 +496,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // within half a share: a tile of one adapter needs no row split by a
         // piece boundary (its rows move by TMA boxes alone) and no second
         // pass when two ranks do not fit one tile.  Chunks of one adapter do
-        // not count as boundaries.  Both neighbours compute the same end.
+        // not count as boundaries, but only the boundaries of the record
+        // holding the end are seen (prepare's table looks at whole adapter
+        // groups).  Both neighbours compute the same end.
         const int half = (int)(Mrows / (2 * (int64_t)G));
         auto adapter_of = [&](int i) { return p.tc_adapter[(int64_t)i * p.tc_rec_stride]; };
         auto share_end = [&](int e) {
