@@ -197,8 +197,9 @@ typedef struct lora_b_slice {
                                4.2: adapter-major, rank-secondary weight blocks).
                                All slices of a call share one layout; rank-major
                                pools run on the streaming kernel only (bf16
-                               lora_delta, batches it takes), other calls return
-                               LORA_ERR_UNSUPPORTED. */
+                               lora_delta; a batch above its 2048 rows runs as
+                               consecutive launches over 2048-row ranges), other
+                               calls return LORA_ERR_UNSUPPORTED. */
 } lora_b_slice_t;
 
 /*

@@ -1,6 +1,7 @@
 // api.cu -- the extern "C" boundary of the library: argument checks,
 // workspace carving and kernel dispatch.  Declarations and the contract of
 // every entry point are in include/lora_sgmv.h.
+#include <algorithm>
 #include <climits>
 #include <cstdarg>
 #include <cstdio>
@@ -228,6 +229,38 @@ cudaError_t refresh_metadata(const lora_batch_t *b, cudaStream_t stream) {
                           b->order == LORA_ORDER_ASCENDING, grid <= kMaxShareGrid ? grid : 0, base, L, &tmp, stream);
 }
 
+// Rows one streaming launch groups on chip.
+constexpr int kStreamRangeRows = 2048;
+
+// The streaming kernel over a batch of any size: consecutive launches over
+// row ranges of at most kStreamRangeRows (ids, x and y offset by the range's
+// first row).  Each launch groups its own rows and writes only them, so the
+// ranges are independent; an adapter seen by several ranges has its weights
+// read once per range.  The kernel's launch geometry only shrinks with the
+// rows, so when the first (fullest) range is taken every later one is too;
+// when it is declined nothing was launched and this returns false.  Sets
+// *n_launched to the launches made.
+static bool try_launch_stream_ranges(const DeltaArgs &p, int sms, cudaStream_t stream, cudaError_t *err,
+                                     int *n_launched) {
+    *n_launched = 0;
+    const size_t es = 2;  // bf16
+    for (int lo = 0; lo < p.M_rows; lo += kStreamRangeRows) {
+        DeltaArgs q = p;
+        q.M_rows = std::min(kStreamRangeRows, p.M_rows - lo);
+        q.ids = p.ids + lo;
+        q.x = static_cast<const char *>(p.x) + (size_t)lo * (size_t)p.ldx * es;
+        q.y = static_cast<char *>(p.y) + (size_t)lo * (size_t)p.ldy * es;
+        if (!try_launch_stream(q, sms, stream, err)) {
+            if (lo == 0) return false;
+            *err = cudaErrorNotSupported;  // not reached: a smaller range fits where the first did
+            return true;
+        }
+        if (*err != cudaSuccess) return true;
+        ++*n_launched;
+    }
+    return true;
+}
+
 // Launches the kernels of one call according to the path.
 lora_status_t dispatch_one(const lora_batch_t *b, int32_t dtype, int mode, int32_t path, int d_in, DeltaArgs &p,
                            cudaStream_t stream) {
@@ -252,17 +285,18 @@ lora_status_t dispatch_one(const lora_batch_t *b, int32_t dtype, int mode, int32
     // With kStreamSplitTc set, LORA_PATH_AUTO gives the long groups to the
     // tensor-core kernel instead.
     if (p.b_rank_major) {
-        // rank-major B pools: the streaming kernel only
+        // rank-major B pools: the streaming kernel only (batches above its
+        // row limit as consecutive launches over row ranges)
+        int n_launched = 0;
         if (mode == kFused && dtype == LORA_BF16 && (path == LORA_PATH_AUTO || path == LORA_PATH_CUDA_CORE) &&
-            try_launch_stream(p, sms, stream, &e)) {
+            try_launch_stream_ranges(p, sms, stream, &e, &n_launched)) {
+            launch_counter().fetch_add(n_launched, std::memory_order_relaxed);
             if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
-            launch_counter().fetch_add(1, std::memory_order_relaxed);
             g_last_kernels = LORA_KERNEL_STREAM;
             return LORA_OK;
         }
         return fail(LORA_ERR_UNSUPPORTED,
-                    "rank-major B pools run on the streaming kernel only (bf16 lora_delta, at most 2048 rows, "
-                    "r_max 16, 32 or 64)");
+                    "rank-major B pools run on the streaming kernel only (bf16 lora_delta, r_max 16, 32 or 64)");
     }
     if (mode == kFused && dtype == LORA_BF16 && (path == LORA_PATH_AUTO || path == LORA_PATH_CUDA_CORE)) {
         if (b->M <= kSmallAutoRows) {

@@ -505,6 +505,11 @@ RANK_MAJOR_CASES = [
          per_adapter_scale=True),
     dict(M=300, d_in=1024, d_outs=[1024, 256, 256], n_pool=30, r_max=32, ranks=[8, 24, 32], run_len=12),
     dict(M=100, d_in=512, d_outs=[520], n_pool=8, r_max=16, ranks=[3, 16]),
+    # above the streaming kernel's 2048 rows: consecutive launches over row ranges
+    dict(M=4500, d_in=1024, d_outs=[2048], n_pool=40, r_max=32, ranks=[8, 16, 32], skip_frac=0.1,
+         per_adapter_scale=True),
+    dict(M=4096, d_in=512, d_outs=[768, 256], n_pool=16, r_max=16, ranks=[8, 16], run_len=64),
+    dict(M=2049, d_in=256, d_outs=[512], n_pool=6, r_max=64, ranks=[16, 64], run_len=700),
 ]
 
 
@@ -523,7 +528,8 @@ def test_rank_major_b(B, ci):
 
 
 def test_rank_major_b_unsupported_elsewhere(B):
-    w = wl.random_batch(seed=995, M=3000, d_in=256, d_outs=[128], n_pool=8, r_max=16, dtype="bf16")
+    # the streaming kernel computes bf16 only
+    w = wl.random_batch(seed=995, M=3000, d_in=256, d_outs=[128], n_pool=8, r_max=16, dtype="f32")
     d = to_dev(w)
     batch = B.lora_prepare_batch(d["ids"], w.n_adapters, 0)
     with pytest.raises(B.LoraError) as e:
