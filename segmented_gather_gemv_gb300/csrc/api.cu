@@ -441,9 +441,20 @@ lora_status_t dispatch(const lora_batch_t *b, int32_t dtype, int mode, int32_t p
         p.stacked = 1;
         p.max_len = 0x7fffffff;
         cudaError_t e = cudaSuccess;
-        if (try_launch_stream(p, sm_count(), stream, &e)) {
+        // rank-major pools run on the streaming kernel alone, so a larger
+        // batch takes it over row ranges (one stacked shrink per range)
+        // rather than one pass per slice
+        int n_launched = 0;
+        bool taken;
+        if (p.b_rank_major) {
+            taken = try_launch_stream_ranges(p, sm_count(), stream, &e, &n_launched);
+        } else {
+            taken = try_launch_stream(p, sm_count(), stream, &e);
+            n_launched = taken && e == cudaSuccess ? 1 : 0;
+        }
+        if (taken) {
+            launch_counter().fetch_add(n_launched, std::memory_order_relaxed);
             if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
-            launch_counter().fetch_add(1, std::memory_order_relaxed);
             g_last_kernels = LORA_KERNEL_STREAM;
             return LORA_OK;
         }

@@ -500,6 +500,33 @@ def test_per_slice_a(B, ci):
 
 # ----------------------------------------- rank-major B pools [n][r][d_out]
 
+# per-slice A pools with rank-major B: the stacked shrink, in one launch and
+# (above 2048 rows) over consecutive row ranges
+@pytest.mark.parametrize("M", [1000, 4200])
+def test_per_slice_a_rank_major(B, M):
+    w = wl.random_batch(seed=986 + M, dtype="bf16", M=M, d_in=512, d_outs=[512, 128, 128], n_pool=24, r_max=16,
+                        ranks=[8, 16], run_len=30, skip_frac=0.05, per_adapter_scale=True)
+    rng = np.random.default_rng(987)
+    A_pools = [w.A] + [wl.round_bf16((rng.standard_normal(w.A.shape) / np.sqrt(w.A.shape[2])).astype(np.float32))
+                       for _ in w.B[1:]]
+    d = to_dev(w)
+    A_dev = [torch.from_numpy(a).to(device="cuda", dtype=torch.bfloat16) for a in A_pools]
+    Bt = [b.transpose(1, 2).contiguous() for b in d["B"]]  # (n, r_max, d_out)
+    batch = B.lora_prepare_batch(d["ids"], w.n_adapters, 0)
+    y = d["y"].clone()
+    B.lora_delta(batch, d["x"], A_dev, Bt, y, scale=w.scale, adapter_scale=d["adapter_scale"],
+                 ranks=d["ranks"], b_rank_major=True)
+    assert B.lora_last_kernels() == B.KERNEL_STREAM
+    torch.cuda.synchronize()
+    yg = y.float().cpu().numpy().astype(np.float64)
+    ref = oracle.delta(w.x, w.ids, A_pools, w.B, w.y, scale=w.scale, adapter_scale=w.adapter_scale,
+                       ranks=w.ranks)
+    act = active_rows(w)
+    assert rel_err(yg, ref, w.y.astype(np.float64), act) <= TOL["bf16"]
+    assert np.array_equal(yg[~act], w.y[~act].astype(np.float64))
+    assert batch.counts()["device_error"] == 0
+
+
 RANK_MAJOR_CASES = [
     dict(M=512, d_in=4096, d_outs=[14336], n_pool=100, r_max=64, ranks=[8, 16, 32, 64], skip_frac=0.25,
          per_adapter_scale=True),
