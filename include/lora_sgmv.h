@@ -392,7 +392,9 @@ lora_status_t lora_expand(const lora_batch_t *batch, int32_t dtype,
  * above that the streaming kernel (r_max 16, 32 or 64, d_in a multiple of
  * 64 per cluster CTA, min(M, n_adapters) <= 2048), whose
  * tiles stream through a ring of TMA copies.  A batch neither takes runs on
- * the kernels of larger batches.  These kernels read ids, the A and B pools,
+ * the kernels of larger batches.  Rank-major B pools run on the streaming
+ * kernel at every batch size: above 2048 rows as consecutive launches over
+ * 2048-row ranges, each grouping its own rows.  These kernels read ids, the A and B pools,
  * ranks and adapter_scale before they wait for the kernels ahead of them in
  * the stream (programmatic dependent launch): those must be final before the
  * kernel preceding this call starts (adapter weights loaded earlier, ids from
